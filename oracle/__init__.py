@@ -1,0 +1,10 @@
+"""CPU oracle (test infrastructure only; see ``oracle.attention``)."""
+from .attention import (  # noqa: F401
+    backward,
+    causal_mask,
+    credited_flops,
+    forward,
+    head_backward,
+    head_forward,
+    preprocess_D,
+)
