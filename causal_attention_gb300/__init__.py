@@ -1,0 +1,158 @@
+"""Python binding of libattn.so: fused causal attention forward/backward on GB300.
+
+Argument marshalling only. Every step of the computation runs in the library's CUDA
+kernels; PyTorch supplies device memory and streams. If the library has not been
+built (``python -m causal_attention_gb300.build``) importing this package raises.
+
+The functions named like the C ABI (``attn_fwd``, ``attn_bwd``, ...) take torch
+tensors and pass their device pointers; ``forward``/``backward`` allocate outputs;
+``CausalAttention`` wraps both as a ``torch.autograd.Function``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from ._lib import load_library, ATTN_OK, AttnError, STATUS_NAMES  # noqa: F401
+
+_dll = load_library()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check(status, what):
+    if status != ATTN_OK:
+        raise AttnError(status, what, _dll.attn_last_cuda_error().decode())
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected a [B, H, T, d] tensor")
+    return tuple(int(x) for x in q.shape)
+
+
+def _need(t, name, dtype):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+
+
+def abi_version() -> int:
+    return _dll.attn_abi_version()
+
+
+def attn_bwd_workspace_size(B, H, T, d) -> int:
+    return int(_dll.attn_bwd_workspace_size(B, H, T, d))
+
+
+def attn_fwd(q, k, v, o, lse, scale, causal=True, stream=None):
+    """O = softmax(Q K^T * scale [causal]) V and the natural-log LSE, in place."""
+    B, H, T, d = _shape(q)
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _need(t, n, torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    _check(_dll.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, d,
+                         ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_fwd")
+
+
+def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal=True, stream=None):
+    """dQ, dK, dV in place (three kernels: preprocess, dK/dV, dQ)."""
+    B, H, T, d = _shape(q)
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, n, torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    _check(_dll.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                         _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         B, H, T, d, ctypes.c_float(scale), int(causal), _stream_handle(stream)),
+           "attn_bwd")
+
+
+def attn_bwd_preprocess(o, do, lse, workspace, stream=None):
+    B, H, T, d = _shape(o)
+    _check(_dll.attn_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), B, H, T, d,
+                                    _stream_handle(stream)), "attn_bwd_preprocess")
+
+
+def attn_bwd_dkdv(q, k, v, do, dk, dv, workspace, scale, causal=True, stream=None):
+    B, H, T, d = _shape(q)
+    _check(_dll.attn_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), B, H, T, d,
+                              ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_bwd_dkdv")
+
+
+def attn_bwd_dq(q, k, v, do, dq, workspace, scale, causal=True, stream=None):
+    B, H, T, d = _shape(q)
+    _check(_dll.attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), B, H, T, d,
+                            ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_bwd_dq")
+
+
+def check_device_error(stream=None):
+    """Synchronises the stream and raises AttnError if a kernel's bounded wait expired."""
+    _check(_dll.attn_check_device_error(_stream_handle(stream)), "attn_check_device_error")
+
+
+def new_workspace(B, H, T, d, device=None):
+    n = attn_bwd_workspace_size(B, H, T, d)
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return torch.empty(n // 4, dtype=torch.float32, device=device or "cuda")
+
+
+def forward(q, k, v, scale=None, causal=True, stream=None):
+    """Allocates and returns (O, LSE)."""
+    B, H, T, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, do, lse, scale=None, causal=True, stream=None, workspace=None):
+    """Allocates and returns (dQ, dK, dV)."""
+    B, H, T, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = new_workspace(B, H, T, d, q.device)
+    attn_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
+    return dq, dk, dv
+
+
+class CausalAttention(torch.autograd.Function):
+    """softmax(Q K^T * scale [causal]) V with the library's fused backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale=None, causal=True):
+        q, k, v = (t.contiguous() for t in (q, k, v))
+        o, lse = forward(q, k, v, scale, causal)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale, ctx.causal = scale, causal
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = backward(q, k, v, o, do.contiguous().to(torch.bfloat16), lse, ctx.scale, ctx.causal)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, scale=None, causal=True):
+    return CausalAttention.apply(q, k, v, scale, causal)

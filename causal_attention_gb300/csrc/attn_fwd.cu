@@ -1,0 +1,361 @@
+// Fused causal attention forward for sm_103a: tcgen05 MMAs into tensor memory,
+// TMA-staged K/V ring, warp-specialised roles, online softmax with exp2.
+//
+// Computes, per (batch, head) and query row i (Forge RESEARCH.md, section 6
+// "Fused attention design (flash-style)"):
+//   S = Q K^T * scale, causal mask (key j visible iff j <= i), online softmax
+//   m_new = max(m, rowmax S), P = exp2((S - m_new) * scale * log2 e),
+//   l = l * corr + rowsum P, O = O * corr + P V, and at the end O /= l and the
+//   per-row logsumexp L = m * scale + ln l (natural log).
+//
+// CTA = two 128-row query tiles (Q0 = tile 2t, Q1 = tile 2t+1) of one (b, h).
+//   warps 0-3  softmax for Q0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax for Q1
+//   warp  8    TMA producer (Q once; K_j, V_j through a STAGES-deep ring)
+//   warp  9    TMEM allocator and MMA issuer (one thread)
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 and O1 from 256;
+// P_q is written as packed bf16 over the first 64 columns of S_q and read back by
+// the PV MMA straight from tensor memory (A operand in TMEM).
+// The MMA issue order S0_{j+1} after PV0_j and S1_{j+1} after PV1_j lets one
+// tile's softmax run while the tensor core works on the other tile.
+// Output rescaling is conditional: the running max is only moved when it grows by
+// more than 2^8 in exp2 units, so most blocks skip touching O.
+#include "kernels.h"
+#include "tile.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  using TL = Tile<D>;
+  static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TL::BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * TL::BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * TL::BYTES;
+  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2],
+  // p_full[2], o_final[2], drain
+  static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out,
+                    float* __restrict__ lse_out, int T, int BH, int n_pairs, float scale,
+                    float scale_log2, uint32_t* __restrict__ err) {
+  using C = FwdCfg<D>;
+  using TL = Tile<D>;
+  constexpr int ST = C::STAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t sQ = base + C::OFF_Q;
+  const uint32_t sK = base + C::OFF_K;
+  const uint32_t sV = base + C::OFF_V;
+  const uint32_t bar0 = base + C::OFF_BAR;
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + ST + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + 2 * ST + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * ST + s); };
+  auto s_full = [&](int q) { return bar0 + 8u * (1 + 4 * ST + q); };
+  auto p_full = [&](int q) { return bar0 + 8u * (3 + 4 * ST + q); };
+  auto o_final = [&](int q) { return bar0 + 8u * (5 + 4 * ST + q); };
+  const uint32_t drain = bar0 + 8u * (7 + 4 * ST);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+  const Abort ab{abort, err};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // work item: longest query-tile pairs first
+  const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int nkv = (T + kTileRows - 1) / kTileRows;
+  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  const int nb0 = CAUSAL ? min(qt0 + 1, nkv) : nkv;
+  const int nb1 = CAUSAL ? min(qt1 + 1, nkv) : nkv;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(s_full(q), 1);
+      mbar_init(p_full(q), 128);
+      mbar_init(o_final(q), 1);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, 2 * TL::BYTES);
+      TL::load(sQ, &tmQ, qt0 * kTileRows, bh, q_full);
+      TL::load(sQ + TL::BYTES, &tmQ, qt1 * kTileRows, bh, q_full);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nb1 && ok; ++j) {
+        const int s = j % ST, n = j / ST;
+        if (j >= ST) ok = mbar_wait(k_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad);
+        if (!ok) break;
+        mbar_arrive_expect_tx(k_full(s), TL::BYTES);
+        TL::load(sK + s * TL::BYTES, &tmK, j * kTileRows, bh, k_full(s));
+        if (j >= ST) ok = mbar_wait(v_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad);
+        if (!ok) {
+          issued = j + 1;  // K_j is in flight, V_j is not
+          mbar_wait_drain(k_full(s), n & 1, ab);
+          break;
+        }
+        mbar_arrive_expect_tx(v_full(s), TL::BYTES);
+        TL::load(sV + s * TL::BYTES, &tmV, j * kTileRows, bh, v_full(s));
+        issued = j + 1;
+      }
+      if (!ok) {
+        // drain: every copy issued must land before the CTA exits
+        mbar_wait_drain(q_full, 0, ab);
+        for (int j = max(0, issued - ST); j < issued; ++j) {
+          const int s = j % ST, n = j / ST;
+          mbar_wait_drain(k_full(s), n & 1, ab);
+          mbar_wait_drain(v_full(s), n & 1, ab);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
+      auto issue_S = [&](int q, int s) {
+        const uint32_t a = sQ + q * TL::BYTES, b = sK + s * TL::BYTES;
+#pragma unroll
+        for (int k = 0; k < TL::KSTEPS_D; ++k)
+          mma_ss(tS[q], TL::desc_kmajor(a, k), TL::desc_kmajor(b, k), idesc_s, k > 0 ? 1u : 0u);
+      };
+      auto issue_PV = [&](int q, int s, bool acc) {
+        const uint32_t b = sV + s * TL::BYTES;
+#pragma unroll
+        for (int k = 0; k < kTileRows / 16; ++k)
+          mma_ts(tO[q], tS[q] + 8u * k, TL::desc_mnmajor(b, k), idesc_pv, (acc || k > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(q_full, 0, ab, kErrTimeoutMma) &&
+                mbar_wait(k_full(0), 0, ab, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0, 0);
+        mma_commit(s_full(0));
+        issue_S(1, 0);
+        mma_commit(s_full(1));
+        mma_commit(k_empty(0));
+      }
+      for (int j = 0; j < nb1 && ok; ++j) {
+        const int s = j % ST, n = j / ST;
+        const int jn = j + 1, sn = jn % ST, nn = jn / ST;
+        if (!(ok = mbar_wait(v_full(s), n & 1, ab, kErrTimeoutMma))) break;
+        bool k_next = false;
+        if (j < nb0) {
+          if (!(ok = mbar_wait(p_full(0), j & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          issue_PV(0, s, j > 0);
+          if (jn < nb0) {
+            if (!(ok = mbar_wait(k_full(sn), nn & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            k_next = true;
+            issue_S(0, sn);
+            mma_commit(s_full(0));
+          } else {
+            mma_commit(o_final(0));
+          }
+        }
+        if (!(ok = mbar_wait(p_full(1), j & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        issue_PV(1, s, j > 0);
+        mma_commit(v_empty(s));
+        if (jn < nb1) {
+          if (!k_next) {
+            if (!(ok = mbar_wait(k_full(sn), nn & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+          }
+          issue_S(1, sn);
+          mma_commit(s_full(1));
+          mma_commit(k_empty(sn));
+        } else {
+          mma_commit(o_final(1));
+        }
+      }
+      if (!ok) {
+        mma_commit(drain);  // completes once every MMA issued so far is done
+        mbar_wait_drain(drain, 0, ab);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int q = warp >> 2;  // 0 or 1
+    const int r = threadIdx.x & 127;
+    const int qt = q ? qt1 : qt0;
+    const int nb = q ? nb1 : nb0;
+    const int row = qt * kTileRows + r;
+    const uint32_t lane_off = warp_lane_base();
+    const uint32_t tS = tmem + lane_off + (q ? 128u : 0u);
+    const uint32_t tO = tmem + lane_off + 256u + (q ? (uint32_t)D : 0u);
+
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      if (!(ok = mbar_wait_warp(s_full(q), j & 1, ab, kErrTimeoutElem))) break;
+      tc_fence_after();
+      float x[128];
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          tmem_ld32(tS + 32u * cb, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[32 * cb + i] = __uint_as_float(u[i]);
+        }
+      }
+      if (CAUSAL && j == qt) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > r) x[c] = -INFINITY;
+      }
+      if (!CAUSAL && (j + 1) * kTileRows > T) {
+        const int lim = T - j * kTileRows;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) x[c] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      float corr = 1.f;
+      if (j == 0) {
+        m = mx;
+      } else {
+        const float m_new = fmaxf(m, mx);
+        const bool need = (m_new - m) * scale_log2 > kRescaleThreshold;
+        if (need) {
+          corr = ex2((m - m_new) * scale_log2);
+          m = m_new;
+        }
+        if (__any_sync(0xffffffffu, need)) {
+          // O_q holds the sum through block j-1 (its PV completed before S_q,j did)
+#pragma unroll
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t u[32];
+            tmem_ld32(tO + 32u * cb, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
+            tmem_st32(tO + 32u * cb, u);
+          }
+        }
+      }
+      const float mc = m * scale_log2;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float p = ex2(fmaf(x[c], scale_log2, -mc));
+        sum += p;
+        x[c] = p;
+      }
+      l = l * corr + sum;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t u[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u[i] = pack_bf16(x[32 * cb + 2 * i], x[32 * cb + 2 * i + 1]);
+        tmem_st16(tS + 16u * cb, u);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full(q));
+    }
+    if (ok && mbar_wait_warp(o_final(q), 0, ab, kErrTimeoutElem)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = out + ((size_t)bh * T + row) * D;
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t u[32];
+        tmem_ld32(tO + 32u * cb, u);
+        tmem_wait_ld();
+        uint4 pk[4];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pw[i] = pack_bf16(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+        if (row < T) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cb);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+        }
+      }
+      if (row < T) lse_out[(size_t)bh * T + row] = (m * scale_log2 + __log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  static uint32_t configured = 0;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
+  if (e != cudaSuccess) return e;
+  const int n_pairs = (a.T + 2 * kTileRows - 1) / (2 * kTileRows);
+  dim3 grid(n_pairs * a.BH), block(kFwdThreads);
+  kern<<<grid, block, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.o, a.lse, a.T, a.BH, n_pairs,
+                                               a.scale, a.scale * 1.4426950408889634f, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 32: return a.causal ? launch<32, true>(a, stream) : launch<32, false>(a, stream);
+    case 64: return a.causal ? launch<64, true>(a, stream) : launch<64, false>(a, stream);
+    case 128: return a.causal ? launch<128, true>(a, stream) : launch<128, false>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace attn

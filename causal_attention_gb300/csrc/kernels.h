@@ -1,0 +1,53 @@
+// Host-side launch interface between the C-ABI layer and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace attn {
+
+struct FwdArgs {
+  const CUtensorMap* tmQ;  // 3-D maps over [B*H, T, d] bf16, 128-row boxes
+  const CUtensorMap* tmK;
+  const CUtensorMap* tmV;
+  __nv_bfloat16* o;
+  float* lse;
+  int T, BH, d, causal;
+  float scale;
+  uint32_t* err;  // device error word
+};
+
+// Workspace of the backward: two fp32 arrays of [B*H, T_pad], T_pad = T rounded
+// up to 128. ws_lse2 = LSE * log2(e) (+inf on padding rows), ws_D = rowsum(dO*O)
+// (0 on padding rows).
+struct BwdArgs {
+  const CUtensorMap* tmQ;
+  const CUtensorMap* tmK;
+  const CUtensorMap* tmV;
+  const CUtensorMap* tmdO;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dO;
+  const float* lse;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* ws_lse2;
+  float* ws_D;
+  int T, T_pad, BH, d, causal;
+  float scale;
+  uint32_t* err;  // device error word
+};
+
+inline int pad_rows(int T) { return (T + 127) / 128 * 128; }
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
+
+// Sets the max dynamic shared memory of a kernel once per device.
+cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask);
+
+}  // namespace attn

@@ -1,0 +1,126 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) fused causal attention library.
+ *
+ * The library computes multi-head attention with an optional causal mask, forward
+ * and backward, for bf16 inputs with fp32 accumulation, on one GPU. Definitions
+ * (Forge RESEARCH.md, section 6 "Fused attention design (flash-style)", and the
+ * Forge paper, sections "Attention kernel design" and "Ecosystem survey"):
+ *
+ *   forward   S = Q K^T * scale;  key j is visible to query i iff j <= i (causal);
+ *             P = softmax(S) over visible keys;  O = P V;
+ *             LSE_i = log sum_j exp(S_ij)   (natural log, saved for the backward)
+ *   backward  D = rowsum(dO * O);  P = exp(S - LSE);  dV = P^T dO;  dP = dO V^T;
+ *             dS = P * (dP - D);  dQ = dS K * scale;  dK = dS^T Q * scale
+ *
+ * Layout and types. Every matrix argument is a contiguous row-major device
+ * tensor [B, H, T, d] of bf16 (16-bit brain floats): element (b, h, t, c) is at
+ * offset ((b*H + h)*T + t)*d + c. LSE is fp32 [B, H, T]. Pointers must be device
+ * (or managed) memory visible to the current CUDA device and 16-byte aligned.
+ *
+ * Ownership. The caller allocates and owns every buffer, including the backward's
+ * workspace. The library allocates no device memory and keeps no per-call state
+ * beyond a cached function pointer of the CUDA driver.
+ *
+ * Execution. Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and does not synchronise the host. Outputs are fully
+ * overwritten. Results are bitwise deterministic run to run (no atomics).
+ *
+ * Errors. Arguments are checked before anything is launched; an invalid call
+ * returns a status and launches nothing. Kernel waits are bounded: if one expires
+ * the kernel records it in a device error word and returns early (its outputs are
+ * then undefined); attn_check_device_error() reports and clears that word.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,     /* null pointer, B/H/T < 1, bad scale or causal flag, sizes too large */
+  ATTN_ERR_UNSUPPORTED = 2,     /* head dimension d not in {32, 64, 128} */
+  ATTN_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned */
+  ATTN_ERR_WORKSPACE = 4,       /* workspace missing or smaller than attn_bwd_workspace_size() */
+  ATTN_ERR_LAUNCH = 5,          /* the CUDA runtime rejected a launch (see attn_last_cuda_error) */
+  ATTN_ERR_DEVICE_TIMEOUT = 6,  /* a kernel's bounded wait expired (attn_check_device_error) */
+  ATTN_ERR_CUDA = 7             /* another CUDA runtime or driver call failed */
+} attn_status;
+
+/* ABI version of the loaded library (ATTN_ABI_VERSION at build time). */
+int attn_abi_version(void);
+
+/*
+ * Forward. Cited definition: Forge RESEARCH.md section 6, the online-softmax
+ * algorithm and "L = m + log(l) (one f32/row, saved for backward)".
+ *   q, k, v : bf16 [B, H, T, d] inputs
+ *   o       : bf16 [B, H, T, d] output, O = softmax(Q K^T * scale) V
+ *   lse     : fp32 [B, H, T] output, natural-log logsumexp of the scaled scores
+ *   scale   : finite, > 0 (typically 1/sqrt(d));  causal: 1 masks keys j > i, 0 none
+ * One kernel launch.
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int T, int d, float scale, int causal, void* stream);
+
+/* Bytes of device workspace attn_bwd (and its stages) need: two fp32 arrays of
+ * B*H*T_pad entries, T_pad = T rounded up to a multiple of 128. 0 if the sizes
+ * are invalid. */
+size_t attn_bwd_workspace_size(int B, int H, int T, int d);
+
+/*
+ * Backward. Cited definition: Forge RESEARCH.md section 6, "The D term is free"
+ * and "Backward (training)"; the three-stage atomic-free structure of the Forge
+ * paper's "Ecosystem survey". Equivalent to attn_bwd_preprocess, then
+ * attn_bwd_dkdv, then attn_bwd_dq, on the same stream.
+ *   q, k, v, o, dO : bf16 [B, H, T, d] (o and lse as written by attn_fwd)
+ *   lse            : fp32 [B, H, T]
+ *   dq, dk, dv     : bf16 [B, H, T, d] outputs
+ *   workspace      : >= attn_bwd_workspace_size(B, H, T, d) bytes of device memory,
+ *                    16-byte aligned; its contents on entry do not matter
+ * Three kernel launches.
+ */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int B, int H, int T, int d, float scale, int causal,
+                     void* stream);
+
+/* Backward stage 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace
+ * (Forge RESEARCH.md section 6, "The D term is free"). Memory-bound. */
+attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
+                                size_t workspace_bytes, int B, int H, int T, int d, void* stream);
+
+/* Backward stage 2: dK and dV, one CTA per 128-key tile looping over query tiles
+ * (Forge paper, "Attention kernel design": transposes by operand-role swap).
+ * Reads the workspace written by stage 1. */
+attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                          void* dv, const void* workspace, size_t workspace_bytes, int B, int H,
+                          int T, int d, float scale, int causal, void* stream);
+
+/* Backward stage 3: dQ, one CTA per 128-query tile looping over key tiles
+ * (deterministic; Forge RESEARCH.md section 6, "a dQ kernel with grid (NQ, H, B)").
+ * Reads the workspace written by stage 1. */
+attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                        const void* workspace, size_t workspace_bytes, int B, int H, int T, int d,
+                        float scale, int causal, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device. Returns ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait
+ * expired since the last check, ATTN_ERR_CUDA if the synchronisation failed. */
+attn_status attn_check_device_error(void* stream);
+
+/* Static description of a status code. */
+const char* attn_status_string(attn_status status);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char* attn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -1,0 +1,99 @@
+"""The C-ABI library on the host: it loads without a GPU, exports every function
+that include/attn.h declares, and rejects invalid calls before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from causal_attention_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        import causal_attention_gb300.build as b
+        b.build()
+    return _lib.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(attn_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
+              "attn_bwd_dq", "attn_check_device_error", "attn_status_string", "attn_abi_version"):
+        assert n in names
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with attn.h"
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_abi_version(lib):
+    assert lib.attn_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.attn_status_string(code)
+    assert b"unknown" in lib.attn_status_string(99)
+
+
+def test_workspace_size(lib):
+    assert lib.attn_bwd_workspace_size(2, 3, 200, 64) == 2 * 4 * 2 * 3 * 256
+    assert lib.attn_bwd_workspace_size(1, 1, 128, 128) == 2 * 4 * 128
+    assert lib.attn_bwd_workspace_size(0, 1, 128, 64) == 0
+    assert lib.attn_bwd_workspace_size(1, 1, 128, 48) == 0
+
+
+P = 0x10000  # a fake, 16-byte aligned address: never dereferenced when a check fails first
+
+
+def fwd(lib, B=1, H=1, T=64, d=64, scale=0.125, causal=1, ptrs=(P, P, P, P, P)):
+    return lib.attn_fwd(*[ctypes.c_void_p(p) for p in ptrs], B, H, T, d, ctypes.c_float(scale), causal,
+                        ctypes.c_void_p(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(T=0), 1), (dict(T=1 << 25), 1),
+    (dict(d=48), 2), (dict(d=256), 2), (dict(d=80), 2),
+    (dict(scale=0.0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1), (dict(scale=-1.0), 1),
+    (dict(causal=2), 1),
+    (dict(ptrs=(0, P, P, P, P)), 1), (dict(ptrs=(P, P, P, P, 0)), 1),
+    (dict(ptrs=(P + 8, P, P, P, P)), 3), (dict(ptrs=(P, P, P, P + 4, P)), 3),
+])
+def test_fwd_rejects_invalid_calls(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+def test_bwd_rejects_invalid_calls(lib):
+    v = [ctypes.c_void_p(P)] * 9
+    ws = lib.attn_bwd_workspace_size(1, 1, 64, 64)
+    args = lambda wsp, wsb, d=64: (*v, ctypes.c_void_p(wsp), wsb, 1, 1, 64, d, ctypes.c_float(0.125), 1,
+                                   ctypes.c_void_p(0))
+    assert lib.attn_bwd(*args(0, ws)) == 4            # no workspace
+    assert lib.attn_bwd(*args(P, ws - 16)) == 4       # too small
+    assert lib.attn_bwd(*args(P + 4, ws)) == 3        # misaligned workspace
+    assert lib.attn_bwd(*args(P, ws, d=40)) == 2
+    assert lib.attn_bwd_preprocess(ctypes.c_void_p(P), ctypes.c_void_p(P), ctypes.c_void_p(P),
+                                   ctypes.c_void_p(P), ws - 1, 1, 1, 64, 64, ctypes.c_void_p(0)) == 4
+
+
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    """With no CUDA device the checks pass and the first CUDA call reports an error."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd(lib) == 7
+    assert lib.attn_last_cuda_error()
