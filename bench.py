@@ -1,0 +1,378 @@
+"""Throughput of the fused causal attention forward + backward on GB300.
+
+One step = attn_fwd followed by attn_bwd (preprocess, dK/dV, dQ) over one batch of
+the workload, through the C ABI. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+* value: credited causal TFLOP/s of the whole job (forward 2*B*H*T^2*d, backward
+  2.5x that), inputs resident in HBM; inputs rotate over several buffer sets whose
+  total size exceeds L2 three times, so no step reads another's operands from L2.
+* e2e: the same metric through the public API with pinned host buffers: every step
+  copies Q, K, V, dO host->device and O, LSE, dQ, dK, dV device->host.
+* roofline: the kernel with the largest share of step time, its algorithmic FLOPs
+  per launch over its mean CUDA-event duration, against the measured bf16 peak.
+* cpu_baseline: the CPU oracle timed on this host on a bounded sample (a few heads
+  of the same workload), as it stands.
+* --impl reference: the CPU oracle as the reference arm (the pages publish no code
+  that runs here), each step a bounded sample of the workload.
+
+Multi-GPU: one process per GPU under torchrun; every rank runs its own replica of the
+workload (independent problems, no collective on the data path), "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="gpt205m")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops", 1900.0), d.get("hbm_gbs", 6800.0), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def oracle_sample(w, n_heads, x=None):
+    """Runs the CPU oracle fwd + bwd on n_heads heads; returns (credited FLOPs, seconds)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    import seeded_inputs as si
+    x = x or si.make_inputs(w)
+    heads = [(i // w.H % w.B, i % w.H) for i in range(n_heads)]
+    q, k, v, do = (si.bf16_bits_to_f64(x[n]) for n in ("q", "k", "v", "do"))
+    t0 = time.perf_counter()
+    for b, h in heads:
+        oracle.head_forward(q[b, h], k[b, h], v[b, h], w.scale, w.causal)
+        oracle.head_backward(q[b, h], k[b, h], v[b, h], do[b, h], w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    fwd, bwd = oracle.credited_flops(1, 1, w.T, w.d)
+    return (fwd + bwd) * n_heads, dt
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step a bounded sample (one head)."""
+    import seeded_inputs as si
+    w = si.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    x = si.make_inputs(w)
+    heads_per_step = 1
+    for _ in range(args.warmup if w.T <= 2048 else 0):
+        oracle_sample(w, heads_per_step, x)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, s = oracle_sample(w, heads_per_step, x)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": "causal attention fwd+bwd TFLOP/s (bf16) and % of GB300 dense BF16 peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "causal": w.causal,
+                   "parallelism": "replicas", "sample": f"{heads_per_step} head(s) per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"{heads_per_step} head of {w.B * w.H} per step, fp64 numpy oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
+
+
+def kernel_flops(w):
+    """Algorithmic FLOPs per launch of each kernel (causal half of every T x T GEMM)."""
+    g = w.B * w.H * w.T * w.T * w.d * (1.0 if w.causal else 2.0)  # one causal GEMM = B*H*T^2*d
+    return {"fwd": 2 * g, "bwd_dkdv": 4 * g, "bwd_dq": 3 * g}
+
+
+def kernel_bytes(w):
+    n = w.B * w.H * w.T
+    return {"bwd_preprocess": 2 * n * w.d * 2 + 4 * n + 8 * n}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    import causal_attention_gb300 as ca
+    import oracle
+    import seeded_inputs as si
+    from tests.gpu_util import to_device
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = si.WORKLOADS[args.workload]
+    # each rank: its own replica of the workload (different seed, same shape)
+    wr = w.with_(seed=w.seed + 1000 * rank)
+    x = si.make_inputs(wr)
+    B, H, T, d = wr.shape
+    scale, causal = wr.scale, wr.causal
+    dev = torch.device("cuda", local)
+
+    per_set = 8 * B * H * T * d * 2 + 3 * B * H * T * 4
+    n_sets = max(2, -(-3 * L2_BYTES // per_set))
+    base = {n: to_device(x[n]) for n in ("q", "k", "v", "do")}
+    sets = []
+    for i in range(n_sets):
+        s = {n: base[n].clone() for n in base}
+        s["o"] = torch.empty_like(s["q"])
+        s["lse"] = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        s["dq"], s["dk"], s["dv"] = (torch.empty_like(s["q"]) for _ in range(3))
+        s["ws"] = ca.new_workspace(B, H, T, d, dev)
+        sets.append(s)
+    stream = torch.cuda.current_stream()
+
+    def step(s, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ca.attn_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], scale, causal, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ca.attn_bwd_preprocess(s["o"], s["do"], s["lse"], s["ws"], stream)
+        if ev is not None:
+            ev[2].record(stream)
+        ca.attn_bwd_dkdv(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"], scale, causal, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        ca.attn_bwd_dq(s["q"], s["k"], s["v"], s["do"], s["dq"], s["ws"], scale, causal, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for i in range(max(3, args.warmup)):
+        step(sets[i % n_sets])
+    ca.check_device_error(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(sets[i % n_sets], evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ca.check_device_error(stream)
+    elapsed_ms = t_start.elapsed_time(t_end)
+
+    per_kernel = {k: [] for k in KERNELS}
+    for ev in evs:
+        for j, k in enumerate(KERNELS):
+            per_kernel[k].append(ev[j].elapsed_time(ev[j + 1]))
+    mean_ms = {k: statistics.fmean(v) for k, v in per_kernel.items()}
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    fwd_f, bwd_f = oracle.credited_flops(B, H, T, d)
+    step_flops = (fwd_f + bwd_f) * (1.0 if causal else 2.0)
+    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+
+    # ------------------------------------------------------------------ e2e
+    pinned = {n: torch.from_numpy(x[n].view("int16")).view(torch.bfloat16).pin_memory() for n in ("q", "k", "v", "do")}
+    outs_h = {n: torch.empty((B, H, T, d), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
+    outs_h["lse"] = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
+    s0 = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+
+    def e2e_step():
+        for n in ("q", "k", "v", "do"):
+            s0[n].copy_(pinned[n], non_blocking=True)
+        ca.attn_fwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["lse"], scale, causal, stream)
+        ca.attn_bwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["do"], s0["lse"], s0["dq"], s0["dk"], s0["dv"],
+                    s0["ws"], scale, causal, stream)
+        for n in ("o", "lse", "dq", "dk", "dv"):
+            outs_h[n].copy_(s0[n], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    ca.check_device_error(stream)
+    e2e_value = step_flops * args.e2e_steps * world / e2e_s / 1e12
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    # ------------------------------------------------------------------ roofline
+    peak_tf, peak_gbs, peak_kind = load_peaks()
+    kf = kernel_flops(wr)
+    top = max(kf, key=lambda k: mean_ms[k])
+    achieved = kf[top] / (mean_ms[top] * 1e-3) / 1e12
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        tj = json.load(open(prof))
+        traffic = tj.get(f"{wr.name}:{top}")
+    roofline = {"bound": "tensor", "kernel": f"attn_{top}", "achieved": round(achieved, 2), "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": traffic,
+                "peak_kind": f"bf16 dense burst, {peak_kind}"}
+    kernels = {}
+    for k in KERNELS:
+        e = {"ms": round(mean_ms[k], 5), "share": round(mean_ms[k] / sum(mean_ms.values()), 4)}
+        if k in kf:
+            tf = kf[k] / (mean_ms[k] * 1e-3) / 1e12
+            e.update(tflops=round(tf, 2), frac=round(tf / peak_tf, 4))
+        else:
+            gbs = kernel_bytes(wr)[k] / (mean_ms[k] * 1e-3) / 1e9
+            e.update(gbs=round(gbs, 1), frac=round(gbs / peak_gbs, 4))
+        kernels[k] = e
+    fwd_tf = fwd_f * (1.0 if causal else 2.0) / (mean_ms["fwd"] * 1e-3) / 1e12
+    bwd_ms = mean_ms["bwd_preprocess"] + mean_ms["bwd_dkdv"] + mean_ms["bwd_dq"]
+    bwd_tf = bwd_f * (1.0 if causal else 2.0) / (bwd_ms * 1e-3) / 1e12
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_heads = 2 if T >= 4096 else (4 if T >= 2048 else 16)
+        f, s = oracle_sample(wr, n_heads, x)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n_heads} of {B * H} heads, fwd+bwd, fp64 numpy oracle, {s:.1f} s"}
+
+    line = {
+        "metric": "causal attention fwd+bwd TFLOP/s (bf16) and % of GB300 dense BF16 peak",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wr.name, "B": B, "H": H, "T": T, "d": d, "causal": causal,
+                   "parallelism": f"replicas x{world}", "l2": f"inputs rotate over {n_sets} sets ({n_sets * per_set / 2**20:.0f} MiB > L2)"},
+        "frac_of_peak": round(value / peak_tf, 4),
+        "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
+        "fwd_frac": round(fwd_tf / peak_tf, 4), "bwd_frac": round(bwd_tf / peak_tf, 4),
+        "kernels": kernels,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -281,22 +281,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
+      // P is rounded to bf16 for the PV MMA, and the row sum l adds up exactly those
+      // rounded values, so that O / l is a convex combination of V rows whatever the
+      // rounding (with a peaked softmax the dominant weight's rounding cancels).
       const float mc = m * scale_log2;
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float p = ex2(fmaf(x[c], scale_log2, -mc));
-        sum += p;
-        x[c] = p;
-      }
-      l = l * corr + sum;
+      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t u[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) u[i] = pack_bf16(x[32 * cb + 2 * i], x[32 * cb + 2 * i + 1]);
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(x[32 * cb + 2 * i], scale_log2, -mc));
+          const float p1 = ex2(fmaf(x[32 * cb + 2 * i + 1], scale_log2, -mc));
+          u[i] = pack_bf16(p0, p1);
+          sum0 += __uint_as_float(u[i] << 16);
+          sum1 += __uint_as_float(u[i] & 0xFFFF0000u);
+        }
         tmem_st16(tS + 16u * cb, u);
       }
+      l = l * corr + (sum0 + sum1);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full(q));
