@@ -1,9 +1,11 @@
 """Builds libattn.so (the C-ABI attention library) in-tree for sm_103a.
 
 Each CUDA translation unit is compiled by its own nvcc process (in parallel), then
-linked into ``causal_attention_gb300/lib/libattn.so``. The CUDA runtime is linked
-statically, so the library loads without a GPU driver present (it looks the
-driver up on first use). Run ``python -m causal_attention_gb300.build``.
+linked into ``causal_attention_gb300/lib/libattn.so``. The CUDA runtime is the shared
+``libcudart.so.13``: when PyTorch has loaded its copy first, the library uses that same
+runtime (one current device per thread for both); otherwise the toolkit's copy is found
+through the RPATH. Nothing links libcuda, so the library loads without a GPU driver
+(the driver is looked up on first use). Run ``python -m causal_attention_gb300.build``.
 """
 from __future__ import annotations
 
@@ -55,7 +57,9 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
     if verbose or ptxas_verbose:
         sys.stdout.write(logs)
     tmp = LIB + ".tmp"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *(o for o, _ in results)]
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(cc)), "lib64")
+    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", f"-rpath,{cuda_lib}", "-o", tmp,
+           *(o for o, _ in results)]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

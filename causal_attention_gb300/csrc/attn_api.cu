@@ -26,10 +26,26 @@ attn_status cuda_fail(cudaError_t e, attn_status code) {
 
 constexpr int kMaxDevices = 32;
 
+// Makes the current device's primary context current in this thread (once per
+// thread and device), so that driver calls such as cuTensorMapEncodeTiled work in
+// threads where only the runtime's device was set (e.g. autograd worker threads).
+cudaError_t bind_device() {
+  thread_local int bound = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (bound == dev) return cudaSuccess;
+  e = cudaSetDevice(dev);
+  if (e == cudaSuccess) bound = dev;
+  return e;
+}
+
 uint32_t* error_word_ptr(cudaError_t* e) {
   static uint32_t* ptrs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
+  *e = bind_device();
+  if (*e != cudaSuccess) return nullptr;
   *e = cudaGetDevice(&dev);
   if (*e != cudaSuccess) return nullptr;
   if (dev < 0 || dev >= kMaxDevices) {
@@ -71,7 +87,8 @@ EncodeTiledFn encode_fn(cudaError_t* e) {
 // A 3-D map over a [B*H, T, d] bf16 tensor with 128-row boxes of one swizzle
 // width of columns. Rows past T (and heads past B*H) read as zero.
 attn_status make_map(CUtensorMap* m, const void* ptr, int BH, int T, int d) {
-  cudaError_t e;
+  cudaError_t e = bind_device();
+  if (e != cudaSuccess) return cuda_fail(e, ATTN_ERR_CUDA);
   EncodeTiledFn fn = encode_fn(&e);
   if (!fn) return cuda_fail(e, ATTN_ERR_CUDA);
   const int row_bytes = d * 2 >= 128 ? 128 : d * 2;

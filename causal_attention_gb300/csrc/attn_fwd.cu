@@ -15,7 +15,9 @@
 //   warp  9    TMEM allocator and MMA issuer (one thread)
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 and O1 from 256;
 // P_q is written as packed bf16 over the first 64 columns of S_q and read back by
-// the PV MMA straight from tensor memory (A operand in TMEM).
+// the PV MMA straight from tensor memory (A operand in TMEM). O is normalised by the
+// sum of those rounded P values (so O / l stays a convex combination of V rows
+// whatever the rounding), the logsumexp by the exact fp32 sum.
 // The MMA issue order S0_{j+1} after PV0_j and S1_{j+1} after PV1_j lets one
 // tile's softmax run while the tensor core works on the other tile.
 // Output rescaling is conditional: the running max is only moved when it grows by
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tS = tmem + lane_off + (q ? 128u : 0u);
     const uint32_t tO = tmem + lane_off + 256u + (q ? (uint32_t)D : 0u);
 
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       if (!(ok = mbar_wait_warp(s_full(q), j & 1, ab, kErrTimeoutElem))) break;
@@ -284,8 +286,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // P is rounded to bf16 for the PV MMA, and the row sum l adds up exactly those
       // rounded values, so that O / l is a convex combination of V rows whatever the
       // rounding (with a peaked softmax the dominant weight's rounding cancels).
+      // The LSE uses the exact row sum l; O is divided by lr, the sum of the same
+      // bf16-rounded P values.
       const float mc = m * scale_log2;
-      float sum0 = 0.f, sum1 = 0.f;
+      float se0 = 0.f, se1 = 0.f, sr0 = 0.f, sr1 = 0.f;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t u[16];
@@ -294,19 +298,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float p0 = ex2(fmaf(x[32 * cb + 2 * i], scale_log2, -mc));
           const float p1 = ex2(fmaf(x[32 * cb + 2 * i + 1], scale_log2, -mc));
           u[i] = pack_bf16(p0, p1);
-          sum0 += __uint_as_float(u[i] << 16);
-          sum1 += __uint_as_float(u[i] & 0xFFFF0000u);
+          se0 += p0;
+          se1 += p1;
+          sr0 += __uint_as_float(u[i] << 16);
+          sr1 += __uint_as_float(u[i] & 0xFFFF0000u);
         }
         tmem_st16(tS + 16u * cb, u);
       }
-      l = l * corr + (sum0 + sum1);
+      l = l * corr + (se0 + se1);
+      lr = lr * corr + (sr0 + sr1);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full(q));
     }
     if (ok && mbar_wait_warp(o_final(q), 0, ab, kErrTimeoutElem)) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
       __nv_bfloat16* orow = out + ((size_t)bh * T + row) * D;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
