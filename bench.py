@@ -172,6 +172,22 @@ def run_reference(args, rank, world):
 KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 
 
+def captured_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu capture, if the kernel source is
+    unchanged since the capture (else None)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(prof):
+        return None
+    rec = json.load(open(prof)).get(f"{workload}:{kernel}")
+    if not rec:
+        return None
+    src = open(os.path.join(ROOT, rec["kernel_source"]), "rb").read()
+    if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_prefix"]:
+        return None
+    return rec["bytes_per_launch"]
+
+
 def kernel_flops(w):
     """Algorithmic FLOPs per launch of each kernel (causal half of every T x T GEMM)."""
     g = w.B * w.H * w.T * w.T * w.d * (1.0 if w.causal else 2.0)  # one causal GEMM = B*H*T^2*d
@@ -314,11 +330,7 @@ def run_ours(args, rank, world, local):
     kf = kernel_flops(wr)
     top = max(kf, key=lambda k: mean_ms[k])
     achieved = kf[top] / (mean_ms[top] * 1e-3) / 1e12
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        tj = json.load(open(prof))
-        traffic = tj.get(f"{wr.name}:{top}")
+    traffic = captured_traffic(wr.name, top)
     roofline = {"bound": "tensor", "kernel": f"attn_{top}", "achieved": round(achieved, 2), "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": traffic,
                 "peak_kind": f"bf16 dense burst, {peak_kind}"}
