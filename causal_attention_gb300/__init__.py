@@ -2,7 +2,7 @@
 
 Argument marshalling only. Every step of the computation runs in the library's CUDA
 kernels; PyTorch supplies device memory and streams. If the library has not been
-built (``python -m causal_attention_gb300.build``) importing this package raises.
+built (``python causal_attention_gb300/build.py``) importing this package raises.
 
 The functions named like the C ABI (``attn_fwd``, ``attn_bwd``, ...) take torch
 tensors and pass their device pointers; ``forward``/``backward`` allocate outputs;
@@ -101,6 +101,19 @@ def attn_bwd_dq(q, k, v, do, dq, workspace, scale, causal=True, stream=None):
     _check(_dll.attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), B, H, T, d,
                             ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_bwd_dq")
+
+
+def attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=True, stream=None):
+    """attn_bwd without a workspace: the library's fixed 8 MiB device scratch is used
+    instead (B*H*T_pad <= 1,048,576). For callers that cannot allocate device memory;
+    calls that overlap on the GPU share that scratch and must be serialised."""
+    B, H, T, d = _shape(q)
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, n, torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    _check(_dll.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), B, H, T, d, ctypes.c_float(scale), int(causal),
+                                 _stream_handle(stream)), "attn_bwd_noalloc")
 
 
 def check_device_error(stream=None):

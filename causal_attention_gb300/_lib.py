@@ -39,6 +39,7 @@ SIGNATURES = {
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _S, _I, _I, _I, _I, _P]),
     "attn_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "attn_check_device_error": (_I, [_P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_cuda_error": (ctypes.c_char_p, []),
@@ -49,7 +50,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     """Loads libattn.so; raises if it is missing (there is no fallback path)."""
     if not os.path.exists(path):
         raise ImportError(
-            f"libattn.so not found at {path}; build it with `python -m causal_attention_gb300.build`")
+            f"libattn.so not found at {path}; build it with `python causal_attention_gb300/build.py`")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)

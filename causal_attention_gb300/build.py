@@ -5,7 +5,8 @@ linked into ``causal_attention_gb300/lib/libattn.so``. The CUDA runtime is the s
 ``libcudart.so.13``: when PyTorch has loaded its copy first, the library uses that same
 runtime (one current device per thread for both); otherwise the toolkit's copy is found
 through the RPATH. Nothing links libcuda, so the library loads without a GPU driver
-(the driver is looked up on first use). Run ``python -m causal_attention_gb300.build``.
+(the driver is looked up on first use). Run ``python causal_attention_gb300/build.py`` (by path: importing
+the package loads the library it builds).
 """
 from __future__ import annotations
 

@@ -184,6 +184,40 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
 
 attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : cuda_fail(e, ATTN_ERR_LAUNCH); }
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for attn_bwd_noalloc: the backward's two fp32 arrays of B*H*T_pad
+// entries live in this array instead of a caller-allocated workspace. It is part of
+// the library image, so every device that loads the library holds it until the
+// process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;  // 8 MiB: B*H*T_pad <= 1,048,576
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device. Host code cannot use the
+// symbol itself (on the host it names a stand-in, not device memory); the address is
+// looked up once per device, with that device current, and cached.
+void* noalloc_scratch_ptr(cudaError_t* e) {
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  *e = bind_device();
+  if (*e != cudaSuccess) return nullptr;
+  int dev = 0;
+  *e = cudaGetDevice(&dev);
+  if (*e != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *e = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    *e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*e != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
 }  // namespace
 
 cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask) {
@@ -299,6 +333,25 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   ATTN_TRY(launched(launch_bwd_preprocess(a, s)));
   ATTN_TRY(launched(launch_bwd_dkdv(a, s)));
   return launched(launch_bwd_dq(a, s));
+}
+
+attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                             int H, int T, int d, float scale, int causal, void* stream) {
+  ATTN_TRY(check_shape(B, H, T, d));
+  const size_t need = workspace_bytes_for(B, H, T);
+  if (need > kNoAllocScratchBytes) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+             "attn_bwd_noalloc: B*H*T_pad = %zu rows needs %zu bytes of scratch; the fixed scratch "
+             "holds %zu bytes (B*H*T_pad <= %zu, T_pad = T rounded up to 128); use attn_bwd",
+             need / 8, need, kNoAllocScratchBytes, kNoAllocScratchBytes / 8);
+    return ATTN_ERR_WORKSPACE;
+  }
+  cudaError_t e;
+  void* scratch = noalloc_scratch_ptr(&e);
+  if (!scratch) return cuda_fail(e, ATTN_ERR_CUDA);
+  return attn_bwd(q, k, v, o, dO, lse, dq, dk, dv, scratch, kNoAllocScratchBytes, B, H, T, d, scale,
+                  causal, stream);
 }
 
 attn_status attn_check_device_error(void* stream) {

@@ -108,6 +108,30 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void*
                         const void* workspace, size_t workspace_bytes, int B, int H, int T, int d,
                         float scale, int causal, void* stream);
 
+/*
+ * Backward without a workspace argument. The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory for the workspace:
+ * code running inside a host framework that owns every device allocation and gives a
+ * plug-in no way to ask for scratch, and latency-critical callers that must not call
+ * cudaMalloc/cudaFree on the step path because those calls can synchronise the whole
+ * device. It computes exactly what attn_bwd computes (same kernels, same results), but
+ * keeps the D / LSE scratch in a fixed 8 MiB array that is part of the library's device
+ * image (every GPU that loads the library holds it until the process exits), and it
+ * calls no allocating routine.
+ *   Limit: B*H*T_pad <= 1,048,576 (T_pad = T rounded up to 128); larger shapes return
+ *   ATTN_ERR_WORKSPACE without launching anything (use attn_bwd with a workspace).
+ *   Set-up: the first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, and the array keeps the last
+ *   call's contents. Nothing in it has to start at zero (each call overwrites every
+ *   entry it reads), but calls whose executions overlap on the GPU (different streams,
+ *   no ordering between them) race on the array and must be serialised by the caller.
+ * Arguments are those of attn_bwd without workspace and workspace_bytes.
+ */
+attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                             int H, int T, int d, float scale, int causal, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device. Returns ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait
  * expired since the last check, ATTN_ERR_CUDA if the synchronisation failed. */
