@@ -164,8 +164,8 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   a->d = d;
   a->causal = causal;
   a->scale = scale;
-  a->ws_lse2 = static_cast<float*>(const_cast<void*>(workspace));
-  a->ws_D = a->ws_lse2 + (size_t)a->BH * a->T_pad;
+  a->ws_nlse2 = static_cast<float*>(const_cast<void*>(workspace));
+  a->ws_D = a->ws_nlse2 + (size_t)a->BH * a->T_pad;
   cudaError_t e;
   a->err = error_word_ptr(&e);
   if (!a->err) return cuda_fail(e, ATTN_ERR_CUDA);

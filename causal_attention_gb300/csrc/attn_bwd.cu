@@ -1,9 +1,10 @@
 // Causal attention backward for sm_103a, three kernels, no atomics:
 //
 //  1. preprocess: D = rowsum(dO * O) in fp32 (Forge RESEARCH.md, section 6, "The D
-//     term is free": D_i = sum_j P_ij dP_ij = dO_i . O_i) and LSE * log2(e), both
-//     written to a [B*H, T_pad] workspace (padding rows: D = 0, LSE = +inf, so
-//     that padded queries contribute P = 0).
+//     term is free": D_i = sum_j P_ij dP_ij = dO_i . O_i) and -LSE * log2(e), both
+//     written to a [B*H, T_pad] workspace (padding rows: D = 0, -LSE*log2e = -inf,
+//     so that padded queries contribute P = 0). With the sign folded in, P is one
+//     fused multiply-add and an exp2 away from S.
 //  2. dK/dV: one CTA per 128-key tile j, looping over query tiles i (i >= j when
 //     causal): S^T = K_j Q_i^T, P^T = exp2(S^T * scale * log2e - LSE_i * log2e),
 //     dV_j += P^T dO_i, dP^T = V_j dO_i^T, dS^T = P^T * (dP^T - D_i),
@@ -17,13 +18,15 @@
 // The dQ-parallel / dKV-parallel split with a D preprocess is the three-stage,
 // atomic-free structure of the Forge paper's section "Ecosystem survey".
 //
-// Roles in the two tensor-core kernels (192 threads):
-//   warps 0-3  elementwise (thread = row of the CTA's own tile = TMEM lane)
-//   warp  4    TMA producer
-//   warp  5    TMEM allocator and MMA issuer
+// Roles in the two tensor-core kernels (320 threads):
+//   warps 0-7  elementwise, two warpgroups: thread = row of the CTA's own tile (TMEM
+//              lane), warpgroup h = columns [64h, 64h+64) of the 128-column tiles
+//   warp  8    TMA producer
+//   warp  9    TMEM allocator and MMA issuer
 // Tensor memory: S or S^T [0,128), dP or dP^T [128,256), accumulators from 256.
-// P^T and dS^T (bf16) are written over the first 64 columns of the S^T and dP^T
-// regions and fed back to the tensor core from TMEM as the A operand.
+// P^T and dS^T (bf16) are written over the S^T and dP^T regions (each warpgroup into
+// the first 32 columns of its own 64-column half) and fed back to the tensor core from
+// TMEM as the A operand.
 #include "kernels.h"
 #include "tile.cuh"
 
@@ -31,7 +34,7 @@ namespace attn {
 
 namespace {
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -40,7 +43,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-    const float* __restrict__ lse, float* __restrict__ ws_lse2, float* __restrict__ ws_D, int T,
+    const float* __restrict__ lse, float* __restrict__ ws_nlse2, float* __restrict__ ws_D, int T,
     int T_pad, int BH) {
   constexpr int TPR = D / 8;           // threads per row, 16 bytes each
   constexpr int RPW = 32 / TPR;        // rows per warp step
@@ -77,7 +80,7 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     if (in_range && sub == 0) {
       const bool valid = t < T;
       ws_D[row] = valid ? acc : 0.f;
-      ws_lse2[row] = valid ? lse[(size_t)bh * T + t] * kLog2e : INFINITY;
+      ws_nlse2[row] = valid ? -lse[(size_t)bh * T + t] * kLog2e : -INFINITY;
     }
   }
 }
@@ -91,12 +94,12 @@ struct BwdCfg {
   static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
   // fixed tiles (K_j, V_j for dK/dV; Q_i, dO_i for dQ)
   static constexpr int OFF_FIX = 0;
-  // per stage: two tiles (+ for dK/dV, 128 fp32 LSE and 128 fp32 D)
+  // per stage: two tiles (+ for dK/dV, 128 fp32 -LSE*log2e and 128 fp32 D)
   static constexpr int STAGE_BYTES = 2 * TL::BYTES + 1024;
   static constexpr int OFF_STAGE = OFF_FIX + 2 * TL::BYTES;
   static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
-  // barriers: fix_full, st_full[S], st_empty[S], s_full, p_full, done, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 4;
+  // barriers: fix_full, st_full[S], st_empty[S], s_full, dp_full, p_full, ds_full, done, drain
+  static constexpr int NBAR = 1 + 2 * STAGES + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -113,10 +116,14 @@ struct BwdSmem {
   __device__ uint32_t st_full(int s) const { return bar0 + 8u * (1 + s); }
   __device__ uint32_t st_empty(int s) const { return bar0 + 8u * (1 + st + s); }
   __device__ uint32_t s_full() const { return bar0 + 8u * (1 + 2 * st); }
-  __device__ uint32_t p_full() const { return bar0 + 8u * (2 + 2 * st); }
-  __device__ uint32_t done() const { return bar0 + 8u * (3 + 2 * st); }
-  __device__ uint32_t drain() const { return bar0 + 8u * (4 + 2 * st); }
+  __device__ uint32_t dp_full() const { return bar0 + 8u * (2 + 2 * st); }
+  __device__ uint32_t p_full() const { return bar0 + 8u * (3 + 2 * st); }
+  __device__ uint32_t ds_full() const { return bar0 + 8u * (4 + 2 * st); }
+  __device__ uint32_t done() const { return bar0 + 8u * (5 + 2 * st); }
+  __device__ uint32_t drain() const { return bar0 + 8u * (6 + 2 * st); }
 };
+
+constexpr int kEwThreads = 256;  // two elementwise warpgroups
 
 template <int D>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
@@ -137,39 +144,57 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
       mbar_init(s.st_empty(i), 1);
     }
     mbar_init(s.s_full(), 1);
-    mbar_init(s.p_full(), 128);
+    mbar_init(s.dp_full(), 1);
+    mbar_init(s.p_full(), kEwThreads);
+    mbar_init(s.ds_full(), kEwThreads);
     mbar_init(s.done(), 1);
     mbar_init(s.drain(), 1);
     *abort = 0;
     fence_barrier_init();
   }
-  if ((threadIdx.x >> 5) == 5) tmem_alloc(smem_u32(tmem_slot), 512);
+  if ((threadIdx.x >> 5) == 9) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   return s;
 }
 
-// Converts 32 fp32 accumulator columns to bf16 (times `mul`) and stores them.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&u)[32], float mul) {
-  uint4 pk[4];
+// Converts 16 fp32 accumulator columns to bf16 (times `mul`) and stores them.
+__device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t (&u)[16], float mul) {
+  uint4 pk[2];
   uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
+  for (int i = 0; i < 8; ++i)
     pw[i] = pack_bf16(__uint_as_float(u[2 * i]) * mul, __uint_as_float(u[2 * i + 1]) * mul);
   uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) d4[i] = pk[i];
+  d4[0] = pk[0];
+  d4[1] = pk[1];
+}
+
+// TMEM column of K-step k of an A operand whose 128 K-columns (bf16) were written by
+// the two elementwise warpgroups, each into the first 32 columns of its own 64-column
+// half of a 128-column fp32 region.
+__device__ __forceinline__ uint32_t halves_col(int k) { return 8u * (k & 3) + 64u * (k >> 2); }
+
+// Producer drain after an abort: every copy issued must land before the CTA exits.
+__device__ __forceinline__ void drain_stages(const BwdSmem& sm, int issued, int st, const Abort& ab) {
+  mbar_wait_drain(sm.fix_full(), 0, ab);
+  for (int it = max(0, issued - st); it < issued; ++it) mbar_wait_drain(sm.st_full(it % st), (it / st) & 1, ab);
 }
 
 // ---------------------------------------------------------------------------
 // 2. dK / dV
 // ---------------------------------------------------------------------------
+// MMA issue order per query tile i (S, dP, P, dS below are the transposed tiles):
+//   S_0, dP_0 | P_0 ready: dV_0, S_1 | dS_0 ready: dK_0, dP_1 | P_1 ready: dV_1, S_2 | ...
+// so the tensor core runs dV_i and S_{i+1} while the elementwise warps compute dS_i,
+// and dK_i and dP_{i+1} while they compute P_{i+1}. S_{i+1} overwrites the region that
+// held P_i only after dV_i (same-thread tcgen05 MMAs execute in issue order).
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                         const float* __restrict__ ws_lse2, const float* __restrict__ ws_D,
+                         const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
                          __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int T,
                          int T_pad, int BH, float scale, float scale_log2, uint32_t* __restrict__ err) {
   using C = BwdCfg<D>;
@@ -192,9 +217,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sK = sm.base + C::OFF_FIX, sV = sK + TL::BYTES;
   auto sQ = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sdO = [&](int s) { return sQ(s) + TL::BYTES; };
-  auto sL = [&](int s) { return sQ(s) + 2 * TL::BYTES; };  // 128 fp32 LSE*log2e, then 128 fp32 D
+  auto sL = [&](int s) { return sQ(s) + 2 * TL::BYTES; };  // 128 fp32 -LSE*log2e, then 128 fp32 D
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -212,44 +237,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         TL::load(sQ(s), &tmQ, qi * kTileRows, bh, sm.st_full(s));
         TL::load(sdO(s), &tmdO, qi * kTileRows, bh, sm.st_full(s));
         const size_t woff = (size_t)bh * T_pad + (size_t)qi * kTileRows;
-        bulk_load(sL(s), ws_lse2 + woff, 512, sm.st_full(s));
+        bulk_load(sL(s), ws_nlse2 + woff, 512, sm.st_full(s));
         bulk_load(sL(s) + 512, ws_D + woff, 512, sm.st_full(s));
         issued = it + 1;
       }
-      if (!ok) {
-        mbar_wait_drain(sm.fix_full(), 0, ab);
-        for (int it = max(0, issued - ST); it < issued; ++it)
-          mbar_wait_drain(sm.st_full(it % ST), (it / ST) & 1, ab);
-      }
+      if (!ok) drain_stages(sm, issued, ST, ab);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
-      bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it % ST, n = it / ST;
-        if (!(ok = mbar_wait(sm.st_full(s), n & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (M = keys, N = queries, K = d)
+      auto issue_S = [&](int s) {  // S^T = K_j Q_i^T (M = keys, N = queries, K = d)
 #pragma unroll
         for (int k = 0; k < TL::KSTEPS_D; ++k)
           mma_ss(tS, TL::desc_kmajor(sK, k), TL::desc_kmajor(sQ(s), k), idesc_s, k > 0 ? 1u : 0u);
+      };
+      auto issue_dP = [&](int s) {  // dP^T = V_j dO_i^T
 #pragma unroll
         for (int k = 0; k < TL::KSTEPS_D; ++k)
           mma_ss(tDP, TL::desc_kmajor(sV, k), TL::desc_kmajor(sdO(s), k), idesc_s, k > 0 ? 1u : 0u);
+      };
+      bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma) && mbar_wait(sm.st_full(0), 0, ab, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
         mma_commit(sm.s_full());
+        issue_dP(0);
+        mma_commit(sm.dp_full());
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it % ST;
+        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
+        const bool more = it + 1 < n_it;
         if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;
         tc_fence_after();
-        // dV += P^T dO_i, dK += dS^T Q_i (M = keys, N = d, K = queries)
+        // dV += P^T dO_i (M = keys, N = d, K = queries)
 #pragma unroll
         for (int k = 0; k < kTileRows / 16; ++k)
-          mma_ts(tDV, tS + 8u * k, TL::desc_mnmajor(sdO(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tDV, tS + halves_col(k), TL::desc_mnmajor(sdO(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+        if (more) {
+          if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          issue_S(s1);
+          mma_commit(sm.s_full());
+        }
+        if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        // dK += dS^T Q_i
 #pragma unroll
         for (int k = 0; k < kTileRows / 16; ++k)
-          mma_ts(tDK, tDP + 8u * k, TL::desc_mnmajor(sQ(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tDK, tDP + halves_col(k), TL::desc_mnmajor(sQ(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
         mma_commit(sm.st_empty(s));
+        if (more) {
+          issue_dP(s1);
+          mma_commit(sm.dp_full());
+        }
       }
       if (ok) {
         mma_commit(sm.done());
@@ -259,46 +302,77 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    // elementwise: thread r owns key row kt*128 + r
-    const int r = threadIdx.x;
+    // elementwise: thread owns key row kt*128 + r and query columns [64*hc, 64*hc + 64)
+    const int hc = warp >> 2;
+    const int r = threadIdx.x & 127;
     const uint32_t lo = warp_lane_base();
-    const uint32_t tS = tmem + lo, tDP = tmem + lo + 128u;
+    const uint32_t tSh = tmem + lo + 64u * hc, tDPh = tmem + lo + 128u + 64u * hc;
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % ST, n = it / ST, qi = i0 + it;
       if (!(ok = mbar_wait_warp(sm.s_full(), it & 1, ab, kErrTimeoutElem))) break;
       if (!(ok = mbar_wait_warp(sm.st_full(s), n & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base));
-      const float* dd = lse2 + 128;
+      const float* nl = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base)) + 64 * hc;
+      const float* dd = nl + 128;
       const bool diag = CAUSAL && qi == kt;
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t us[32], ud[32];
-        tmem_ld32(tS + 32u * cb, us);
-        tmem_ld32(tDP + 32u * cb, ud);
+      // ---- P^T = exp2(S^T * scale*log2e - LSE_i*log2e), kept in fp32 for dS
+      float p[64];
+      {
+        uint32_t u[64];
+        tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
-        uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float p[2], g[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 32 * cb + 2 * i + h;  // query column
-            float pv = ex2(fmaf(__uint_as_float(us[2 * i + h]), scale_log2, -lse2[c]));
-            if (diag && c < r) pv = 0.f;
-            p[h] = pv;
-            g[h] = pv * (__uint_as_float(ud[2 * i + h]) - dd[c]);
-          }
-          pp[i] = pack_bf16(p[0], p[1]);
-          pd[i] = pack_bf16(g[0], g[1]);
+        for (int i = 0; i < 32; ++i) {
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2,
+                                    *reinterpret_cast<const uint64_t*>(nl + 2 * i));
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          p[2 * i] = ex2(x0);
+          p[2 * i + 1] = ex2(x1);
         }
-        tmem_st16(tS + 16u * cb, pp);
-        tmem_st16(tDP + 16u * cb, pd);
+      }
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (64 * hc + c < r) p[c] = 0.f;
+      }
+      {
+        uint32_t pp[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+        tmem_st16(tSh, *reinterpret_cast<uint32_t(*)[16]>(&pp[0]));
+        tmem_st16(tSh + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pp[16]));
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(sm.p_full());
+      // ---- dS^T = P^T * (dP^T - D_i)
+      if (!(ok = mbar_wait_warp(sm.dp_full(), it & 1, ab, kErrTimeoutElem))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t u[32];
+        tmem_ld32(tDPh + 32u * cb, u);
+        tmem_wait_ld();
+        uint32_t pd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 32 * cb + 2 * i;
+          const uint64_t g = f2_mul(f2_pack(p[c], p[c + 1]),
+                                    f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])),
+                                           *reinterpret_cast<const uint64_t*>(dd + c)));
+          float g0, g1;
+          f2_unpack(g, g0, g1);
+          pd[i] = pack_bf16(g0, g1);
+        }
+        tmem_st16(tDPh + 16u * cb, pd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sm.ds_full());
     }
     if (ok && mbar_wait_warp(sm.done(), 0, ab, kErrTimeoutElem)) {
       tc_fence_after();
@@ -306,20 +380,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)D;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t u[32];
-        tmem_ld32(tDV + 32u * cb, u);
+        const int col = hc * (D / 2) + 16 * cb;
+        uint32_t u[16];
+        tmem_ld16(tDV + (uint32_t)col, u);
         tmem_wait_ld();
-        if (key < T) store_row32(dv + ((size_t)bh * T + key) * D + 32 * cb, u, 1.f);
-        tmem_ld32(tDK + 32u * cb, u);
+        if (key < T) store_row16(dv + ((size_t)bh * T + key) * D + col, u, 1.f);
+        tmem_ld16(tDK + (uint32_t)col, u);
         tmem_wait_ld();
-        if (key < T) store_row32(dk + ((size_t)bh * T + key) * D + 32 * cb, u, scale);
+        if (key < T) store_row16(dk + ((size_t)bh * T + key) * D + col, u, scale);
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -328,11 +403,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------------------
 // 3. dQ
 // ---------------------------------------------------------------------------
+// MMA issue order per key tile j: S_0, dP_0 | S_0 read out: S_1 | dS_0 ready: dQ += dS_0 K_0,
+// dP_1 | S_1 read out: S_2 | ... The elementwise warps release S_j as soon as it is in
+// registers, so S_{j+1} runs on the tensor core while they compute the exponentials.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const float* __restrict__ ws_lse2, const float* __restrict__ ws_D,
+                       const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
                        __nv_bfloat16* __restrict__ dq, int T, int T_pad, int BH, float scale,
                        float scale_log2, uint32_t* __restrict__ err) {
   using C = BwdCfg<D>;
@@ -355,7 +433,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sV = [&](int s) { return sK(s) + TL::BYTES; };
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -374,37 +452,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         TL::load(sV(s), &tmV, it * kTileRows, bh, sm.st_full(s));
         issued = it + 1;
       }
-      if (!ok) {
-        mbar_wait_drain(sm.fix_full(), 0, ab);
-        for (int it = max(0, issued - ST); it < issued; ++it)
-          mbar_wait_drain(sm.st_full(it % ST), (it / ST) & 1, ab);
-      }
+      if (!ok) drain_stages(sm, issued, ST, ab);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tS = tmem, tDP = tmem + 128u, tDQ = tmem + 256u;
-      bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it % ST, n = it / ST;
-        if (!(ok = mbar_wait(sm.st_full(s), n & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        // S = Q_i K_j^T and dP = dO_i V_j^T (M = queries, N = keys, K = d)
+      auto issue_S = [&](int s) {  // S = Q_i K_j^T (M = queries, N = keys, K = d)
 #pragma unroll
         for (int k = 0; k < TL::KSTEPS_D; ++k)
           mma_ss(tS, TL::desc_kmajor(sQ, k), TL::desc_kmajor(sK(s), k), idesc_s, k > 0 ? 1u : 0u);
+      };
+      auto issue_dP = [&](int s) {  // dP = dO_i V_j^T
 #pragma unroll
         for (int k = 0; k < TL::KSTEPS_D; ++k)
           mma_ss(tDP, TL::desc_kmajor(sdO, k), TL::desc_kmajor(sV(s), k), idesc_s, k > 0 ? 1u : 0u);
+      };
+      bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma) && mbar_wait(sm.st_full(0), 0, ab, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
         mma_commit(sm.s_full());
-        if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;
+        issue_dP(0);
+        mma_commit(sm.dp_full());
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it % ST;
+        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
+        const bool more = it + 1 < n_it;
+        if (more) {
+          if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;  // S_it read out
+          if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          issue_S(s1);
+          mma_commit(sm.s_full());
+        }
+        if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
         tc_fence_after();
         // dQ += dS K_j (M = queries, N = d, K = keys)
 #pragma unroll
         for (int k = 0; k < kTileRows / 16; ++k)
-          mma_ts(tDQ, tDP + 8u * k, TL::desc_mnmajor(sK(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tDQ, tDP + halves_col(k), TL::desc_mnmajor(sK(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
         mma_commit(sm.st_empty(s));
+        if (more) {
+          issue_dP(s1);
+          mma_commit(sm.dp_full());
+        }
       }
       if (ok) {
         mma_commit(sm.done());
@@ -414,61 +508,87 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    // elementwise: thread r owns query row qt*128 + r
-    const int r = threadIdx.x;
+    // elementwise: thread owns query row qt*128 + r and key columns [64*hc, 64*hc + 64)
+    const int hc = warp >> 2;
+    const int r = threadIdx.x & 127;
     const int row = qt * kTileRows + r;
     const uint32_t lo = warp_lane_base();
-    const uint32_t tS = tmem + lo, tDP = tmem + lo + 128u;
-    const float lse2 = ws_lse2[(size_t)bh * T_pad + row];
+    const uint32_t tSh = tmem + lo + 64u * hc, tDPh = tmem + lo + 128u + 64u * hc;
+    const float nl = ws_nlse2[(size_t)bh * T_pad + row];
     const float Dr = ws_D[(size_t)bh * T_pad + row];
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(nl, nl), D2 = f2_pack(Dr, Dr);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       if (!(ok = mbar_wait_warp(sm.s_full(), it & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
-      const bool diag = CAUSAL && it == qt;
-      const int key_lim = T - it * kTileRows;  // keys at column >= key_lim are padding
+      float p[64];
+      {
+        uint32_t u[64];
+        tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(sm.p_full());  // S_it is in registers: the tensor core may overwrite it
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t us[32], ud[32];
-        tmem_ld32(tS + 32u * cb, us);
-        tmem_ld32(tDP + 32u * cb, ud);
+        for (int i = 0; i < 32; ++i) {
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nl2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          p[2 * i] = ex2(x0);
+          p[2 * i + 1] = ex2(x1);
+        }
+      }
+      if (CAUSAL && it == qt) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (64 * hc + c > r) p[c] = 0.f;
+      }
+      if (!CAUSAL) {
+        const int lim = T - it * kTileRows - 64 * hc;  // key columns >= lim are padding
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c >= lim) p[c] = 0.f;
+      }
+      if (!(ok = mbar_wait_warp(sm.dp_full(), it & 1, ab, kErrTimeoutElem))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t u[32];
+        tmem_ld32(tDPh + 32u * cb, u);
         tmem_wait_ld();
         uint32_t pd[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float g[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = 32 * cb + 2 * i + h;  // key column
-            float pv = ex2(fmaf(__uint_as_float(us[2 * i + h]), scale_log2, -lse2));
-            if (diag && c > r) pv = 0.f;
-            if (!CAUSAL && c >= key_lim) pv = 0.f;
-            g[h] = pv * (__uint_as_float(ud[2 * i + h]) - Dr);
-          }
-          pd[i] = pack_bf16(g[0], g[1]);
+          const int c = 32 * cb + 2 * i;
+          const uint64_t g = f2_mul(f2_pack(p[c], p[c + 1]),
+                                    f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), D2));
+          float g0, g1;
+          f2_unpack(g, g0, g1);
+          pd[i] = pack_bf16(g0, g1);
         }
-        tmem_st16(tDP + 16u * cb, pd);
+        tmem_st16(tDPh + 16u * cb, pd);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(sm.p_full());
+      mbar_arrive(sm.ds_full());
     }
     if (ok && mbar_wait_warp(sm.done(), 0, ab, kErrTimeoutElem)) {
       tc_fence_after();
       const uint32_t tDQ = tmem + lo + 256u;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t u[32];
-        tmem_ld32(tDQ + 32u * cb, u);
+        const int col = hc * (D / 2) + 16 * cb;
+        uint32_t u[16];
+        tmem_ld16(tDQ + (uint32_t)col, u);
         tmem_wait_ld();
-        if (row < T) store_row32(dq + ((size_t)bh * T + row) * D + 32 * cb, u, scale);
+        if (row < T) store_row16(dq + ((size_t)bh * T + row) * D + col, u, scale);
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -484,7 +604,7 @@ cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   const long long cap = 152LL * 8;  // grid-stride beyond 8 blocks per SM
   if (blocks > cap) blocks = cap;
-  attn_bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.o, a.dO, a.lse, a.ws_lse2, a.ws_D,
+  attn_bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.o, a.dO, a.lse, a.ws_nlse2, a.ws_D,
                                                                       a.T, a.T_pad, a.BH);
   return cudaGetLastError();
 }
@@ -497,7 +617,7 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int n_t = (a.T + kTileRows - 1) / kTileRows;
   kern<<<n_t * a.BH, kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
-      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_lse2, a.ws_D, a.dk, a.dv, a.T, a.T_pad, a.BH, a.scale,
+      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.T, a.T_pad, a.BH, a.scale,
       a.scale * kLog2e, a.err);
   return cudaGetLastError();
 }
@@ -510,7 +630,7 @@ cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int n_t = (a.T + kTileRows - 1) / kTileRows;
   kern<<<n_t * a.BH, kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
-      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_lse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.scale,
+      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.scale,
       a.scale * kLog2e, a.err);
   return cudaGetLastError();
 }

@@ -20,7 +20,7 @@ struct FwdArgs {
 };
 
 // Workspace of the backward: two fp32 arrays of [B*H, T_pad], T_pad = T rounded
-// up to 128. ws_lse2 = LSE * log2(e) (+inf on padding rows), ws_D = rowsum(dO*O)
+// up to 128. ws_nlse2 = -LSE * log2(e) (-inf on padding rows), ws_D = rowsum(dO*O)
 // (0 on padding rows).
 struct BwdArgs {
   const CUtensorMap* tmQ;
@@ -33,7 +33,7 @@ struct BwdArgs {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* ws_lse2;
+  float* ws_nlse2;
   float* ws_D;
   int T, T_pad, BH, d, causal;
   float scale;

@@ -164,8 +164,8 @@ def test_preprocess_D_against_oracle():
     ref = oracle.preprocess_D(si.bf16_bits_to_f64(o_bits), si.bf16_bits_to_f64(x["do"])).reshape(-1, w.T)
     assert np.max(np.abs(wsn[1][:, :w.T] - ref)) <= 1e-4 * np.max(np.abs(ref))
     assert np.all(wsn[1][:, w.T:] == 0)
-    assert np.allclose(wsn[0][:, :w.T], lse.cpu().numpy().reshape(-1, w.T) * np.log2(np.e), rtol=1e-6)
-    assert np.all(np.isinf(wsn[0][:, w.T:]))
+    assert np.allclose(wsn[0][:, :w.T], -lse.cpu().numpy().reshape(-1, w.T) * np.log2(np.e), rtol=1e-6)
+    assert np.all(np.isneginf(wsn[0][:, w.T:]))
 
 
 def test_autograd_function():
