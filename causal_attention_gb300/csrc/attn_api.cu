@@ -5,7 +5,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "kernels.h"
 
 namespace attn {

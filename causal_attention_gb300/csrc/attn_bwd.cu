@@ -18,11 +18,15 @@
 // The dQ-parallel / dKV-parallel split with a D preprocess is the three-stage,
 // atomic-free structure of the Forge paper's section "Ecosystem survey".
 //
-// Roles in the two tensor-core kernels (320 threads):
+// Roles in the two tensor-core kernels (352 threads):
 //   warps 0-7  elementwise, two warpgroups: thread = row of the CTA's own tile (TMEM
 //              lane), warpgroup h = columns [64h, 64h+64) of the 128-column tiles
 //   warp  8    TMA producer
-//   warp  9    TMEM allocator and MMA issuer
+//   warp  9    TMEM allocator and MMA issuer (S and dP)
+//   warp  10   second MMA issuer (dV and dK, or dQ) where the elementwise results have
+//              their own TMEM columns. A tcgen05.mma issue blocks until the tensor core
+//              can take it, and any wait of the issuing thread drains the queue, so two
+//              issuers keep the tensor core fed while either one waits.
 // Tensor memory: S or S^T [0,128), dP or dP^T [128,256), accumulators from 256.
 // P^T and dS^T (bf16) are written over the S^T and dP^T regions (each warpgroup into
 // the first 32 columns of its own 64-column half) and fed back to the tensor core from
@@ -34,7 +38,7 @@ namespace attn {
 
 namespace {
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -98,8 +102,12 @@ struct BwdCfg {
   static constexpr int STAGE_BYTES = 2 * TL::BYTES + 1024;
   static constexpr int OFF_STAGE = OFF_FIX + 2 * TL::BYTES;
   static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
-  // barriers: fix_full, st_full[S], st_empty[S], s_full, dp_full, p_full, ds_full, done, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 6;
+  // barriers: fix_full, st_full[S], st_empty[S], s_full, dp_full, p_full, ds_full, done,
+  // drain, s_free, dp_free, dv_done, dk_done (dq_done shares dk_done's slot), drain2
+  static constexpr int NBAR = 1 + 2 * STAGES + 11;
+  // The dK/dV kernel gives P^T and dS^T their own TMEM columns when they fit (d <= 64).
+  static constexpr bool SEP_DKDV = D <= 64;
+  static constexpr uint32_t COL_P = 384, COL_DS = 448;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -121,6 +129,11 @@ struct BwdSmem {
   __device__ uint32_t ds_full() const { return bar0 + 8u * (4 + 2 * st); }
   __device__ uint32_t done() const { return bar0 + 8u * (5 + 2 * st); }
   __device__ uint32_t drain() const { return bar0 + 8u * (6 + 2 * st); }
+  __device__ uint32_t s_free() const { return bar0 + 8u * (7 + 2 * st); }
+  __device__ uint32_t dp_free() const { return bar0 + 8u * (8 + 2 * st); }
+  __device__ uint32_t dv_done() const { return bar0 + 8u * (9 + 2 * st); }
+  __device__ uint32_t dk_done() const { return bar0 + 8u * (10 + 2 * st); }
+  __device__ uint32_t drain2() const { return bar0 + 8u * (11 + 2 * st); }
 };
 
 constexpr int kEwThreads = 256;  // two elementwise warpgroups
@@ -149,6 +162,11 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     mbar_init(s.ds_full(), kEwThreads);
     mbar_init(s.done(), 1);
     mbar_init(s.drain(), 1);
+    mbar_init(s.s_free(), kEwThreads);
+    mbar_init(s.dp_free(), kEwThreads);
+    mbar_init(s.dv_done(), 1);
+    mbar_init(s.dk_done(), 1);
+    mbar_init(s.drain2(), 1);
     *abort = 0;
     fence_barrier_init();
   }
@@ -170,11 +188,6 @@ __device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t (
   d4[0] = pk[0];
   d4[1] = pk[1];
 }
-
-// TMEM column of K-step k of an A operand whose 128 K-columns (bf16) were written by
-// the two elementwise warpgroups, each into the first 32 columns of its own 64-column
-// half of a 128-column fp32 region.
-__device__ __forceinline__ uint32_t halves_col(int k) { return 8u * (k & 3) + 64u * (k >> 2); }
 
 // Producer drain after an abort: every copy issued must land before the CTA exits.
 __device__ __forceinline__ void drain_stages(const BwdSmem& sm, int issued, int st, const Abort& ab) {
@@ -248,15 +261,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
+      // K-step-0 descriptors, computed once; stage s adds s stages
+      const uint64_t dKk = TL::desc_kmajor0(sK), dVk = TL::desc_kmajor0(sV);
+      const uint64_t dQk0 = TL::desc_kmajor0(sQ(0)), dQm0 = TL::desc_mnmajor0(sQ(0));
+      const uint64_t dOk0 = TL::desc_kmajor0(sdO(0)), dOm0 = TL::desc_mnmajor0(sdO(0));
+      constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       auto issue_S = [&](int s) {  // S^T = K_j Q_i^T (M = keys, N = queries, K = d)
-#pragma unroll
-        for (int k = 0; k < TL::KSTEPS_D; ++k)
-          mma_ss(tS, TL::desc_kmajor(sK, k), TL::desc_kmajor(sQ(s), k), idesc_s, k > 0 ? 1u : 0u);
+        mma_chain_ss<TL, TL::KSTEPS_D>(tS, dKk, dQk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
       };
       auto issue_dP = [&](int s) {  // dP^T = V_j dO_i^T
-#pragma unroll
-        for (int k = 0; k < TL::KSTEPS_D; ++k)
-          mma_ss(tDP, TL::desc_kmajor(sV, k), TL::desc_kmajor(sdO(s), k), idesc_s, k > 0 ? 1u : 0u);
+        mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dVk, dOk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
       };
       bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma) && mbar_wait(sm.st_full(0), 0, ab, kErrTimeoutMma);
       if (ok) {
@@ -266,16 +280,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_dP(0);
         mma_commit(sm.dp_full());
       }
-      for (int it = 0; it < n_it && ok; ++it) {
+      for (int it = 0; it + 1 < n_it && ok && C::SEP_DKDV; ++it) {
+        // separate P^T / dS^T columns: S_{i+1} and dP_{i+1} start as soon as S_i and
+        // dP_i have been read into registers (dV and dK are issued by warp 10)
+        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
+        if (!(ok = mbar_wait(sm.s_free(), it & 1, ab, kErrTimeoutMma))) break;
+        if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        issue_S(s1);
+        mma_commit(sm.s_full());
+        if (!(ok = mbar_wait(sm.dp_free(), it & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        issue_dP(s1);
+        mma_commit(sm.dp_full());
+      }
+      for (int it = 0; it < n_it && ok && !C::SEP_DKDV; ++it) {
         const int s = it % ST;
         const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
         const bool more = it + 1 < n_it;
         if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;
         tc_fence_after();
         // dV += P^T dO_i (M = keys, N = d, K = queries)
-#pragma unroll
-        for (int k = 0; k < kTileRows / 16; ++k)
-          mma_ts(tDV, tS + halves_col(k), TL::desc_mnmajor(sdO(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+        mma_chain_ts<TL, true>(tDV, tS, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
         if (more) {
           if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
           tc_fence_after();
@@ -285,20 +311,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
         tc_fence_after();
         // dK += dS^T Q_i
-#pragma unroll
-        for (int k = 0; k < kTileRows / 16; ++k)
-          mma_ts(tDK, tDP + halves_col(k), TL::desc_mnmajor(sQ(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+        mma_chain_ts<TL, true>(tDK, tDP, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
         mma_commit(sm.st_empty(s));
         if (more) {
           issue_dP(s1);
           mma_commit(sm.dp_full());
         }
       }
+      if (!ok) {
+        mma_commit(sm.drain());
+        mbar_wait_drain(sm.drain(), 0, ab);
+      } else if (!C::SEP_DKDV) {
+        mma_commit(sm.done());
+      }
+    }
+  } else if (warp == 10) {
+    // second issuer: dV_i and dK_i, each as soon as its elementwise operand is in TMEM
+    if (lane == 0 && C::SEP_DKDV) {
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
+      const uint32_t tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
+      const uint64_t dQm0 = TL::desc_mnmajor0(sQ(0)), dOm0 = TL::desc_mnmajor0(sdO(0));
+      constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
+      bool ok = true;
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it % ST;
+        if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        // dV += P^T dO_i (M = keys, N = d, K = queries)
+        mma_chain_ts<TL, false>(tDV, tmem + C::COL_P, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+        mma_commit(sm.dv_done());
+        if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        // dK += dS^T Q_i
+        mma_chain_ts<TL, false>(tDK, tmem + C::COL_DS, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+        mma_commit(sm.dk_done());
+        // S_i and dP_i (warp 9) were read out before P_i / dS_i were signalled, so this
+        // commit covers every MMA that reads stage s
+        mma_commit(sm.st_empty(s));
+      }
       if (ok) {
         mma_commit(sm.done());
       } else {
-        mma_commit(sm.drain());
-        mbar_wait_drain(sm.drain(), 0, ab);
+        mma_commit(sm.drain2());
+        mbar_wait_drain(sm.drain2(), 0, ab);
       }
     }
   } else {
@@ -309,7 +364,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tSh = tmem + lo + 64u * hc, tDPh = tmem + lo + 128u + 64u * hc;
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0; it < n_it && C::SEP_DKDV; ++it) {
+      const int s = it % ST, n = it / ST, qi = i0 + it;
+      if (!(ok = mbar_wait_warp(sm.s_full(), it & 1, ab, kErrTimeoutElem))) break;
+      if (!(ok = mbar_wait_warp(sm.st_full(s), n & 1, ab, kErrTimeoutElem))) break;
+      tc_fence_after();
+      const float* nl = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base)) + 64 * hc;
+      const float* dd = nl + 128;
+      const bool diag = CAUSAL && qi == kt;
+      float p[64];
+      {
+        uint32_t u[64];
+        tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(sm.s_free());  // S^T_i is in registers
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2,
+                                    *reinterpret_cast<const uint64_t*>(nl + 2 * i));
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          p[2 * i] = ex2(x0);
+          p[2 * i + 1] = ex2(x1);
+        }
+      }
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (64 * hc + c < r) p[c] = 0.f;
+      }
+      {
+        uint32_t pp[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+        // dV_{i-1} reads the P^T columns: it must be complete before they are rewritten
+        if (it > 0 && !(ok = mbar_wait_warp(sm.dv_done(), (it - 1) & 1, ab, kErrTimeoutElem))) break;
+        tc_fence_after();
+        const uint32_t tP = tmem + lo + C::COL_P + 32u * hc;
+        tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pp[0]));
+        tmem_st16(tP + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pp[16]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sm.p_full());
+      if (!(ok = mbar_wait_warp(sm.dp_full(), it & 1, ab, kErrTimeoutElem))) break;
+      tc_fence_after();
+      {
+        uint32_t u[64];
+        tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(sm.dp_free());  // dP^T_i is in registers
+        uint32_t pd[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint64_t g = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
+                                    f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])),
+                                           *reinterpret_cast<const uint64_t*>(dd + 2 * i)));
+          float g0, g1;
+          f2_unpack(g, g0, g1);
+          pd[i] = pack_bf16(g0, g1);
+        }
+        if (it > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (it - 1) & 1, ab, kErrTimeoutElem))) break;
+        tc_fence_after();
+        const uint32_t tDS = tmem + lo + C::COL_DS + 32u * hc;
+        tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
+        tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sm.ds_full());
+    }
+    for (int it = 0; it < n_it && ok && !C::SEP_DKDV; ++it) {
       const int s = it % ST, n = it / ST, qi = i0 + it;
       if (!(ok = mbar_wait_warp(sm.s_full(), it & 1, ab, kErrTimeoutElem))) break;
       if (!(ok = mbar_wait_warp(sm.st_full(s), n & 1, ab, kErrTimeoutElem))) break;
@@ -403,9 +532,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------------------
 // 3. dQ
 // ---------------------------------------------------------------------------
-// MMA issue order per key tile j: S_0, dP_0 | S_0 read out: S_1 | dS_0 ready: dQ += dS_0 K_0,
-// dP_1 | S_1 read out: S_2 | ... The elementwise warps release S_j as soon as it is in
-// registers, so S_{j+1} runs on the tensor core while they compute the exponentials.
+// MMA issue order per key tile j: S_0, dP_0 | S_0 read out: S_1 | dP_0 read out: dP_1 |
+// dS_0 ready: dQ += dS_0 K_0 | S_1 read out: S_2 | ... The elementwise warps release S_j
+// and dP_j as soon as they are in registers, and dS has its own 64 TMEM columns (after
+// the dQ accumulator), so the next tile's MMAs run while they compute.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -458,16 +588,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-      const uint32_t tS = tmem, tDP = tmem + 128u, tDQ = tmem + 256u;
+      const uint32_t tS = tmem, tDP = tmem + 128u;
+      // K-step-0 descriptors, computed once; stage s adds s stages
+      const uint64_t dQk = TL::desc_kmajor0(sQ), dOk = TL::desc_kmajor0(sdO);
+      const uint64_t dKk0 = TL::desc_kmajor0(sK(0)), dVk0 = TL::desc_kmajor0(sV(0)), dKm0 = TL::desc_mnmajor0(sK(0));
+      constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       auto issue_S = [&](int s) {  // S = Q_i K_j^T (M = queries, N = keys, K = d)
-#pragma unroll
-        for (int k = 0; k < TL::KSTEPS_D; ++k)
-          mma_ss(tS, TL::desc_kmajor(sQ, k), TL::desc_kmajor(sK(s), k), idesc_s, k > 0 ? 1u : 0u);
+        mma_chain_ss<TL, TL::KSTEPS_D>(tS, dQk, dKk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
       };
       auto issue_dP = [&](int s) {  // dP = dO_i V_j^T
-#pragma unroll
-        for (int k = 0; k < TL::KSTEPS_D; ++k)
-          mma_ss(tDP, TL::desc_kmajor(sdO, k), TL::desc_kmajor(sV(s), k), idesc_s, k > 0 ? 1u : 0u);
+        mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
       };
       bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma) && mbar_wait(sm.st_full(0), 0, ab, kErrTimeoutMma);
       if (ok) {
@@ -477,34 +607,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_dP(0);
         mma_commit(sm.dp_full());
       }
+      for (int it = 0; it + 1 < n_it && ok; ++it) {
+        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
+        if (!(ok = mbar_wait(sm.s_free(), it & 1, ab, kErrTimeoutMma))) break;  // S_it read out
+        if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        issue_S(s1);
+        mma_commit(sm.s_full());
+        if (!(ok = mbar_wait(sm.dp_free(), it & 1, ab, kErrTimeoutMma))) break;  // dP_it read out
+        tc_fence_after();
+        issue_dP(s1);
+        mma_commit(sm.dp_full());
+      }
+      if (!ok) {
+        mma_commit(sm.drain());
+        mbar_wait_drain(sm.drain(), 0, ab);
+      }
+    }
+  } else if (warp == 10) {
+    // second issuer: dQ += dS_j K_j as soon as dS_j is in TMEM
+    if (lane == 0) {
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
+      const uint32_t tDQ = tmem + 256u, tDS = tmem + 256u + (uint32_t)D;
+      const uint64_t dKm0 = TL::desc_mnmajor0(sK(0));
+      constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
+      bool ok = true;
       for (int it = 0; it < n_it && ok; ++it) {
         const int s = it % ST;
-        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
-        const bool more = it + 1 < n_it;
-        if (more) {
-          if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;  // S_it read out
-          if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
-          tc_fence_after();
-          issue_S(s1);
-          mma_commit(sm.s_full());
-        }
         if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
         tc_fence_after();
-        // dQ += dS K_j (M = queries, N = d, K = keys)
-#pragma unroll
-        for (int k = 0; k < kTileRows / 16; ++k)
-          mma_ts(tDQ, tDP + halves_col(k), TL::desc_mnmajor(sK(s), k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+        // dQ += dS K_j (M = queries, N = d, K = keys); dS has its own 64 columns
+        mma_chain_ts<TL, false>(tDQ, tDS, dKm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+        mma_commit(sm.dk_done());  // "dQ_it done": the dS columns may be rewritten
+        // S_j and dP_j (warp 9) were read out before dS_j was signalled
         mma_commit(sm.st_empty(s));
-        if (more) {
-          issue_dP(s1);
-          mma_commit(sm.dp_full());
-        }
       }
       if (ok) {
         mma_commit(sm.done());
       } else {
-        mma_commit(sm.drain());
-        mbar_wait_drain(sm.drain(), 0, ab);
+        mma_commit(sm.drain2());
+        mbar_wait_drain(sm.drain2(), 0, ab);
       }
     }
   } else {
@@ -528,7 +670,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(sm.p_full());  // S_it is in registers: the tensor core may overwrite it
+        mbar_arrive(sm.s_free());  // S_it is in registers: the tensor core may overwrite it
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nl2);
@@ -551,22 +693,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!(ok = mbar_wait_warp(sm.dp_full(), it & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
-#pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t u[32];
-        tmem_ld32(tDPh + 32u * cb, u);
+      {
+        uint32_t u[64];
+        tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
-        uint32_t pd[16];
+        tc_fence_before();
+        mbar_arrive(sm.dp_free());  // dP_it is in registers
+        uint32_t pd[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = 32 * cb + 2 * i;
-          const uint64_t g = f2_mul(f2_pack(p[c], p[c + 1]),
+        for (int i = 0; i < 32; ++i) {
+          const uint64_t g = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
                                     f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), D2));
           float g0, g1;
           f2_unpack(g, g0, g1);
           pd[i] = pack_bf16(g0, g1);
         }
-        tmem_st16(tDPh + 16u * cb, pd);
+        // dQ_{it-1} reads the dS columns: it must be complete before they are rewritten
+        if (it > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (it - 1) & 1, ab, kErrTimeoutElem))) break;
+        tc_fence_after();
+        const uint32_t tDS = tmem + lo + 256u + (uint32_t)D + 32u * hc;
+        tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
+        tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
       }
       tmem_wait_st();
       tc_fence_before();

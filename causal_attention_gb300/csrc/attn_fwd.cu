@@ -13,13 +13,14 @@
 //   warps 4-7  softmax for Q1
 //   warp  8    TMA producer (Q once; K_j, V_j through a STAGES-deep ring)
 //   warp  9    TMEM allocator and MMA issuer (one thread)
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 and O1 from 256;
-// P_q is written as packed bf16 over the first 64 columns of S_q and read back by
-// the PV MMA straight from tensor memory (A operand in TMEM). O is normalised by the
-// sum of those rounded P values (so O / l stays a convex combination of V rows
-// whatever the rounding), the logsumexp by the exact fp32 sum.
-// The MMA issue order S0_{j+1} after PV0_j and S1_{j+1} after PV1_j lets one
-// tile's softmax run while the tensor core works on the other tile.
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 and O1 from 256. P_q is
+// packed bf16, read by the PV MMA straight from tensor memory (A operand in TMEM):
+// at d <= 64 it has its own 64 columns (384 / 448), so S_{q,j+1} is issued as soon as
+// the softmax warps have read S_{q,j} into registers and runs while they compute;
+// at d = 128 (no free columns) P is written over S_q, S_{q,j+1} follows PV_{q,j}, and
+// the two tiles ping-pong on the tensor core. O is normalised by the sum of the
+// rounded P values (so O / l stays a convex combination of V rows whatever the
+// rounding), the logsumexp by the exact fp32 sum.
 // Output rescaling is conditional: the running max is only moved when it grows by
 // more than 2^8 in exp2 units, so most blocks skip touching O.
 #include "kernels.h"
@@ -36,16 +37,33 @@ template <int D>
 struct FwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
+  // P gets its own TMEM columns when they fit (d <= 64); at d = 128 S, O of both
+  // tiles fill all 512 columns and P is written over S.
+  static constexpr bool SEP_P = D <= 64;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  static constexpr uint32_t COL_P0 = SEP_P ? 384 : COL_S0, COL_P1 = SEP_P ? 448 : COL_S1;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * TL::BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * TL::BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * TL::BYTES;
-  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2],
-  // p_full[2], o_final[2], drain
-  static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 1;
+  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], then per tile:
+  // s_full, s_free, p_full, pv_done, o_final; then drain
+  static constexpr int NBAR = 1 + 4 * STAGES + 10 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 };
+
+// Row max of 128 values: eight independent chains of 3-input max, then a short tree.
+__device__ __forceinline__ float rowmax128(const float (&x)[128]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+  for (int c = 16; c < 128; c += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], x[c + 2 * k], x[c + 2 * k + 1]);
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -56,6 +74,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   using C = FwdCfg<D>;
   using TL = Tile<D>;
   constexpr int ST = C::STAGES;
+  constexpr bool SEP = C::SEP_P;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -71,10 +90,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   auto v_full = [&](int s) { return bar0 + 8u * (1 + ST + s); };
   auto k_empty = [&](int s) { return bar0 + 8u * (1 + 2 * ST + s); };
   auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * ST + s); };
-  auto s_full = [&](int q) { return bar0 + 8u * (1 + 4 * ST + q); };
-  auto p_full = [&](int q) { return bar0 + 8u * (3 + 4 * ST + q); };
-  auto o_final = [&](int q) { return bar0 + 8u * (5 + 4 * ST + q); };
-  const uint32_t drain = bar0 + 8u * (7 + 4 * ST);
+  auto s_full = [&](int q) { return bar0 + 8u * (1 + 4 * ST + 5 * q); };
+  auto s_free = [&](int q) { return bar0 + 8u * (2 + 4 * ST + 5 * q); };
+  auto p_full = [&](int q) { return bar0 + 8u * (3 + 4 * ST + 5 * q); };
+  auto pv_done = [&](int q) { return bar0 + 8u * (4 + 4 * ST + 5 * q); };
+  auto o_final = [&](int q) { return bar0 + 8u * (5 + 4 * ST + 5 * q); };
+  const uint32_t drain = bar0 + 8u * (11 + 4 * ST);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
   const Abort ab{abort, err};
@@ -100,7 +121,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(s_full(q), 1);
+      mbar_init(s_free(q), 128);
       mbar_init(p_full(q), 128);
+      mbar_init(pv_done(q), 1);
       mbar_init(o_final(q), 1);
     }
     mbar_init(drain, 1);
@@ -155,19 +178,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
-      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
+      const uint32_t tS[2] = {tmem + C::COL_S0, tmem + C::COL_S1};
+      const uint32_t tO[2] = {tmem + C::COL_O0, tmem + C::COL_O1};
+      const uint32_t tP[2] = {tmem + C::COL_P0, tmem + C::COL_P1};
+      const int nbq[2] = {nb0, nb1};
+      // K-step-0 descriptors, computed once; stage s adds s tiles
+      const uint64_t dQ0 = TL::desc_kmajor0(sQ), dQ1 = TL::desc_kmajor0(sQ + TL::BYTES);
+      const uint64_t dK0 = TL::desc_kmajor0(sK), dV0 = TL::desc_mnmajor0(sV);
+      constexpr uint64_t kTileOff = TL::bytes_off(TL::BYTES);
       auto issue_S = [&](int q, int s) {
-        const uint32_t a = sQ + q * TL::BYTES, b = sK + s * TL::BYTES;
-#pragma unroll
-        for (int k = 0; k < TL::KSTEPS_D; ++k)
-          mma_ss(tS[q], TL::desc_kmajor(a, k), TL::desc_kmajor(b, k), idesc_s, k > 0 ? 1u : 0u);
+        mma_chain_ss<TL, TL::KSTEPS_D>(q ? tS[1] : tS[0], q ? dQ1 : dQ0, dK0 + (uint64_t)s * kTileOff, idesc_s, 0u);
       };
       auto issue_PV = [&](int q, int s, bool acc) {
-        const uint32_t b = sV + s * TL::BYTES;
-#pragma unroll
-        for (int k = 0; k < kTileRows / 16; ++k)
-          mma_ts(tO[q], tS[q] + 8u * k, TL::desc_mnmajor(b, k), idesc_pv, (acc || k > 0) ? 1u : 0u);
+        mma_chain_ts<TL, false>(q ? tO[1] : tO[0], q ? tP[1] : tP[0], dV0 + (uint64_t)s * kTileOff, idesc_pv, acc ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, ab, kErrTimeoutMma) &&
                 mbar_wait(k_full(0), 0, ab, kErrTimeoutMma);
@@ -179,39 +202,71 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit(s_full(1));
         mma_commit(k_empty(0));
       }
-      for (int j = 0; j < nb1 && ok; ++j) {
-        const int s = j % ST, n = j / ST;
-        const int jn = j + 1, sn = jn % ST, nn = jn / ST;
-        if (!(ok = mbar_wait(v_full(s), n & 1, ab, kErrTimeoutMma))) break;
-        bool k_next = false;
-        if (j < nb0) {
-          if (!(ok = mbar_wait(p_full(0), j & 1, ab, kErrTimeoutMma))) break;
-          tc_fence_after();
-          issue_PV(0, s, j > 0);
-          if (jn < nb0) {
+      if constexpr (SEP) {
+        // S_{q,j+1} as soon as tile q's S_j has been read out; then PV_{q,j}.
+        for (int j = 0; j < nb1 && ok; ++j) {
+          const int s = j % ST, n = j / ST;
+          const int jn = j + 1, sn = jn % ST, nn = jn / ST;
+          if (jn < nb1) {
             if (!(ok = mbar_wait(k_full(sn), nn & 1, ab, kErrTimeoutMma))) break;
-            tc_fence_after();
-            k_next = true;
-            issue_S(0, sn);
-            mma_commit(s_full(0));
-          } else {
-            mma_commit(o_final(0));
+            for (int q = 0; q < 2 && ok; ++q) {
+              if (jn >= nbq[q]) continue;
+              if (!(ok = mbar_wait(s_free(q), j & 1, ab, kErrTimeoutMma))) break;
+              tc_fence_after();
+              issue_S(q, sn);
+              mma_commit(s_full(q));
+            }
+            if (!ok) break;
+            mma_commit(k_empty(sn));
           }
+          if (!(ok = mbar_wait(v_full(s), n & 1, ab, kErrTimeoutMma))) break;
+          for (int q = 0; q < 2 && ok; ++q) {
+            if (j >= nbq[q]) continue;
+            if (!(ok = mbar_wait(p_full(q), j & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            issue_PV(q, s, j > 0);
+            mma_commit(pv_done(q));
+            if (j == nbq[q] - 1) mma_commit(o_final(q));
+          }
+          if (!ok) break;
+          mma_commit(v_empty(s));
         }
-        if (!(ok = mbar_wait(p_full(1), j & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        issue_PV(1, s, j > 0);
-        mma_commit(v_empty(s));
-        if (jn < nb1) {
-          if (!k_next) {
-            if (!(ok = mbar_wait(k_full(sn), nn & 1, ab, kErrTimeoutMma))) break;
+      } else {
+        // P is written over S: S_{q,j+1} must follow PV_{q,j} (in-order execution).
+        for (int j = 0; j < nb1 && ok; ++j) {
+          const int s = j % ST, n = j / ST;
+          const int jn = j + 1, sn = jn % ST, nn = jn / ST;
+          if (!(ok = mbar_wait(v_full(s), n & 1, ab, kErrTimeoutMma))) break;
+          bool k_next = false;
+          if (j < nb0) {
+            if (!(ok = mbar_wait(p_full(0), j & 1, ab, kErrTimeoutMma))) break;
             tc_fence_after();
+            issue_PV(0, s, j > 0);
+            if (jn < nb0) {
+              if (!(ok = mbar_wait(k_full(sn), nn & 1, ab, kErrTimeoutMma))) break;
+              tc_fence_after();
+              k_next = true;
+              issue_S(0, sn);
+              mma_commit(s_full(0));
+            } else {
+              mma_commit(o_final(0));
+            }
           }
-          issue_S(1, sn);
-          mma_commit(s_full(1));
-          mma_commit(k_empty(sn));
-        } else {
-          mma_commit(o_final(1));
+          if (!(ok = mbar_wait(p_full(1), j & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          issue_PV(1, s, j > 0);
+          mma_commit(v_empty(s));
+          if (jn < nb1) {
+            if (!k_next) {
+              if (!(ok = mbar_wait(k_full(sn), nn & 1, ab, kErrTimeoutMma))) break;
+              tc_fence_after();
+            }
+            issue_S(1, sn);
+            mma_commit(s_full(1));
+            mma_commit(k_empty(sn));
+          } else {
+            mma_commit(o_final(1));
+          }
         }
       }
       if (!ok) {
@@ -227,8 +282,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int nb = q ? nb1 : nb0;
     const int row = qt * kTileRows + r;
     const uint32_t lane_off = warp_lane_base();
-    const uint32_t tS = tmem + lane_off + (q ? 128u : 0u);
-    const uint32_t tO = tmem + lane_off + 256u + (q ? (uint32_t)D : 0u);
+    const uint32_t tS = tmem + lane_off + (q ? C::COL_S1 : C::COL_S0);
+    const uint32_t tO = tmem + lane_off + (q ? C::COL_O1 : C::COL_O0);
+    const uint32_t tP = tmem + lane_off + (q ? C::COL_P1 : C::COL_P0);
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
 
     float m = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
@@ -237,14 +294,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       float x[128];
       {
-        uint32_t u[32];
+        uint32_t u[128];
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          tmem_ld32(tS + 32u * cb, u);
-          tmem_wait_ld();
+        for (int cb = 0; cb < 4; ++cb) tmem_ld32(tS + 32u * cb, *reinterpret_cast<uint32_t(*)[32]>(&u[32 * cb]));
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[32 * cb + i] = __uint_as_float(u[i]);
-        }
+        for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(u[i]);
+      }
+      if constexpr (SEP) {
+        tc_fence_before();
+        mbar_arrive(s_free(q));  // S_q,j is in registers: the tensor core may overwrite it
       }
       if (CAUSAL && j == qt) {
 #pragma unroll
@@ -257,56 +316,61 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) x[c] = -INFINITY;
       }
-      float mx = x[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      const float mx = rowmax128(x);
       float corr = 1.f;
+      bool need = false;
       if (j == 0) {
         m = mx;
       } else {
         const float m_new = fmaxf(m, mx);
-        const bool need = (m_new - m) * scale_log2 > kRescaleThreshold;
+        need = (m_new - m) * scale_log2 > kRescaleThreshold;
         if (need) {
           corr = ex2((m - m_new) * scale_log2);
           m = m_new;
         }
-        if (__any_sync(0xffffffffu, need)) {
-          // O_q holds the sum through block j-1 (its PV completed before S_q,j did)
+      }
+      // P = exp2(S*scale*log2e - m*scale*log2e), rounded to bf16 for the PV MMA. The
+      // LSE uses the exact row sum l; O is divided by lr, the sum of the same rounded
+      // values, so that O / lr stays a convex combination of V rows.
+      const uint64_t nmc = f2_pack(-m * scale_log2, -m * scale_log2);
+      uint32_t pk[64];
+      uint64_t se[4] = {0, 0, 0, 0}, sr[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int cb = 0; cb < D / 32; ++cb) {
-            uint32_t u[32];
-            tmem_ld32(tO + 32u * cb, u);
-            tmem_wait_ld();
+      for (int i = 0; i < 64; ++i) {
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), c2, nmc), a, b);
+        a = ex2(a);
+        b = ex2(b);
+        pk[i] = pack_bf16(a, b);
+        se[i & 3] = f2_add(se[i & 3], f2_pack(a, b));
+        sr[i & 3] = f2_add(sr[i & 3], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
+      }
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(f2_add(se[0], se[1]), f2_add(se[2], se[3])), a0, a1);
+        f2_unpack(f2_add(f2_add(sr[0], sr[1]), f2_add(sr[2], sr[3])), b0, b1);
+        l = l * corr + (a0 + a1);
+        lr = lr * corr + (b0 + b1);
+      }
+      if constexpr (SEP) {
+        // PV_{q,j-1} must be complete: it reads the P buffer and writes O
+        if (j > 0 && !(ok = mbar_wait_warp(pv_done(q), (j - 1) & 1, ab, kErrTimeoutElem))) break;
+        tc_fence_after();
+      }
+      // (non-SEP: S_q,j completing implies PV_{q,j-1} completed, issued before it)
+      if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
-            tmem_st32(tO + 32u * cb, u);
-          }
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t u[32];
+          tmem_ld32(tO + 32u * cb, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * corr);
+          tmem_st32(tO + 32u * cb, u);
         }
       }
-      // P is rounded to bf16 for the PV MMA, and the row sum l adds up exactly those
-      // rounded values, so that O / l is a convex combination of V rows whatever the
-      // rounding (with a peaked softmax the dominant weight's rounding cancels).
-      // The LSE uses the exact row sum l; O is divided by lr, the sum of the same
-      // bf16-rounded P values.
-      const float mc = m * scale_log2;
-      float se0 = 0.f, se1 = 0.f, sr0 = 0.f, sr1 = 0.f;
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t u[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(x[32 * cb + 2 * i], scale_log2, -mc));
-          const float p1 = ex2(fmaf(x[32 * cb + 2 * i + 1], scale_log2, -mc));
-          u[i] = pack_bf16(p0, p1);
-          se0 += p0;
-          se1 += p1;
-          sr0 += __uint_as_float(u[i] << 16);
-          sr1 += __uint_as_float(u[i] & 0xFFFF0000u);
-        }
-        tmem_st16(tS + 16u * cb, u);
-      }
-      l = l * corr + (se0 + se1);
-      lr = lr * corr + (sr0 + sr1);
+      for (int cb = 0; cb < 4; ++cb) tmem_st16(tP + 16u * cb, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * cb]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full(q));
@@ -320,15 +384,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t u[32];
         tmem_ld32(tO + 32u * cb, u);
         tmem_wait_ld();
-        uint4 pk[4];
-        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+        uint4 pkd[4];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pw[i] = pack_bf16(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
         if (row < T) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cb);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+          for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
         }
       }
       if (row < T) lse_out[(size_t)bh * T + row] = (m * scale_log2 + __log2f(l)) * 0.69314718055994531f;

@@ -39,6 +39,24 @@ struct Tile {
     return smem_desc<ROW_BYTES>(addr, CHUNK_BYTES, 8 * ROW_BYTES);
   }
 
+  // Lean forms for the MMA issue loop: the descriptor of K-step 0 is computed once per
+  // tile, and K-step k adds a compile-time offset (in the 16-byte units of the start
+  // address field; shared-memory addresses stay below 2^18, so the add never carries
+  // out of that 14-bit field). A single thread issues every MMA of the CTA, and at
+  // K = 16 per instruction its own instruction count bounds the tensor-core rate.
+  static __device__ __forceinline__ uint64_t desc_kmajor0(uint32_t base) {
+    return smem_desc<ROW_BYTES>(base, 16, 8 * ROW_BYTES);
+  }
+  static __device__ __forceinline__ uint64_t desc_mnmajor0(uint32_t base) {
+    return smem_desc<ROW_BYTES>(base, CHUNK_BYTES, 8 * ROW_BYTES);
+  }
+  static __host__ __device__ constexpr uint64_t kmajor_off(int k) {
+    return (uint64_t)(((16 * k) / CHUNK_ELEMS) * CHUNK_BYTES + ((16 * k) % CHUNK_ELEMS) * 2) >> 4;
+  }
+  static __host__ __device__ constexpr uint64_t mnmajor_off(int k) { return (uint64_t)(16 * k * ROW_BYTES) >> 4; }
+  // descriptor offset of a tile that starts `bytes` later
+  static __host__ __device__ constexpr uint64_t bytes_off(uint32_t bytes) { return bytes >> 4; }
+
   // Issue the TMA loads of one tile (rows row0..row0+127 of slice bh).
   static __device__ __forceinline__ void load(uint32_t dst, const CUtensorMap* m, int row0, int bh,
                                               uint32_t bar) {
@@ -46,6 +64,27 @@ struct Tile {
     for (int c = 0; c < NCHUNK; ++c) tma_load_3d(dst + c * CHUNK_BYTES, m, c * CHUNK_ELEMS, row0, bh, bar);
   }
 };
+
+// D[tmem] (+)= A[smem] B[smem] over NK K-steps of 16, both operands K-major (contraction
+// over the head dimension d). acc0: accumulate at K-step 0.
+template <class TL, int NK>
+__device__ __forceinline__ void mma_chain_ss(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc, uint32_t acc0) {
+#pragma unroll
+  for (int k = 0; k < NK; ++k) mma_ss(d, a0 + TL::kmajor_off(k), b0 + TL::kmajor_off(k), idesc, k ? 1u : acc0);
+}
+
+// D[tmem] (+)= A[tmem] B[smem] over 8 K-steps of 16 (K = 128 tile rows), B MN-major.
+// The A operand's K-step k starts at TMEM column a0 + 8k, or, with HALVES (bf16
+// K-columns written by two warpgroups into the first 32 columns of their own 64-column
+// halves of a 128-column fp32 region), at a0 + 8(k mod 4) + 64(k div 4).
+template <class TL, bool HALVES>
+__device__ __forceinline__ void mma_chain_ts(uint32_t d, uint32_t a0, uint64_t b0, uint32_t idesc, uint32_t acc0) {
+#pragma unroll
+  for (int k = 0; k < kTileRows / 16; ++k) {
+    const uint32_t col = HALVES ? 8u * (k & 3) + 64u * (k >> 2) : 8u * k;
+    mma_ts(d, a0 + col, b0 + TL::mnmajor_off(k), idesc, k ? 1u : acc0);
+  }
+}
 
 // The TMEM lane offset of this warp within its warpgroup (a warp may only access
 // the 32-lane quarter numbered warp_id % 4).
