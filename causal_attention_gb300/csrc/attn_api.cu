@@ -62,6 +62,21 @@ uint32_t* error_word_ptr(cudaError_t* e) {
   return ptrs[dev];
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms(cudaError_t* e) {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  *e = cudaGetDevice(&dev);
+  if (*e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    *e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (*e != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime so that the
 // library does not link libcuda (it loads on machines without a GPU driver).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -169,6 +184,8 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   cudaError_t e;
   a->err = error_word_ptr(&e);
   if (!a->err) return cuda_fail(e, ATTN_ERR_CUDA);
+  a->num_sms = num_sms(&e);
+  if (a->num_sms <= 0) return cuda_fail(e, ATTN_ERR_CUDA);
   if (need_maps) {
     ATTN_TRY(make_map(&maps[0], q, a->BH, T, d));
     ATTN_TRY(make_map(&maps[1], k, a->BH, T, d));
@@ -262,6 +279,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   cudaError_t e;
   a.err = error_word_ptr(&e);
   if (!a.err) return cuda_fail(e, ATTN_ERR_CUDA);
+  a.num_sms = num_sms(&e);
+  if (a.num_sms <= 0) return cuda_fail(e, ATTN_ERR_CUDA);
   return launched(launch_fwd(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -96,25 +96,29 @@ template <int D>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
-  // fixed tiles (K_j, V_j for dK/dV; Q_i, dO_i for dQ)
+  // fixed tiles of a work item (K_j, V_j for dK/dV; Q_i, dO_i for dQ)
   static constexpr int OFF_FIX = 0;
   // per stage: two tiles (+ for dK/dV, 128 fp32 -LSE*log2e and 128 fp32 D)
   static constexpr int STAGE_BYTES = 2 * TL::BYTES + 1024;
   static constexpr int OFF_STAGE = OFF_FIX + 2 * TL::BYTES;
   static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
-  // barriers: fix_full, st_full[S], st_empty[S], s_full, dp_full, p_full, ds_full, done,
-  // drain, s_free, dp_free, dv_done, dk_done (dq_done shares dk_done's slot), drain2
-  static constexpr int NBAR = 1 + 2 * STAGES + 11;
-  // The dK/dV kernel gives P^T and dS^T their own TMEM columns when they fit (d <= 64).
-  static constexpr bool SEP_DKDV = D <= 64;
-  static constexpr uint32_t COL_P = 384, COL_DS = 448;
+  static constexpr int NBAR = 1 + 2 * STAGES + 14;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
   static constexpr int SMEM_RAW = OFF_MISC + 16 + 1024;
   static constexpr int SMEM_BYTES = SMEM_RAW > 116 * 1024 ? SMEM_RAW : 116 * 1024;
+  // The dK/dV kernel gives P^T and dS^T their own TMEM columns when they fit (d <= 64);
+  // then it also runs persistently with two MMA issuers.
+  static constexpr bool SEP_DKDV = D <= 64;
+  static constexpr uint32_t COL_P = 384, COL_DS = 448;
 };
 
+// Barriers (one 8-byte mbarrier each). Per work item: fix_full / fix_empty (the item's
+// fixed tiles), acc_full / acc_free (its accumulators). Per stage: st_full / st_empty.
+// Per iteration (global count over the CTA's items): s_full, dp_full (MMA results),
+// s_free, dp_free (read out by the elementwise warps), p_full, ds_full (their results
+// written to TMEM), dv_done, dk_done (the MMAs reading those results finished).
 struct BwdSmem {
   uint32_t base;
   uint8_t* gbase;
@@ -127,13 +131,15 @@ struct BwdSmem {
   __device__ uint32_t dp_full() const { return bar0 + 8u * (2 + 2 * st); }
   __device__ uint32_t p_full() const { return bar0 + 8u * (3 + 2 * st); }
   __device__ uint32_t ds_full() const { return bar0 + 8u * (4 + 2 * st); }
-  __device__ uint32_t done() const { return bar0 + 8u * (5 + 2 * st); }
+  __device__ uint32_t acc_full() const { return bar0 + 8u * (5 + 2 * st); }
   __device__ uint32_t drain() const { return bar0 + 8u * (6 + 2 * st); }
   __device__ uint32_t s_free() const { return bar0 + 8u * (7 + 2 * st); }
   __device__ uint32_t dp_free() const { return bar0 + 8u * (8 + 2 * st); }
   __device__ uint32_t dv_done() const { return bar0 + 8u * (9 + 2 * st); }
   __device__ uint32_t dk_done() const { return bar0 + 8u * (10 + 2 * st); }
   __device__ uint32_t drain2() const { return bar0 + 8u * (11 + 2 * st); }
+  __device__ uint32_t fix_empty() const { return bar0 + 8u * (12 + 2 * st); }
+  __device__ uint32_t acc_free() const { return bar0 + 8u * (13 + 2 * st); }
 };
 
 constexpr int kEwThreads = 256;  // two elementwise warpgroups
@@ -152,6 +158,7 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
   abort = reinterpret_cast<volatile int*>(s.gbase + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
     mbar_init(s.fix_full(), 1);
+    mbar_init(s.fix_empty(), 1);
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(s.st_full(i), 1);
       mbar_init(s.st_empty(i), 1);
@@ -160,12 +167,13 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     mbar_init(s.dp_full(), 1);
     mbar_init(s.p_full(), kEwThreads);
     mbar_init(s.ds_full(), kEwThreads);
-    mbar_init(s.done(), 1);
-    mbar_init(s.drain(), 1);
     mbar_init(s.s_free(), kEwThreads);
     mbar_init(s.dp_free(), kEwThreads);
     mbar_init(s.dv_done(), 1);
     mbar_init(s.dk_done(), 1);
+    mbar_init(s.acc_full(), 1);
+    mbar_init(s.acc_free(), kEwThreads);
+    mbar_init(s.drain(), 1);
     mbar_init(s.drain2(), 1);
     *abort = 0;
     fence_barrier_init();
@@ -189,20 +197,37 @@ __device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t (
   d4[1] = pk[1];
 }
 
+// Work items of a persistent kernel, sorted longest first, dealt to the CTAs in a snake
+// order (round r goes left to right when r is even, right to left when odd) so that every
+// CTA gets about the same total work.
+struct Sched {
+  int n_items;
+  __device__ __forceinline__ int item(int r) const {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int u = r * G + ((r & 1) ? (G - 1 - c) : c);
+    return u < n_items ? u : -1;
+  }
+};
+
 // Producer drain after an abort: every copy issued must land before the CTA exits.
-__device__ __forceinline__ void drain_stages(const BwdSmem& sm, int issued, int st, const Abort& ab) {
-  mbar_wait_drain(sm.fix_full(), 0, ab);
-  for (int it = max(0, issued - st); it < issued; ++it) mbar_wait_drain(sm.st_full(it % st), (it / st) & 1, ab);
+__device__ __forceinline__ void drain_loads(const BwdSmem& sm, int fix_issued, int st_issued, int st,
+                                            const Abort& ab) {
+  if (fix_issued > 0) mbar_wait_drain(sm.fix_full(), (fix_issued - 1) & 1, ab);
+  for (int g = max(0, st_issued - st); g < st_issued; ++g) mbar_wait_drain(sm.st_full(g % st), (g / st) & 1, ab);
 }
 
 // ---------------------------------------------------------------------------
 // 2. dK / dV
 // ---------------------------------------------------------------------------
-// MMA issue order per query tile i (S, dP, P, dS below are the transposed tiles):
-//   S_0, dP_0 | P_0 ready: dV_0, S_1 | dS_0 ready: dK_0, dP_1 | P_1 ready: dV_1, S_2 | ...
-// so the tensor core runs dV_i and S_{i+1} while the elementwise warps compute dS_i,
-// and dK_i and dP_{i+1} while they compute P_{i+1}. S_{i+1} overwrites the region that
-// held P_i only after dV_i (same-thread tcgen05 MMAs execute in issue order).
+// Work item = one 128-key tile j of one (b, h); its iterations run over the query tiles
+// i (i >= j when causal). With separate P^T / dS^T columns (d <= 64) the kernel is
+// persistent and two threads issue MMAs:
+//   warp 9:  S_i (= S^T, K_j Q_i^T) as soon as S_{i-1} was read out, dP_i likewise;
+//   warp 10: dV += P_i^T dO_i once P_i^T is in TMEM, dK += dS_i^T Q_i once dS_i^T is.
+// The next item's S and dP run while the elementwise warps store this item's dK, dV.
+// At d = 128 (TMEM full, P^T / dS^T written over S^T / dP^T) one thread issues in the
+// order S_0, dP_0 | P_0: dV_0, S_1 | dS_0: dK_0, dP_1 | ..., which relies on same-thread
+// MMAs executing in issue order, and each CTA takes one item.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -213,6 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = BwdCfg<D>;
   using TL = Tile<D>;
   constexpr int ST = C::STAGES;
+  constexpr bool SEP = C::SEP_DKDV;
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
@@ -222,10 +248,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_q = (T + kTileRows - 1) / kTileRows;
-  const int kt = (int)(blockIdx.x / BH);  // key tile: small j = most work, launched first
-  const int bh = (int)(blockIdx.x % BH);
-  const int i0 = CAUSAL ? kt : 0;
-  const int n_it = n_q - i0;
+  const Sched sched{n_q * BH};
+  // item u: key tile u / BH (small j = most work first), slice u % BH
+  auto key_tile = [&](int u) { return u / BH; };
+  auto n_iters = [&](int u) { return n_q - (CAUSAL ? key_tile(u) : 0); };
 
   const uint32_t sK = sm.base + C::OFF_FIX, sV = sK + TL::BYTES;
   auto sQ = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
@@ -233,30 +259,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sL = [&](int s) { return sQ(s) + 2 * TL::BYTES; };  // 128 fp32 -LSE*log2e, then 128 fp32 D
 
   if (warp == 8) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(sm.fix_full(), 2 * TL::BYTES);
-      TL::load(sK, &tmK, kt * kTileRows, bh, sm.fix_full());
-      TL::load(sV, &tmV, kt * kTileRows, bh, sm.fix_full());
-      int issued = 0;
       bool ok = true;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % ST, n = it / ST, qi = i0 + it;
-        if (it >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
-        mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES + 1024);
-        TL::load(sQ(s), &tmQ, qi * kTileRows, bh, sm.st_full(s));
-        TL::load(sdO(s), &tmdO, qi * kTileRows, bh, sm.st_full(s));
-        const size_t woff = (size_t)bh * T_pad + (size_t)qi * kTileRows;
-        bulk_load(sL(s), ws_nlse2 + woff, 512, sm.st_full(s));
-        bulk_load(sL(s) + 512, ws_D + woff, 512, sm.st_full(s));
-        issued = it + 1;
+      int g = 0, r = 0, fix_issued = 0;
+      for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
+        const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
+        if (r > 0 && !(ok = mbar_wait(sm.fix_empty(), (r - 1) & 1, ab, kErrTimeoutLoad))) break;
+        ++fix_issued;
+        mbar_arrive_expect_tx(sm.fix_full(), 2 * TL::BYTES);
+        TL::load(sK, &tmK, kt * kTileRows, bh, sm.fix_full());
+        TL::load(sV, &tmV, kt * kTileRows, bh, sm.fix_full());
+        for (int it = 0; it < n_it; ++it, ++g) {
+          const int s = g % ST, n = g / ST, qi = i0 + it;
+          if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
+          mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES + 1024);
+          TL::load(sQ(s), &tmQ, qi * kTileRows, bh, sm.st_full(s));
+          TL::load(sdO(s), &tmdO, qi * kTileRows, bh, sm.st_full(s));
+          const size_t woff = (size_t)bh * T_pad + (size_t)qi * kTileRows;
+          bulk_load(sL(s), ws_nlse2 + woff, 512, sm.st_full(s));
+          bulk_load(sL(s) + 512, ws_D + woff, 512, sm.st_full(s));
+        }
       }
-      if (!ok) drain_stages(sm, issued, ST, ab);
+      if (!ok) drain_loads(sm, fix_issued, g, ST, ab);
     }
   } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer (S, dP)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
@@ -272,252 +304,211 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_dP = [&](int s) {  // dP^T = V_j dO_i^T
         mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dVk, dOk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
       };
-      bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma) && mbar_wait(sm.st_full(0), 0, ab, kErrTimeoutMma);
-      if (ok) {
-        tc_fence_after();
-        issue_S(0);
-        mma_commit(sm.s_full());
-        issue_dP(0);
-        mma_commit(sm.dp_full());
-      }
-      for (int it = 0; it + 1 < n_it && ok && C::SEP_DKDV; ++it) {
-        // separate P^T / dS^T columns: S_{i+1} and dP_{i+1} start as soon as S_i and
-        // dP_i have been read into registers (dV and dK are issued by warp 10)
-        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
-        if (!(ok = mbar_wait(sm.s_free(), it & 1, ab, kErrTimeoutMma))) break;
-        if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        issue_S(s1);
-        mma_commit(sm.s_full());
-        if (!(ok = mbar_wait(sm.dp_free(), it & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        issue_dP(s1);
-        mma_commit(sm.dp_full());
-      }
-      for (int it = 0; it < n_it && ok && !C::SEP_DKDV; ++it) {
-        const int s = it % ST;
-        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
-        const bool more = it + 1 < n_it;
-        if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        // dV += P^T dO_i (M = keys, N = d, K = queries)
-        mma_chain_ts<TL, true>(tDV, tS, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
-        if (more) {
-          if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
+      bool ok = true;
+      int g = 0;
+      for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
+        const int n_it = n_iters(u);
+        if (!(ok = mbar_wait(sm.fix_full(), r & 1, ab, kErrTimeoutMma))) break;
+        if constexpr (SEP) {
+          for (int it = 0; it < n_it; ++it, ++g) {
+            const int s = g % ST;
+            if (g > 0 && !(ok = mbar_wait(sm.s_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;
+            if (!(ok = mbar_wait(sm.st_full(s), (g / ST) & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            issue_S(s);
+            mma_commit(sm.s_full());
+            if (g > 0 && !(ok = mbar_wait(sm.dp_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            issue_dP(s);
+            mma_commit(sm.dp_full());
+            if (it == n_it - 1) mma_commit(sm.fix_empty());  // K_j, V_j are no longer read
+          }
+        } else {
+          // P^T / dS^T written over S^T / dP^T: same-thread issue order is the guard
+          if (!(ok = mbar_wait(sm.st_full(g % ST), (g / ST) & 1, ab, kErrTimeoutMma))) break;
           tc_fence_after();
-          issue_S(s1);
+          issue_S(g % ST);
           mma_commit(sm.s_full());
-        }
-        if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        // dK += dS^T Q_i
-        mma_chain_ts<TL, true>(tDK, tDP, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
-        mma_commit(sm.st_empty(s));
-        if (more) {
-          issue_dP(s1);
+          issue_dP(g % ST);
           mma_commit(sm.dp_full());
+          for (int it = 0; it < n_it; ++it, ++g) {
+            const int s = g % ST, s1 = (g + 1) % ST;
+            const bool more = it + 1 < n_it;
+            if (!(ok = mbar_wait(sm.p_full(), g & 1, ab, kErrTimeoutMma))) break;
+            if (it == 0 && r > 0 && !(ok = mbar_wait(sm.acc_free(), (r - 1) & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            mma_chain_ts<TL, true>(tDV, tS, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+            if (more) {
+              if (!(ok = mbar_wait(sm.st_full(s1), ((g + 1) / ST) & 1, ab, kErrTimeoutMma))) break;
+              tc_fence_after();
+              issue_S(s1);
+              mma_commit(sm.s_full());
+            }
+            if (!(ok = mbar_wait(sm.ds_full(), g & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            mma_chain_ts<TL, true>(tDK, tDP, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+            mma_commit(sm.st_empty(s));
+            if (more) {
+              issue_dP(s1);
+              mma_commit(sm.dp_full());
+            }
+          }
+          if (!ok) break;
+          mma_commit(sm.fix_empty());
+          mma_commit(sm.acc_full());
         }
       }
       if (!ok) {
         mma_commit(sm.drain());
         mbar_wait_drain(sm.drain(), 0, ab);
-      } else if (!C::SEP_DKDV) {
-        mma_commit(sm.done());
       }
     }
   } else if (warp == 10) {
-    // second issuer: dV_i and dK_i, each as soon as its elementwise operand is in TMEM
-    if (lane == 0 && C::SEP_DKDV) {
+    // ------------------------------------------------------------ MMA issuer (dV, dK)
+    if (lane == 0 && SEP) {
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
       const uint64_t dQm0 = TL::desc_mnmajor0(sQ(0)), dOm0 = TL::desc_mnmajor0(sdO(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       bool ok = true;
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it % ST;
-        if (!(ok = mbar_wait(sm.p_full(), it & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        // dV += P^T dO_i (M = keys, N = d, K = queries)
-        mma_chain_ts<TL, false>(tDV, tmem + C::COL_P, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
-        mma_commit(sm.dv_done());
-        if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        // dK += dS^T Q_i
-        mma_chain_ts<TL, false>(tDK, tmem + C::COL_DS, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
-        mma_commit(sm.dk_done());
-        // S_i and dP_i (warp 9) were read out before P_i / dS_i were signalled, so this
-        // commit covers every MMA that reads stage s
-        mma_commit(sm.st_empty(s));
+      int g = 0;
+      for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
+        const int n_it = n_iters(u);
+        for (int it = 0; it < n_it; ++it, ++g) {
+          const int s = g % ST;
+          if (!(ok = mbar_wait(sm.p_full(), g & 1, ab, kErrTimeoutMma))) break;
+          // the accumulators still hold the previous item until its epilogue read them
+          if (it == 0 && r > 0 && !(ok = mbar_wait(sm.acc_free(), (r - 1) & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          // dV += P^T dO_i (M = keys, N = d, K = queries)
+          mma_chain_ts<TL, false>(tDV, tmem + C::COL_P, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+          mma_commit(sm.dv_done());
+          if (!(ok = mbar_wait(sm.ds_full(), g & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          // dK += dS^T Q_i
+          mma_chain_ts<TL, false>(tDK, tmem + C::COL_DS, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+          mma_commit(sm.dk_done());
+          // S_i and dP_i (warp 9) were read out before P_i / dS_i were signalled, so this
+          // commit covers every MMA that reads stage s
+          mma_commit(sm.st_empty(s));
+        }
+        if (ok) mma_commit(sm.acc_full());
       }
-      if (ok) {
-        mma_commit(sm.done());
-      } else {
+      if (!ok) {
         mma_commit(sm.drain2());
         mbar_wait_drain(sm.drain2(), 0, ab);
       }
     }
   } else {
-    // elementwise: thread owns key row kt*128 + r and query columns [64*hc, 64*hc + 64)
+    // ------------------------------------------------------------ elementwise
+    // thread owns key row kt*128 + r and query columns [64*hc, 64*hc + 64)
     const int hc = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lo = warp_lane_base();
     const uint32_t tSh = tmem + lo + 64u * hc, tDPh = tmem + lo + 128u + 64u * hc;
+    const uint32_t tP = tmem + lo + (SEP ? C::COL_P + 32u * hc : 64u * hc);
+    const uint32_t tDS = tmem + lo + (SEP ? C::COL_DS + 32u * hc : 128u + 64u * hc);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
-    for (int it = 0; it < n_it && C::SEP_DKDV; ++it) {
-      const int s = it % ST, n = it / ST, qi = i0 + it;
-      if (!(ok = mbar_wait_warp(sm.s_full(), it & 1, ab, kErrTimeoutElem))) break;
-      if (!(ok = mbar_wait_warp(sm.st_full(s), n & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-      const float* nl = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base)) + 64 * hc;
-      const float* dd = nl + 128;
-      const bool diag = CAUSAL && qi == kt;
-      float p[64];
-      {
-        uint32_t u[64];
-        tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(sm.s_free());  // S^T_i is in registers
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2,
-                                    *reinterpret_cast<const uint64_t*>(nl + 2 * i));
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          p[2 * i] = ex2(x0);
-          p[2 * i + 1] = ex2(x1);
-        }
-      }
-      if (diag) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (64 * hc + c < r) p[c] = 0.f;
-      }
-      {
-        uint32_t pp[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
-        // dV_{i-1} reads the P^T columns: it must be complete before they are rewritten
-        if (it > 0 && !(ok = mbar_wait_warp(sm.dv_done(), (it - 1) & 1, ab, kErrTimeoutElem))) break;
+    int g = 0;
+    for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
+      const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
+      for (int it = 0; it < n_it; ++it, ++g) {
+        const int s = g % ST, qi = i0 + it;
+        if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
+        if (!(ok = mbar_wait_warp(sm.st_full(s), (g / ST) & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
-        const uint32_t tP = tmem + lo + C::COL_P + 32u * hc;
-        tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pp[0]));
-        tmem_st16(tP + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pp[16]));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(sm.p_full());
-      if (!(ok = mbar_wait_warp(sm.dp_full(), it & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-      {
-        uint32_t u[64];
-        tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_wait_ld();
+        const float* nl = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base)) + 64 * hc;
+        const float* dd = nl + 128;
+        // ---- P^T = exp2(S^T * scale*log2e - LSE_i*log2e), kept in fp32 for dS
+        float p[64];
+        {
+          uint32_t u2[64];
+          tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
+          tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          tmem_wait_ld();
+          if (SEP) {
+            tc_fence_before();
+            mbar_arrive(sm.s_free());  // S^T_i is in registers
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), c2,
+                                      *reinterpret_cast<const uint64_t*>(nl + 2 * i));
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            p[2 * i] = ex2(x0);
+            p[2 * i + 1] = ex2(x1);
+          }
+        }
+        if (CAUSAL && qi == kt) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (64 * hc + c < r) p[c] = 0.f;
+        }
+        {
+          uint32_t pp[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+          // the previous dV read the P^T columns: it must be complete before they are rewritten
+          if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dv_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
+          tc_fence_after();
+          tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pp[0]));
+          tmem_st16(tP + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pp[16]));
+        }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(sm.dp_free());  // dP^T_i is in registers
-        uint32_t pd[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint64_t g = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
-                                    f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])),
-                                           *reinterpret_cast<const uint64_t*>(dd + 2 * i)));
-          float g0, g1;
-          f2_unpack(g, g0, g1);
-          pd[i] = pack_bf16(g0, g1);
-        }
-        if (it > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (it - 1) & 1, ab, kErrTimeoutElem))) break;
+        mbar_arrive(sm.p_full());
+        // ---- dS^T = P^T * (dP^T - D_i)
+        if (!(ok = mbar_wait_warp(sm.dp_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
-        const uint32_t tDS = tmem + lo + C::COL_DS + 32u * hc;
-        tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
-        tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(sm.ds_full());
-    }
-    for (int it = 0; it < n_it && ok && !C::SEP_DKDV; ++it) {
-      const int s = it % ST, n = it / ST, qi = i0 + it;
-      if (!(ok = mbar_wait_warp(sm.s_full(), it & 1, ab, kErrTimeoutElem))) break;
-      if (!(ok = mbar_wait_warp(sm.st_full(s), n & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-      const float* nl = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base)) + 64 * hc;
-      const float* dd = nl + 128;
-      const bool diag = CAUSAL && qi == kt;
-      // ---- P^T = exp2(S^T * scale*log2e - LSE_i*log2e), kept in fp32 for dS
-      float p[64];
-      {
-        uint32_t u[64];
-        tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_wait_ld();
+        {
+          uint32_t u2[64];
+          tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
+          tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          tmem_wait_ld();
+          if (SEP) {
+            tc_fence_before();
+            mbar_arrive(sm.dp_free());  // dP^T_i is in registers
+          }
+          uint32_t pd[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2,
-                                    *reinterpret_cast<const uint64_t*>(nl + 2 * i));
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          p[2 * i] = ex2(x0);
-          p[2 * i + 1] = ex2(x1);
+          for (int i = 0; i < 32; ++i) {
+            const uint64_t gg = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
+                                       f2_sub(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])),
+                                              *reinterpret_cast<const uint64_t*>(dd + 2 * i)));
+            float g0, g1;
+            f2_unpack(gg, g0, g1);
+            pd[i] = pack_bf16(g0, g1);
+          }
+          if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
+          tc_fence_after();
+          tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
+          tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(sm.ds_full());
       }
-      if (diag) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (64 * hc + c < r) p[c] = 0.f;
-      }
-      {
-        uint32_t pp[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
-        tmem_st16(tSh, *reinterpret_cast<uint32_t(*)[16]>(&pp[0]));
-        tmem_st16(tSh + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pp[16]));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(sm.p_full());
-      // ---- dS^T = P^T * (dP^T - D_i)
-      if (!(ok = mbar_wait_warp(sm.dp_full(), it & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t u[32];
-        tmem_ld32(tDPh + 32u * cb, u);
-        tmem_wait_ld();
-        uint32_t pd[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = 32 * cb + 2 * i;
-          const uint64_t g = f2_mul(f2_pack(p[c], p[c + 1]),
-                                    f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])),
-                                           *reinterpret_cast<const uint64_t*>(dd + c)));
-          float g0, g1;
-          f2_unpack(g, g0, g1);
-          pd[i] = pack_bf16(g0, g1);
-        }
-        tmem_st16(tDPh + 16u * cb, pd);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(sm.ds_full());
-    }
-    if (ok && mbar_wait_warp(sm.done(), 0, ab, kErrTimeoutElem)) {
+      // ---- epilogue: dV, dK (x scale) of this key tile; then free the accumulators
+      if (!ok || !(ok = mbar_wait_warp(sm.acc_full(), ri & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
       const int key = kt * kTileRows + r;
       const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)D;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
         const int col = hc * (D / 2) + 16 * cb;
-        uint32_t u[16];
-        tmem_ld16(tDV + (uint32_t)col, u);
+        uint32_t v16[16], k16[16];
+        tmem_ld16(tDV + (uint32_t)col, v16);
+        tmem_ld16(tDK + (uint32_t)col, k16);
         tmem_wait_ld();
-        if (key < T) store_row16(dv + ((size_t)bh * T + key) * D + col, u, 1.f);
-        tmem_ld16(tDK + (uint32_t)col, u);
-        tmem_wait_ld();
-        if (key < T) store_row16(dk + ((size_t)bh * T + key) * D + col, u, scale);
+        if (key < T) {
+          store_row16(dv + ((size_t)bh * T + key) * D + col, v16, 1.f);
+          store_row16(dk + ((size_t)bh * T + key) * D + col, k16, scale);
+        }
       }
+      tc_fence_before();
+      mbar_arrive(sm.acc_free());
     }
   }
 
@@ -532,10 +523,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------------------
 // 3. dQ
 // ---------------------------------------------------------------------------
-// MMA issue order per key tile j: S_0, dP_0 | S_0 read out: S_1 | dP_0 read out: dP_1 |
-// dS_0 ready: dQ += dS_0 K_0 | S_1 read out: S_2 | ... The elementwise warps release S_j
-// and dP_j as soon as they are in registers, and dS has its own 64 TMEM columns (after
-// the dQ accumulator), so the next tile's MMAs run while they compute.
+// Work item = one 128-query tile i of one (b, h); its iterations run over the key tiles
+// j (j <= i when causal). Persistent, two MMA issuers:
+//   warp 9:  S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
+//   warp 10: dQ += dS_j K_j once dS_j (its own 64 TMEM columns) is written.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -555,69 +546,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_k = (T + kTileRows - 1) / kTileRows;
-  const int qt = n_k - 1 - (int)(blockIdx.x / BH);  // largest query tile (most work) first
-  const int bh = (int)(blockIdx.x % BH);
-  const int n_it = CAUSAL ? qt + 1 : n_k;
+  const Sched sched{n_k * BH};
+  // item u: query tile n_k - 1 - u / BH (largest, i.e. most work, first), slice u % BH
+  auto query_tile = [&](int u) { return n_k - 1 - u / BH; };
+  auto n_iters = [&](int u) { return CAUSAL ? query_tile(u) + 1 : n_k; };
 
   const uint32_t sQ = sm.base + C::OFF_FIX, sdO = sQ + TL::BYTES;
   auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sV = [&](int s) { return sK(s) + TL::BYTES; };
 
   if (warp == 8) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(sm.fix_full(), 2 * TL::BYTES);
-      TL::load(sQ, &tmQ, qt * kTileRows, bh, sm.fix_full());
-      TL::load(sdO, &tmdO, qt * kTileRows, bh, sm.fix_full());
-      int issued = 0;
       bool ok = true;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % ST, n = it / ST;
-        if (it >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
-        mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES);
-        TL::load(sK(s), &tmK, it * kTileRows, bh, sm.st_full(s));
-        TL::load(sV(s), &tmV, it * kTileRows, bh, sm.st_full(s));
-        issued = it + 1;
+      int g = 0, r = 0, fix_issued = 0;
+      for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
+        const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
+        if (r > 0 && !(ok = mbar_wait(sm.fix_empty(), (r - 1) & 1, ab, kErrTimeoutLoad))) break;
+        ++fix_issued;
+        mbar_arrive_expect_tx(sm.fix_full(), 2 * TL::BYTES);
+        TL::load(sQ, &tmQ, qt * kTileRows, bh, sm.fix_full());
+        TL::load(sdO, &tmdO, qt * kTileRows, bh, sm.fix_full());
+        for (int it = 0; it < n_it; ++it, ++g) {
+          const int s = g % ST, n = g / ST;
+          if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
+          mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES);
+          TL::load(sK(s), &tmK, it * kTileRows, bh, sm.st_full(s));
+          TL::load(sV(s), &tmV, it * kTileRows, bh, sm.st_full(s));
+        }
       }
-      if (!ok) drain_stages(sm, issued, ST, ab);
+      if (!ok) drain_loads(sm, fix_issued, g, ST, ab);
     }
   } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer (S, dP)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tS = tmem, tDP = tmem + 128u;
-      // K-step-0 descriptors, computed once; stage s adds s stages
       const uint64_t dQk = TL::desc_kmajor0(sQ), dOk = TL::desc_kmajor0(sdO);
-      const uint64_t dKk0 = TL::desc_kmajor0(sK(0)), dVk0 = TL::desc_kmajor0(sV(0)), dKm0 = TL::desc_mnmajor0(sK(0));
+      const uint64_t dKk0 = TL::desc_kmajor0(sK(0)), dVk0 = TL::desc_kmajor0(sV(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
-      auto issue_S = [&](int s) {  // S = Q_i K_j^T (M = queries, N = keys, K = d)
-        mma_chain_ss<TL, TL::KSTEPS_D>(tS, dQk, dKk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
-      };
-      auto issue_dP = [&](int s) {  // dP = dO_i V_j^T
-        mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
-      };
-      bool ok = mbar_wait(sm.fix_full(), 0, ab, kErrTimeoutMma) && mbar_wait(sm.st_full(0), 0, ab, kErrTimeoutMma);
-      if (ok) {
-        tc_fence_after();
-        issue_S(0);
-        mma_commit(sm.s_full());
-        issue_dP(0);
-        mma_commit(sm.dp_full());
-      }
-      for (int it = 0; it + 1 < n_it && ok; ++it) {
-        const int s1 = (it + 1) % ST, n1 = (it + 1) / ST;
-        if (!(ok = mbar_wait(sm.s_free(), it & 1, ab, kErrTimeoutMma))) break;  // S_it read out
-        if (!(ok = mbar_wait(sm.st_full(s1), n1 & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        issue_S(s1);
-        mma_commit(sm.s_full());
-        if (!(ok = mbar_wait(sm.dp_free(), it & 1, ab, kErrTimeoutMma))) break;  // dP_it read out
-        tc_fence_after();
-        issue_dP(s1);
-        mma_commit(sm.dp_full());
+      bool ok = true;
+      int g = 0;
+      for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
+        const int n_it = n_iters(u);
+        if (!(ok = mbar_wait(sm.fix_full(), r & 1, ab, kErrTimeoutMma))) break;
+        for (int it = 0; it < n_it; ++it, ++g) {
+          const int s = g % ST;
+          if (g > 0 && !(ok = mbar_wait(sm.s_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // S read out
+          if (!(ok = mbar_wait(sm.st_full(s), (g / ST) & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          // S = Q_i K_j^T (M = queries, N = keys, K = d)
+          mma_chain_ss<TL, TL::KSTEPS_D>(tS, dQk, dKk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
+          mma_commit(sm.s_full());
+          if (g > 0 && !(ok = mbar_wait(sm.dp_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // dP read out
+          tc_fence_after();
+          // dP = dO_i V_j^T
+          mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
+          mma_commit(sm.dp_full());
+          if (it == n_it - 1) mma_commit(sm.fix_empty());  // Q_i, dO_i are no longer read
+        }
       }
       if (!ok) {
         mma_commit(sm.drain());
@@ -625,112 +616,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == 10) {
-    // second issuer: dQ += dS_j K_j as soon as dS_j is in TMEM
+    // ------------------------------------------------------------ MMA issuer (dQ)
     if (lane == 0) {
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tDQ = tmem + 256u, tDS = tmem + 256u + (uint32_t)D;
       const uint64_t dKm0 = TL::desc_mnmajor0(sK(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       bool ok = true;
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it % ST;
-        if (!(ok = mbar_wait(sm.ds_full(), it & 1, ab, kErrTimeoutMma))) break;
-        tc_fence_after();
-        // dQ += dS K_j (M = queries, N = d, K = keys); dS has its own 64 columns
-        mma_chain_ts<TL, false>(tDQ, tDS, dKm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
-        mma_commit(sm.dk_done());  // "dQ_it done": the dS columns may be rewritten
-        // S_j and dP_j (warp 9) were read out before dS_j was signalled
-        mma_commit(sm.st_empty(s));
+      int g = 0;
+      for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
+        const int n_it = n_iters(u);
+        for (int it = 0; it < n_it; ++it, ++g) {
+          const int s = g % ST;
+          if (!(ok = mbar_wait(sm.ds_full(), g & 1, ab, kErrTimeoutMma))) break;
+          if (it == 0 && r > 0 && !(ok = mbar_wait(sm.acc_free(), (r - 1) & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          // dQ += dS K_j (M = queries, N = d, K = keys); dS has its own 64 columns
+          mma_chain_ts<TL, false>(tDQ, tDS, dKm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+          mma_commit(sm.dk_done());  // "dQ_j done": the dS columns may be rewritten
+          // S_j and dP_j (warp 9) were read out before dS_j was signalled
+          mma_commit(sm.st_empty(s));
+        }
+        if (ok) mma_commit(sm.acc_full());
       }
-      if (ok) {
-        mma_commit(sm.done());
-      } else {
+      if (!ok) {
         mma_commit(sm.drain2());
         mbar_wait_drain(sm.drain2(), 0, ab);
       }
     }
   } else {
-    // elementwise: thread owns query row qt*128 + r and key columns [64*hc, 64*hc + 64)
+    // ------------------------------------------------------------ elementwise
+    // thread owns query row qt*128 + r and key columns [64*hc, 64*hc + 64)
     const int hc = warp >> 2;
     const int r = threadIdx.x & 127;
-    const int row = qt * kTileRows + r;
     const uint32_t lo = warp_lane_base();
     const uint32_t tSh = tmem + lo + 64u * hc, tDPh = tmem + lo + 128u + 64u * hc;
-    const float nl = ws_nlse2[(size_t)bh * T_pad + row];
-    const float Dr = ws_D[(size_t)bh * T_pad + row];
-    const uint64_t c2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(nl, nl), D2 = f2_pack(Dr, Dr);
+    const uint32_t tDS = tmem + lo + 256u + (uint32_t)D + 32u * hc;
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      if (!(ok = mbar_wait_warp(sm.s_full(), it & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-      float p[64];
-      {
-        uint32_t u[64];
-        tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(sm.s_free());  // S_it is in registers: the tensor core may overwrite it
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), c2, nl2);
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          p[2 * i] = ex2(x0);
-          p[2 * i + 1] = ex2(x1);
-        }
-      }
-      if (CAUSAL && it == qt) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (64 * hc + c > r) p[c] = 0.f;
-      }
-      if (!CAUSAL) {
-        const int lim = T - it * kTileRows - 64 * hc;  // key columns >= lim are padding
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c >= lim) p[c] = 0.f;
-      }
-      if (!(ok = mbar_wait_warp(sm.dp_full(), it & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-      {
-        uint32_t u[64];
-        tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(sm.dp_free());  // dP_it is in registers
-        uint32_t pd[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint64_t g = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
-                                    f2_sub(f2_pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), D2));
-          float g0, g1;
-          f2_unpack(g, g0, g1);
-          pd[i] = pack_bf16(g0, g1);
-        }
-        // dQ_{it-1} reads the dS columns: it must be complete before they are rewritten
-        if (it > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (it - 1) & 1, ab, kErrTimeoutElem))) break;
+    int g = 0;
+    for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
+      const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
+      const int row = qt * kTileRows + r;
+      const float nl = ws_nlse2[(size_t)bh * T_pad + row];
+      const float Dr = ws_D[(size_t)bh * T_pad + row];
+      const uint64_t nl2 = f2_pack(nl, nl), D2 = f2_pack(Dr, Dr);
+      for (int it = 0; it < n_it; ++it, ++g) {
+        if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
-        const uint32_t tDS = tmem + lo + 256u + (uint32_t)D + 32u * hc;
-        tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
-        tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
+        float p[64];
+        {
+          uint32_t u2[64];
+          tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
+          tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(sm.s_free());  // S_j is in registers: the tensor core may overwrite it
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), c2, nl2);
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            p[2 * i] = ex2(x0);
+            p[2 * i + 1] = ex2(x1);
+          }
+        }
+        if (CAUSAL && it == qt) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (64 * hc + c > r) p[c] = 0.f;
+        }
+        if (!CAUSAL) {
+          const int lim = T - it * kTileRows - 64 * hc;  // key columns >= lim are padding
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c >= lim) p[c] = 0.f;
+        }
+        if (!(ok = mbar_wait_warp(sm.dp_full(), g & 1, ab, kErrTimeoutElem))) break;
+        tc_fence_after();
+        {
+          uint32_t u2[64];
+          tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
+          tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(sm.dp_free());  // dP_j is in registers
+          uint32_t pd[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint64_t gg = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
+                                       f2_sub(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), D2));
+            float g0, g1;
+            f2_unpack(gg, g0, g1);
+            pd[i] = pack_bf16(g0, g1);
+          }
+          // the previous dQ MMA read the dS columns: it must be complete before they are rewritten
+          if (g > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
+          tc_fence_after();
+          tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
+          tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(sm.ds_full());
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(sm.ds_full());
-    }
-    if (ok && mbar_wait_warp(sm.done(), 0, ab, kErrTimeoutElem)) {
+      // ---- epilogue: dQ (x scale) of this query tile; then free the accumulator
+      if (!ok || !(ok = mbar_wait_warp(sm.acc_full(), ri & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
       const uint32_t tDQ = tmem + lo + 256u;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
         const int col = hc * (D / 2) + 16 * cb;
-        uint32_t u[16];
-        tmem_ld16(tDQ + (uint32_t)col, u);
+        uint32_t u16[16];
+        tmem_ld16(tDQ + (uint32_t)col, u16);
         tmem_wait_ld();
-        if (row < T) store_row16(dq + ((size_t)bh * T + row) * D + col, u, scale);
+        if (row < T) store_row16(dq + ((size_t)bh * T + row) * D + col, u16, scale);
       }
+      tc_fence_before();
+      mbar_arrive(sm.acc_free());
     }
   }
 
@@ -750,7 +753,7 @@ cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.BH * a.T_pad;
   constexpr int rows_per_block = 256 / (D / 8);
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
-  const long long cap = 152LL * 8;  // grid-stride beyond 8 blocks per SM
+  const long long cap = (long long)a.num_sms * 8;  // grid-stride beyond 8 blocks per SM
   if (blocks > cap) blocks = cap;
   attn_bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.o, a.dO, a.lse, a.ws_nlse2, a.ws_D,
                                                                       a.T, a.T_pad, a.BH);
@@ -763,8 +766,10 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), BwdCfg<D>::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
-  const int n_t = (a.T + kTileRows - 1) / kTileRows;
-  kern<<<n_t * a.BH, kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
+  const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
+  // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
+  const int grid = BwdCfg<D>::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
+  kern<<<grid, kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
       *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.T, a.T_pad, a.BH, a.scale,
       a.scale * kLog2e, a.err);
   return cudaGetLastError();
@@ -776,8 +781,8 @@ cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), BwdCfg<D>::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
-  const int n_t = (a.T + kTileRows - 1) / kTileRows;
-  kern<<<n_t * a.BH, kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
+  const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
+  kern<<<min(n_items, a.num_sms), kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
       *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.scale,
       a.scale * kLog2e, a.err);
   return cudaGetLastError();

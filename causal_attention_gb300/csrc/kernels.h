@@ -17,6 +17,7 @@ struct FwdArgs {
   int T, BH, d, causal;
   float scale;
   uint32_t* err;  // device error word
+  int num_sms;    // streaming multiprocessors of the device (persistent grids)
 };
 
 // Workspace of the backward: two fp32 arrays of [B*H, T_pad], T_pad = T rounded
@@ -38,6 +39,7 @@ struct BwdArgs {
   int T, T_pad, BH, d, causal;
   float scale;
   uint32_t* err;  // device error word
+  int num_sms;    // streaming multiprocessors of the device (persistent grids)
 };
 
 inline int pad_rows(int T) { return (T + 127) / 128 * 128; }
