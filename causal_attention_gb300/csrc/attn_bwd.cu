@@ -18,19 +18,20 @@
 // The dQ-parallel / dKV-parallel split with a D preprocess is the three-stage,
 // atomic-free structure of the Forge paper's section "Ecosystem survey".
 //
-// Roles in the two tensor-core kernels (352 threads):
-//   warps 0-7  elementwise, two warpgroups: thread = row of the CTA's own tile (TMEM
-//              lane), warpgroup h = columns [64h, 64h+64) of the 128-column tiles
-//   warp  8    TMA producer
-//   warp  9    TMEM allocator and MMA issuer (S and dP)
-//   warp  10   second MMA issuer (dV and dK, or dQ) where the elementwise results have
+// Roles in the two tensor-core kernels (608 threads):
+//   warps 0-15 elementwise, four warpgroups: thread = row of the CTA's own tile (TMEM
+//              lane), warpgroup h = columns [32h, 32h+32) of the 128-column tiles
+//              (four warps per scheduler to hide the exp / TMEM / barrier latencies)
+//   warp  16   TMA producer
+//   warp  17   TMEM allocator and MMA issuer (S and dP)
+//   warp  18   second MMA issuer (dV and dK, or dQ) where the elementwise results have
 //              their own TMEM columns. A tcgen05.mma issue blocks until the tensor core
 //              can take it, and any wait of the issuing thread drains the queue, so two
 //              issuers keep the tensor core fed while either one waits.
 // Tensor memory: S or S^T [0,128), dP or dP^T [128,256), accumulators from 256.
-// P^T and dS^T (bf16) are written over the S^T and dP^T regions (each warpgroup into
-// the first 32 columns of its own 64-column half) and fed back to the tensor core from
-// TMEM as the A operand.
+// P^T and dS^T (bf16) go to their own TMEM columns where they fit, else over the S^T
+// and dP^T regions (each warpgroup into the first 16 columns of its own 32-column
+// quarter), and are fed back to the tensor core from TMEM as the A operand.
 #include "kernels.h"
 #include "tile.cuh"
 
@@ -38,7 +39,9 @@ namespace attn {
 
 namespace {
 
-constexpr int kBwdThreads = 352;
+// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers
+constexpr int kBwdThreads = 608;
+constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -142,7 +145,7 @@ struct BwdSmem {
   __device__ uint32_t acc_free() const { return bar0 + 8u * (13 + 2 * st); }
 };
 
-constexpr int kEwThreads = 256;  // two elementwise warpgroups
+constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
 template <int D>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
@@ -178,7 +181,7 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     *abort = 0;
     fence_barrier_init();
   }
-  if ((threadIdx.x >> 5) == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  if ((threadIdx.x >> 5) == kWarpMmaA) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -195,6 +198,37 @@ __device__ __forceinline__ void store_row16(__nv_bfloat16* dst, const uint32_t (
   uint4* d4 = reinterpret_cast<uint4*>(dst);
   d4[0] = pk[0];
   d4[1] = pk[1];
+}
+
+// Epilogue of one accumulator row (d fp32 TMEM columns from `tacc`): the warpgroup hc
+// of four converts its quarter, columns [hc*d/4, (hc+1)*d/4), to bf16 (times `mul`) and
+// stores it to `dst_row` (a [d] bf16 row) when `valid`.
+template <int D>
+__device__ __forceinline__ void store_acc_quarter(uint32_t tacc, __nv_bfloat16* dst_row, int hc, float mul,
+                                                  bool valid) {
+  constexpr int QW = D / 4;  // 8, 16 or 32 columns
+  if constexpr (QW == 8) {
+    uint32_t u[8];
+    tmem_ld8(tacc + (uint32_t)(hc * QW), u);
+    tmem_wait_ld();
+    if (valid) {
+      uint4 pk;
+      pk.x = pack_bf16(__uint_as_float(u[0]) * mul, __uint_as_float(u[1]) * mul);
+      pk.y = pack_bf16(__uint_as_float(u[2]) * mul, __uint_as_float(u[3]) * mul);
+      pk.z = pack_bf16(__uint_as_float(u[4]) * mul, __uint_as_float(u[5]) * mul);
+      pk.w = pack_bf16(__uint_as_float(u[6]) * mul, __uint_as_float(u[7]) * mul);
+      *reinterpret_cast<uint4*>(dst_row + hc * QW) = pk;
+    }
+  } else {
+#pragma unroll
+    for (int cb = 0; cb < QW / 16; ++cb) {
+      const int col = hc * QW + 16 * cb;
+      uint32_t u[16];
+      tmem_ld16(tacc + (uint32_t)col, u);
+      tmem_wait_ld();
+      if (valid) store_row16(dst_row + col, u, mul);
+    }
+  }
 }
 
 // Work items of a persistent kernel, sorted longest first, dealt to the CTAs in a snake
@@ -222,8 +256,8 @@ __device__ __forceinline__ void drain_loads(const BwdSmem& sm, int fix_issued, i
 // Work item = one 128-key tile j of one (b, h); its iterations run over the query tiles
 // i (i >= j when causal). With separate P^T / dS^T columns (d <= 64) the kernel is
 // persistent and two threads issue MMAs:
-//   warp 9:  S_i (= S^T, K_j Q_i^T) as soon as S_{i-1} was read out, dP_i likewise;
-//   warp 10: dV += P_i^T dO_i once P_i^T is in TMEM, dK += dS_i^T Q_i once dS_i^T is.
+//   warp 17: S_i (= S^T, K_j Q_i^T) as soon as S_{i-1} was read out, dP_i likewise;
+//   warp 18: dV += P_i^T dO_i once P_i^T is in TMEM, dK += dS_i^T Q_i once dS_i^T is.
 // The next item's S and dP run while the elementwise warps store this item's dK, dV.
 // At d = 128 (TMEM full, P^T / dS^T written over S^T / dP^T) one thread issues in the
 // order S_0, dP_0 | P_0: dV_0, S_1 | dS_0: dK_0, dP_1 | ..., which relies on same-thread
@@ -258,7 +292,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sdO = [&](int s) { return sQ(s) + TL::BYTES; };
   auto sL = [&](int s) { return sQ(s) + 2 * TL::BYTES; };  // 128 fp32 -LSE*log2e, then 128 fp32 D
 
-  if (warp == 8) {
+  if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -287,7 +321,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) drain_loads(sm, fix_issued, g, ST, ab);
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMmaA) {
     // ------------------------------------------------------------ MMA issuer (S, dP)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
@@ -363,7 +397,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait_drain(sm.drain(), 0, ab);
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kWarpMmaB) {
     // ------------------------------------------------------------ MMA issuer (dV, dK)
     if (lane == 0 && SEP) {
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
@@ -388,7 +422,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dK += dS^T Q_i
           mma_chain_ts<TL, false>(tDK, tmem + C::COL_DS, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
           mma_commit(sm.dk_done());
-          // S_i and dP_i (warp 9) were read out before P_i / dS_i were signalled, so this
+          // S_i and dP_i (warp 17) were read out before P_i / dS_i were signalled, so this
           // commit covers every MMA that reads stage s
           mma_commit(sm.st_empty(s));
         }
@@ -401,13 +435,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise
-    // thread owns key row kt*128 + r and query columns [64*hc, 64*hc + 64)
+    // thread owns key row kt*128 + r and query columns [32*hc, 32*hc + 32)
     const int hc = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lo = warp_lane_base();
-    const uint32_t tSh = tmem + lo + 64u * hc, tDPh = tmem + lo + 128u + 64u * hc;
-    const uint32_t tP = tmem + lo + (SEP ? C::COL_P + 32u * hc : 64u * hc);
-    const uint32_t tDS = tmem + lo + (SEP ? C::COL_DS + 32u * hc : 128u + 64u * hc);
+    const uint32_t tSh = tmem + lo + 32u * hc, tDPh = tmem + lo + 128u + 32u * hc;
+    const uint32_t tP = tmem + lo + (SEP ? C::COL_P + 16u * hc : 32u * hc);
+    const uint32_t tDS = tmem + lo + (SEP ? C::COL_DS + 16u * hc : 128u + 32u * hc);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
     int g = 0;
@@ -418,21 +452,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
         if (!(ok = mbar_wait_warp(sm.st_full(s), (g / ST) & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
-        const float* nl = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base)) + 64 * hc;
+        const float* nl = reinterpret_cast<const float*>(sm.gbase + (sL(s) - sm.base)) + 32 * hc;
         const float* dd = nl + 128;
         // ---- P^T = exp2(S^T * scale*log2e - LSE_i*log2e), kept in fp32 for dS
-        float p[64];
+        float p[32];
         {
-          uint32_t u2[64];
-          tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
-          tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          uint32_t u2[32];
+          tmem_ld32(tSh, u2);
           tmem_wait_ld();
           if (SEP) {
             tc_fence_before();
             mbar_arrive(sm.s_free());  // S^T_i is in registers
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const uint64_t x = f2_fma(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), c2,
                                       *reinterpret_cast<const uint64_t*>(nl + 2 * i));
             float x0, x1;
@@ -443,18 +476,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (CAUSAL && qi == kt) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (64 * hc + c < r) p[c] = 0.f;
+          for (int c = 0; c < 32; ++c)
+            if (32 * hc + c < r) p[c] = 0.f;
         }
         {
-          uint32_t pp[32];
+          uint32_t pp[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+          for (int i = 0; i < 16; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
           // the previous dV read the P^T columns: it must be complete before they are rewritten
           if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dv_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
           tc_fence_after();
-          tmem_st16(tP, *reinterpret_cast<uint32_t(*)[16]>(&pp[0]));
-          tmem_st16(tP + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pp[16]));
+          tmem_st16(tP, pp);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -463,17 +495,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait_warp(sm.dp_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
         {
-          uint32_t u2[64];
-          tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
-          tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          uint32_t u2[32];
+          tmem_ld32(tDPh, u2);
           tmem_wait_ld();
           if (SEP) {
             tc_fence_before();
             mbar_arrive(sm.dp_free());  // dP^T_i is in registers
           }
-          uint32_t pd[32];
+          uint32_t pd[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const uint64_t gg = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
                                        f2_sub(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])),
                                               *reinterpret_cast<const uint64_t*>(dd + 2 * i)));
@@ -483,8 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
           tc_fence_after();
-          tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
-          tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
+          tmem_st16(tDS, pd);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -495,18 +525,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int key = kt * kTileRows + r;
       const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)D;
-#pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        const int col = hc * (D / 2) + 16 * cb;
-        uint32_t v16[16], k16[16];
-        tmem_ld16(tDV + (uint32_t)col, v16);
-        tmem_ld16(tDK + (uint32_t)col, k16);
-        tmem_wait_ld();
-        if (key < T) {
-          store_row16(dv + ((size_t)bh * T + key) * D + col, v16, 1.f);
-          store_row16(dk + ((size_t)bh * T + key) * D + col, k16, scale);
-        }
-      }
+      store_acc_quarter<D>(tDV, dv + ((size_t)bh * T + key) * D, hc, 1.f, key < T);
+      store_acc_quarter<D>(tDK, dk + ((size_t)bh * T + key) * D, hc, scale, key < T);
       tc_fence_before();
       mbar_arrive(sm.acc_free());
     }
@@ -514,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMmaA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -525,8 +545,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------------------
 // Work item = one 128-query tile i of one (b, h); its iterations run over the key tiles
 // j (j <= i when causal). Persistent, two MMA issuers:
-//   warp 9:  S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
-//   warp 10: dQ += dS_j K_j once dS_j (its own 64 TMEM columns) is written.
+//   warp 17: S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
+//   warp 18: dQ += dS_j K_j once dS_j (its own 64 TMEM columns) is written.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -555,7 +575,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sV = [&](int s) { return sK(s) + TL::BYTES; };
 
-  if (warp == 8) {
+  if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -581,7 +601,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!ok) drain_loads(sm, fix_issued, g, ST, ab);
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMmaA) {
     // ------------------------------------------------------------ MMA issuer (S, dP)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
@@ -615,7 +635,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait_drain(sm.drain(), 0, ab);
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kWarpMmaB) {
     // ------------------------------------------------------------ MMA issuer (dQ)
     if (lane == 0) {
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
@@ -634,7 +654,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dQ += dS K_j (M = queries, N = d, K = keys); dS has its own 64 columns
           mma_chain_ts<TL, false>(tDQ, tDS, dKm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
           mma_commit(sm.dk_done());  // "dQ_j done": the dS columns may be rewritten
-          // S_j and dP_j (warp 9) were read out before dS_j was signalled
+          // S_j and dP_j (warp 17) were read out before dS_j was signalled
           mma_commit(sm.st_empty(s));
         }
         if (ok) mma_commit(sm.acc_full());
@@ -646,12 +666,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise
-    // thread owns query row qt*128 + r and key columns [64*hc, 64*hc + 64)
+    // thread owns query row qt*128 + r and key columns [32*hc, 32*hc + 32)
     const int hc = warp >> 2;
     const int r = threadIdx.x & 127;
     const uint32_t lo = warp_lane_base();
-    const uint32_t tSh = tmem + lo + 64u * hc, tDPh = tmem + lo + 128u + 64u * hc;
-    const uint32_t tDS = tmem + lo + 256u + (uint32_t)D + 32u * hc;
+    const uint32_t tSh = tmem + lo + 32u * hc, tDPh = tmem + lo + 128u + 32u * hc;
+    const uint32_t tDS = tmem + lo + 256u + (uint32_t)D + 16u * hc;
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
     int g = 0;
@@ -664,16 +684,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int it = 0; it < n_it; ++it, ++g) {
         if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
-        float p[64];
+        float p[32];
         {
-          uint32_t u2[64];
-          tmem_ld32(tSh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
-          tmem_ld32(tSh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          uint32_t u2[32];
+          tmem_ld32(tSh, u2);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(sm.s_free());  // S_j is in registers: the tensor core may overwrite it
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const uint64_t x = f2_fma(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), c2, nl2);
             float x0, x1;
             f2_unpack(x, x0, x1);
@@ -683,27 +702,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (CAUSAL && it == qt) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (64 * hc + c > r) p[c] = 0.f;
+          for (int c = 0; c < 32; ++c)
+            if (32 * hc + c > r) p[c] = 0.f;
         }
         if (!CAUSAL) {
-          const int lim = T - it * kTileRows - 64 * hc;  // key columns >= lim are padding
+          const int lim = T - it * kTileRows - 32 * hc;  // key columns >= lim are padding
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+          for (int c = 0; c < 32; ++c)
             if (c >= lim) p[c] = 0.f;
         }
         if (!(ok = mbar_wait_warp(sm.dp_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
         {
-          uint32_t u2[64];
-          tmem_ld32(tDPh, *reinterpret_cast<uint32_t(*)[32]>(&u2[0]));
-          tmem_ld32(tDPh + 32u, *reinterpret_cast<uint32_t(*)[32]>(&u2[32]));
+          uint32_t u2[32];
+          tmem_ld32(tDPh, u2);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(sm.dp_free());  // dP_j is in registers
-          uint32_t pd[32];
+          uint32_t pd[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const uint64_t gg = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
                                        f2_sub(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), D2));
             float g0, g1;
@@ -713,8 +731,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // the previous dQ MMA read the dS columns: it must be complete before they are rewritten
           if (g > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
           tc_fence_after();
-          tmem_st16(tDS, *reinterpret_cast<uint32_t(*)[16]>(&pd[0]));
-          tmem_st16(tDS + 16u, *reinterpret_cast<uint32_t(*)[16]>(&pd[16]));
+          tmem_st16(tDS, pd);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -723,15 +740,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ---- epilogue: dQ (x scale) of this query tile; then free the accumulator
       if (!ok || !(ok = mbar_wait_warp(sm.acc_full(), ri & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
-      const uint32_t tDQ = tmem + lo + 256u;
-#pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        const int col = hc * (D / 2) + 16 * cb;
-        uint32_t u16[16];
-        tmem_ld16(tDQ + (uint32_t)col, u16);
-        tmem_wait_ld();
-        if (row < T) store_row16(dq + ((size_t)bh * T + row) * D + col, u16, scale);
-      }
+      store_acc_quarter<D>(tmem + lo + 256u, dq + ((size_t)bh * T + row) * D, hc, scale, row < T);
       tc_fence_before();
       mbar_arrive(sm.acc_free());
     }
@@ -739,7 +748,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMmaA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

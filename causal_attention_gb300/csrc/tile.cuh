@@ -74,14 +74,14 @@ __device__ __forceinline__ void mma_chain_ss(uint32_t d, uint64_t a0, uint64_t b
 }
 
 // D[tmem] (+)= A[tmem] B[smem] over 8 K-steps of 16 (K = 128 tile rows), B MN-major.
-// The A operand's K-step k starts at TMEM column a0 + 8k, or, with HALVES (bf16
-// K-columns written by two warpgroups into the first 32 columns of their own 64-column
-// halves of a 128-column fp32 region), at a0 + 8(k mod 4) + 64(k div 4).
-template <class TL, bool HALVES>
+// The A operand's K-step k starts at TMEM column a0 + 8k, or, with QUARTERS (bf16
+// K-columns written by four warpgroups into the first 16 columns of their own 32-column
+// quarters of a 128-column fp32 region), at a0 + 32(k div 2) + 8(k mod 2).
+template <class TL, bool QUARTERS>
 __device__ __forceinline__ void mma_chain_ts(uint32_t d, uint32_t a0, uint64_t b0, uint32_t idesc, uint32_t acc0) {
 #pragma unroll
   for (int k = 0; k < kTileRows / 16; ++k) {
-    const uint32_t col = HALVES ? 8u * (k & 3) + 64u * (k >> 2) : 8u * k;
+    const uint32_t col = QUARTERS ? 32u * (k >> 1) + 8u * (k & 1) : 8u * k;
     mma_ts(d, a0 + col, b0 + TL::mnmajor_off(k), idesc, k ? 1u : acc0);
   }
 }
