@@ -465,13 +465,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(sm.s_free());  // S^T_i is in registers
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint64_t x = f2_fma(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), c2,
-                                      *reinterpret_cast<const uint64_t*>(nl + 2 * i));
-            float x0, x1;
-            f2_unpack(x, x0, x1);
-            p[2 * i] = ex2(x0);
-            p[2 * i + 1] = ex2(x1);
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 L = reinterpret_cast<const float4*>(nl)[i4];  // 128-bit shared loads
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int i = 2 * i4 + h;
+              const uint64_t x = f2_fma(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])), c2,
+                                        h ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y));
+              float x0, x1;
+              f2_unpack(x, x0, x1);
+              p[2 * i] = ex2(x0);
+              p[2 * i + 1] = ex2(x1);
+            }
           }
         }
         if (CAUSAL && qi == kt) {
@@ -504,13 +509,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           uint32_t pd[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint64_t gg = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
-                                       f2_sub(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])),
-                                              *reinterpret_cast<const uint64_t*>(dd + 2 * i)));
-            float g0, g1;
-            f2_unpack(gg, g0, g1);
-            pd[i] = pack_bf16(g0, g1);
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 Dv = reinterpret_cast<const float4*>(dd)[i4];  // 128-bit shared loads
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int i = 2 * i4 + h;
+              const uint64_t gg = f2_mul(f2_pack(p[2 * i], p[2 * i + 1]),
+                                         f2_sub(f2_pack(__uint_as_float(u2[2 * i]), __uint_as_float(u2[2 * i + 1])),
+                                                h ? f2_pack(Dv.z, Dv.w) : f2_pack(Dv.x, Dv.y)));
+              float g0, g1;
+              f2_unpack(gg, g0, g1);
+              pd[i] = pack_bf16(g0, g1);
+            }
           }
           if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
           tc_fence_after();

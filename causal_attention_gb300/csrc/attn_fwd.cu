@@ -235,11 +235,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (j == nbq - 1) mma_commit(o_final(q));
         }
         if (!ok) break;
-        // blocks of the item this tile does not need (causal tile 0): release them too
-        for (int j = nbq; j < nb; ++j) {
-          mma_commit(k_empty((g + j) % ST));
-          mma_commit(v_empty((g + j) % ST));
+        // blocks of the item this tile does not need (causal tile 0): release them too,
+        // but only once they are loaded, so that the arrival counts toward this block's
+        // phase of the two-arrival barrier and not toward the previous use of the stage
+        for (int j = nbq; j < nb && ok; ++j) {
+          const int gb = g + j, s = gb % ST;
+          if (!(ok = mbar_wait(k_full(s), (gb / ST) & 1, ab, kErrTimeoutMma))) break;
+          mma_commit(k_empty(s));
+          if (!(ok = mbar_wait(v_full(s), (gb / ST) & 1, ab, kErrTimeoutMma))) break;
+          mma_commit(v_empty(s));
         }
+        if (!ok) break;
         g += nb;
         gq += nbq;
       }

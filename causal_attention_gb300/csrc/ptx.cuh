@@ -96,9 +96,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
   }
 }
 
-// The same wait with a warp-uniform result: every lane of the warp waits, and the
-// warp proceeds only if all lanes succeeded (needed before .sync.aligned tcgen05
-// instructions, which all 32 lanes must execute together).
+// The same wait for a whole warp with a warp-uniform result (needed before .sync.aligned
+// tcgen05 instructions, which all 32 lanes must execute together): every lane waits, and
+// the warp proceeds only if all lanes succeeded.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const Abort& ab,
                                                uint32_t err_bit) {
   const bool ok = mbar_wait(bar, parity, ab, err_bit);
