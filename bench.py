@@ -1,7 +1,8 @@
 """Throughput of the fused causal attention forward + backward on GB300.
 
 One step = attn_fwd followed by attn_bwd (preprocess, dK/dV, dQ) over one batch of
-the workload, through the C ABI. Prints ONE JSON line (rank 0).
+the workload, through the C ABI (with --fused-dq, at d <= 64: preprocess, dK/dV with
+dQ fused, dQ conversion). Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -46,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-dq", action="store_true",
+                    help="time the fused-dQ backward stages (d <= 64) instead of attn_bwd's kernels")
     return ap.parse_args()
 
 
@@ -169,7 +172,12 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
+def kernels_for(d, fused_dq):
+    """The four launches of one step: attn_bwd's separate dK/dV and dQ kernels, or (the
+    fused-dQ stages, d <= 64) dK/dV with dQ formed inside and a conversion launch."""
+    if fused_dq and d <= 64:
+        return ("fwd", "bwd_preprocess", "bwd_dkdv_dq", "bwd_dq_finish")
+    return ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 
 
 def captured_traffic(workload, kernel):
@@ -191,12 +199,12 @@ def captured_traffic(workload, kernel):
 def kernel_flops(w):
     """Algorithmic FLOPs per launch of each kernel (causal half of every T x T GEMM)."""
     g = w.B * w.H * w.T * w.T * w.d * (1.0 if w.causal else 2.0)  # one causal GEMM = B*H*T^2*d
-    return {"fwd": 2 * g, "bwd_dkdv": 4 * g, "bwd_dq": 3 * g}
+    return {"fwd": 2 * g, "bwd_dkdv": 4 * g, "bwd_dq": 3 * g, "bwd_dkdv_dq": 5 * g}
 
 
 def kernel_bytes(w):
     n = w.B * w.H * w.T
-    return {"bwd_preprocess": 2 * n * w.d * 2 + 4 * n + 8 * n}
+    return {"bwd_preprocess": 2 * n * w.d * 2 + 4 * n + 8 * n, "bwd_dq_finish": n * w.d * (4 + 2)}
 
 
 def run_ours(args, rank, world, local):
@@ -218,7 +226,10 @@ def run_ours(args, rank, world, local):
     scale, causal = wr.scale, wr.causal
     dev = torch.device("cuda", local)
 
-    per_set = 8 * B * H * T * d * 2 + 3 * B * H * T * 4
+    KERNELS = kernels_for(d, args.fused_dq)
+    fused = KERNELS[2] == "bwd_dkdv_dq"
+    ws_bytes = (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d)
+    per_set = 8 * B * H * T * d * 2 + B * H * T * 4 + ws_bytes
     n_sets = max(2, -(-3 * L2_BYTES // per_set))
     base = {n: to_device(x[n]) for n in ("q", "k", "v", "do")}
     sets = []
@@ -227,11 +238,12 @@ def run_ours(args, rank, world, local):
         s["o"] = torch.empty_like(s["q"])
         s["lse"] = torch.empty((B, H, T), dtype=torch.float32, device=dev)
         s["dq"], s["dk"], s["dv"] = (torch.empty_like(s["q"]) for _ in range(3))
-        s["ws"] = ca.new_workspace(B, H, T, d, dev)
+        s["ws"] = ca.new_workspace(B, H, T, d, dev, fused_dq=fused)
         sets.append(s)
     stream = torch.cuda.current_stream()
 
     def step(s, ev=None):
+        # the stages attn_bwd runs, called one by one so that each can be timed
         if ev is not None:
             ev[0].record(stream)
         ca.attn_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], scale, causal, stream)
@@ -240,10 +252,16 @@ def run_ours(args, rank, world, local):
         ca.attn_bwd_preprocess(s["o"], s["do"], s["lse"], s["ws"], stream)
         if ev is not None:
             ev[2].record(stream)
-        ca.attn_bwd_dkdv(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"], scale, causal, stream)
+        if fused:
+            ca.attn_bwd_dkdv_dq(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"], scale, causal, stream)
+        else:
+            ca.attn_bwd_dkdv(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"], scale, causal, stream)
         if ev is not None:
             ev[3].record(stream)
-        ca.attn_bwd_dq(s["q"], s["k"], s["v"], s["do"], s["dq"], s["ws"], scale, causal, stream)
+        if fused:
+            ca.attn_bwd_dq_finish(s["dq"], s["ws"], scale, stream)
+        else:
+            ca.attn_bwd_dq(s["q"], s["k"], s["v"], s["do"], s["dq"], s["ws"], scale, causal, stream)
         if ev is not None:
             ev[4].record(stream)
 
@@ -298,9 +316,12 @@ def run_ours(args, rank, world, local):
     def e2e_step():
         for n in ("q", "k", "v", "do"):
             s0[n].copy_(pinned[n], non_blocking=True)
-        ca.attn_fwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["lse"], scale, causal, stream)
-        ca.attn_bwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["do"], s0["lse"], s0["dq"], s0["dk"], s0["dv"],
-                    s0["ws"], scale, causal, stream)
+        if fused:
+            step(s0)  # the fused-dQ stages are called one by one, as a user of them would
+        else:
+            ca.attn_fwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["lse"], scale, causal, stream)
+            ca.attn_bwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["do"], s0["lse"], s0["dq"], s0["dk"], s0["dv"],
+                        s0["ws"], scale, causal, stream)
         for n in ("o", "lse", "dq", "dk", "dv"):
             outs_h[n].copy_(s0[n], non_blocking=True)
 
@@ -327,7 +348,7 @@ def run_ours(args, rank, world, local):
 
     # ------------------------------------------------------------------ roofline
     peak_tf, peak_gbs, peak_kind = load_peaks()
-    kf = kernel_flops(wr)
+    kf = {k: f for k, f in kernel_flops(wr).items() if k in KERNELS}
     top = max(kf, key=lambda k: mean_ms[k])
     achieved = kf[top] / (mean_ms[top] * 1e-3) / 1e12
     traffic = captured_traffic(wr.name, top)
@@ -345,7 +366,7 @@ def run_ours(args, rank, world, local):
             e.update(gbs=round(gbs, 1), frac=round(gbs / peak_gbs, 4))
         kernels[k] = e
     fwd_tf = fwd_f * (1.0 if causal else 2.0) / (mean_ms["fwd"] * 1e-3) / 1e12
-    bwd_ms = mean_ms["bwd_preprocess"] + mean_ms["bwd_dkdv"] + mean_ms["bwd_dq"]
+    bwd_ms = sum(mean_ms[k] for k in KERNELS[1:])
     bwd_tf = bwd_f * (1.0 if causal else 2.0) / (bwd_ms * 1e-3) / 1e12
 
     cpu = None

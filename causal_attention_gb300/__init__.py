@@ -103,6 +103,23 @@ def attn_bwd_dq(q, k, v, do, dq, workspace, scale, causal=True, stream=None):
                             ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_bwd_dq")
 
 
+def attn_bwd_dkdv_dq(q, k, v, do, dk, dv, workspace, scale, causal=True, stream=None):
+    """dK, dV and (into the workspace) the fp32 dQ sums in one kernel; d <= 64 and a
+    workspace of attn_bwd_fused_workspace_size bytes, prepared by attn_bwd_preprocess."""
+    B, H, T, d = _shape(q)
+    _check(_dll.attn_bwd_dkdv_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), B, H, T, d,
+                                 ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_bwd_dkdv_dq")
+
+
+def attn_bwd_dq_finish(dq, workspace, scale, stream=None):
+    """dQ (bf16) = scale times the fp32 sums attn_bwd_dkdv_dq left in the workspace."""
+    B, H, T, d = _shape(dq)
+    _check(_dll.attn_bwd_dq_finish(_ptr(dq), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   B, H, T, d, ctypes.c_float(scale), _stream_handle(stream)),
+           "attn_bwd_dq_finish")
+
+
 def attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=True, stream=None):
     """attn_bwd without a workspace: the library's fixed 8 MiB device scratch is used
     instead (B*H*T_pad <= 1,048,576). For callers that cannot allocate device memory;
@@ -121,10 +138,15 @@ def check_device_error(stream=None):
     _check(_dll.attn_check_device_error(_stream_handle(stream)), "attn_check_device_error")
 
 
-def new_workspace(B, H, T, d, device=None):
-    n = attn_bwd_workspace_size(B, H, T, d)
+def attn_bwd_fused_workspace_size(B, H, T, d) -> int:
+    return int(_dll.attn_bwd_fused_workspace_size(B, H, T, d))
+
+
+def new_workspace(B, H, T, d, device=None, fused_dq=False):
+    """Device workspace for attn_bwd (or, with fused_dq, for the fused-dQ stages)."""
+    n = (attn_bwd_fused_workspace_size if fused_dq else attn_bwd_workspace_size)(B, H, T, d)
     if n == 0:
-        raise ValueError("invalid sizes")
+        raise ValueError("invalid sizes" + (" (the fused dQ needs d <= 64)" if fused_dq else ""))
     return torch.empty(n // 4, dtype=torch.float32, device=device or "cuda")
 
 

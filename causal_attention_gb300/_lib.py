@@ -35,10 +35,13 @@ SIGNATURES = {
     "attn_abi_version": (_I, []),
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_workspace_size": (_S, [_I, _I, _I, _I]),
+    "attn_bwd_fused_workspace_size": (_S, [_I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _S, _I, _I, _I, _I, _P]),
     "attn_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_bwd_dkdv_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_bwd_dq_finish": (_I, [_P, _P, _S, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "attn_check_device_error": (_I, [_P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),

@@ -156,6 +156,18 @@ size_t workspace_bytes_for(int B, int H, int T) {
   return 2 * sizeof(float) * (size_t)B * H * (size_t)pad_rows(T);
 }
 
+// The fused dQ (d <= 64) appends the fp32 dQ tiles (B*H*T_pad*d floats) and one int32
+// ordering counter per 128-row query tile, rounded up to 256 bytes.
+size_t fused_workspace_bytes_for(int B, int H, int T, int d) {
+  const size_t rows = (size_t)B * H * (size_t)pad_rows(T);
+  const size_t cnt = ((size_t)B * H * (size_t)(pad_rows(T) / 128) * sizeof(int) + 255) / 256 * 256;
+  return workspace_bytes_for(B, H, T) + rows * (size_t)d * sizeof(float) + cnt;
+}
+
+bool fused_dq_ok(int d, size_t workspace_bytes, int B, int H, int T) {
+  return d <= 64 && workspace_bytes >= fused_workspace_bytes_for(B, H, T, d);
+}
+
 attn_status check_workspace(const void* ws, size_t bytes, int B, int H, int T) {
   if (!ws || bytes < workspace_bytes_for(B, H, T)) return ATTN_ERR_WORKSPACE;
   if (!aligned16(ws)) return ATTN_ERR_MISALIGNED;
@@ -181,6 +193,9 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   a->scale = scale;
   a->ws_nlse2 = static_cast<float*>(const_cast<void*>(workspace));
   a->ws_D = a->ws_nlse2 + (size_t)a->BH * a->T_pad;
+  // fused-dQ parts (used only where the workspace is large enough and d <= 64)
+  a->dq_acc = a->ws_D + (size_t)a->BH * a->T_pad;
+  a->dq_cnt = reinterpret_cast<int*>(a->dq_acc + (size_t)a->BH * a->T_pad * d);
   cudaError_t e;
   a->err = error_word_ptr(&e);
   if (!a->err) return cuda_fail(e, ATTN_ERR_CUDA);
@@ -289,6 +304,11 @@ size_t attn_bwd_workspace_size(int B, int H, int T, int d) {
   return workspace_bytes_for(B, H, T);
 }
 
+size_t attn_bwd_fused_workspace_size(int B, int H, int T, int d) {
+  if (check_shape(B, H, T, d) != ATTN_OK || d > 64) return 0;
+  return fused_workspace_bytes_for(B, H, T, d);
+}
+
 attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
                                 size_t workspace_bytes, int B, int H, int T, int d, void* stream) {
   ATTN_TRY(check_shape(B, H, T, d));
@@ -299,6 +319,7 @@ attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse,
   a.o = static_cast<const __nv_bfloat16*>(o);
   a.dO = static_cast<const __nv_bfloat16*>(dO);
   a.lse = lse;
+  if (!fused_dq_ok(d, workspace_bytes, B, H, T)) a.dq_cnt = nullptr;  // no counters to reset
   return launched(launch_bwd_preprocess(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -315,6 +336,37 @@ attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const voi
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   return launched(launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_bwd_dkdv_dq(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                             void* dv, void* workspace, size_t workspace_bytes, int B, int H, int T,
+                             int d, float scale, int causal, void* stream) {
+  ATTN_TRY(check_shape(B, H, T, d));
+  ATTN_TRY(check_scale(scale, causal));
+  ATTN_TRY(check_ptrs({q, k, v, dO, dk, dv}));
+  if (d > 64) return ATTN_ERR_UNSUPPORTED;
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, T));
+  if (!fused_dq_ok(d, workspace_bytes, B, H, T)) return ATTN_ERR_WORKSPACE;
+  BwdArgs a;
+  CUtensorMap maps[4];
+  ATTN_TRY(bwd_args(&a, q, k, v, dO, workspace, B, H, T, d, scale, causal, maps, true));
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  return launched(launch_bwd_dkdv_dq(a, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_bwd_dq_finish(void* dq, const void* workspace, size_t workspace_bytes, int B, int H,
+                               int T, int d, float scale, void* stream) {
+  ATTN_TRY(check_shape(B, H, T, d));
+  ATTN_TRY(check_scale(scale, 1));
+  ATTN_TRY(check_ptrs({dq}));
+  if (d > 64) return ATTN_ERR_UNSUPPORTED;
+  ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, T));
+  if (!fused_dq_ok(d, workspace_bytes, B, H, T)) return ATTN_ERR_WORKSPACE;
+  BwdArgs a;
+  ATTN_TRY(bwd_args(&a, nullptr, nullptr, nullptr, nullptr, workspace, B, H, T, d, scale, 1, nullptr, false));
+  a.dq = static_cast<__nv_bfloat16*>(dq);
+  return launched(launch_bwd_dq_finish(a, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
@@ -349,6 +401,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  a.dq_cnt = nullptr;  // the fused dQ's counters are not used here
   ATTN_TRY(launched(launch_bwd_preprocess(a, s)));
   ATTN_TRY(launched(launch_bwd_dkdv(a, s)));
   return launched(launch_bwd_dq(a, s));

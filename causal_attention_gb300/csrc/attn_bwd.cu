@@ -39,21 +39,23 @@ namespace attn {
 
 namespace {
 
-// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers
+// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers, 19 (fused dQ) reducer
 constexpr int kBwdThreads = 608;
-constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18;
+constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18, kWarpRed = 19;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
 // 1. preprocess
 // ---------------------------------------------------------------------------
+// With the fused dQ it also zeroes the per-tile ordering counters (dq_cnt, n_cnt entries).
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-    const float* __restrict__ lse, float* __restrict__ ws_nlse2, float* __restrict__ ws_D, int T,
-    int T_pad, int BH) {
+    const float* __restrict__ lse, float* __restrict__ ws_nlse2, float* __restrict__ ws_D, int* __restrict__ dq_cnt,
+    int n_cnt, int T, int T_pad, int BH) {
   constexpr int TPR = D / 8;           // threads per row, 16 bytes each
   constexpr int RPW = 32 / TPR;        // rows per warp step
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_cnt; i += gridDim.x * blockDim.x) dq_cnt[i] = 0;
   const int lane = threadIdx.x & 31;
   const int sub = lane % TPR;
   const long long total = (long long)BH * T_pad;
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
 // ---------------------------------------------------------------------------
 // shared-memory plan of the two tensor-core kernels
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool FUSE = false>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
@@ -104,8 +106,15 @@ struct BwdCfg {
   // per stage: two tiles (+ for dK/dV, 128 fp32 -LSE*log2e and 128 fp32 D)
   static constexpr int STAGE_BYTES = 2 * TL::BYTES + 1024;
   static constexpr int OFF_STAGE = OFF_FIX + 2 * TL::BYTES;
-  static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 14;
+  // fused dQ only: dS^T as a bf16 128x128 shared-memory tile (A operand of dK += dS^T Q_i
+  // and, read transposed, of dQ_ij = dS K_j), then the fp32 staging tile of dQ_ij on its
+  // way to the workspace
+  static constexpr int DS_BYTES = FUSE ? kTileRows * kTileRows * 2 : 0;
+  static constexpr int DQS_BYTES = FUSE ? kTileRows * D * 4 : 0;
+  static constexpr int OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
+  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
+  static constexpr int NBAR = 1 + 2 * STAGES + 14 + (FUSE ? 5 : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -115,6 +124,10 @@ struct BwdCfg {
   // then it also runs persistently with two MMA issuers.
   static constexpr bool SEP_DKDV = D <= 64;
   static constexpr uint32_t COL_P = 384, COL_DS = 448;
+  // fused dQ: dQ_ij (fp32, d columns) takes the columns of dS^T, which lives in shared memory
+  static constexpr uint32_t COL_DQ = 448;
+  static constexpr int THREADS = FUSE ? kBwdThreads + 32 : kBwdThreads;
+  static_assert(!FUSE || SEP_DKDV, "the fused dQ needs the separate P^T columns (d <= 64)");
 };
 
 // Barriers (one 8-byte mbarrier each). Per work item: fix_full / fix_empty (the item's
@@ -143,14 +156,21 @@ struct BwdSmem {
   __device__ uint32_t drain2() const { return bar0 + 8u * (11 + 2 * st); }
   __device__ uint32_t fix_empty() const { return bar0 + 8u * (12 + 2 * st); }
   __device__ uint32_t acc_free() const { return bar0 + 8u * (13 + 2 * st); }
+  // fused dQ: the dQ_ij MMA finished (dS^T tile and TMEM columns read) / its TMEM columns
+  // were read out / the staging tile is written / the staging tile was read by the copy
+  __device__ uint32_t dq_done() const { return bar0 + 8u * (14 + 2 * st); }
+  __device__ uint32_t dq_free() const { return bar0 + 8u * (15 + 2 * st); }
+  __device__ uint32_t dqs_full() const { return bar0 + 8u * (16 + 2 * st); }
+  __device__ uint32_t dqs_free() const { return bar0 + 8u * (17 + 2 * st); }
+  __device__ uint32_t drain3() const { return bar0 + 8u * (18 + 2 * st); }
 };
 
 constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
-template <int D>
+template <int D, bool FUSE = false>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
                                                   volatile int*& abort) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, FUSE>;
   BwdSmem s;
   const uint32_t raw = smem_u32(smem_raw);
   s.base = (raw + 1023u) & ~1023u;
@@ -178,6 +198,13 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     mbar_init(s.acc_free(), kEwThreads);
     mbar_init(s.drain(), 1);
     mbar_init(s.drain2(), 1);
+    if (FUSE) {
+      mbar_init(s.dq_done(), 1);
+      mbar_init(s.dq_free(), kEwThreads);
+      mbar_init(s.dqs_full(), kEwThreads);
+      mbar_init(s.dqs_free(), 1);
+      mbar_init(s.drain3(), 1);
+    }
     *abort = 0;
     fence_barrier_init();
   }
@@ -250,8 +277,27 @@ __device__ __forceinline__ void drain_loads(const BwdSmem& sm, int fix_issued, i
   for (int g = max(0, st_issued - st); g < st_issued; ++g) mbar_wait_drain(sm.st_full(g % st), (g / st) & 1, ab);
 }
 
+// Fused dQ: waits until the workspace tile's counter shows `want` contributions (all key
+// tiles before this one). Bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_turn(const int* cnt, int want, const Abort& ab) {
+  if (ld_acquire_gpu(cnt) == want) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(cnt) == want) return true;
+    if ((it & 15u) == 0) {
+      if (*ab.flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        atomicOr(ab.err, kErrTimeoutOrder);
+        *ab.flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
-// 2. dK / dV
+// 2. dK / dV (and, fused, dQ)
 // ---------------------------------------------------------------------------
 // Work item = one 128-key tile j of one (b, h); its iterations run over the query tiles
 // i (i >= j when causal). With separate P^T / dS^T columns (d <= 64) the kernel is
@@ -262,21 +308,36 @@ __device__ __forceinline__ void drain_loads(const BwdSmem& sm, int fix_issued, i
 // At d = 128 (TMEM full, P^T / dS^T written over S^T / dP^T) one thread issues in the
 // order S_0, dP_0 | P_0: dV_0, S_1 | dS_0: dK_0, dP_1 | ..., which relies on same-thread
 // MMAs executing in issue order, and each CTA takes one item.
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+//
+// FUSE (d <= 64): the dQ contributions are formed here too, so the separate dQ kernel and
+// its two recomputed GEMMs (S and dP) go away. The elementwise warps write dS^T to shared
+// memory instead of TMEM; warp 18 then issues dK += dS^T Q_i from there and
+// dQ_ij = dS K_j (the same tile read transposed) into the TMEM columns dS^T used to take.
+// The elementwise warps move dQ_ij into a shared fp32 staging tile, and warp 19 adds it
+// to the fp32 workspace tile of query tile i with one bulk shared->global copy (a plain
+// copy for key tile 0, an fp32 reduce-add for the others). Each workspace tile has a
+// counter of the contributions already added; the contribution of key tile j is added
+// when the counter reads j, so every tile sums its terms in the order j = 0, 1, 2, ...
+// and the result is the same on every run. Items run longest (smallest j) first, so a
+// wait is only ever on an item that started no later; all CTAs of the persistent grid
+// are resident together (one per SM).
+template <int D, bool CAUSAL, bool FUSE>
+__global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                          const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
-                         __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int T,
-                         int T_pad, int BH, float scale, float scale_log2, uint32_t* __restrict__ err) {
-  using C = BwdCfg<D>;
+                         __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dq_acc,
+                         int* __restrict__ dq_cnt, int T, int T_pad, int BH, float scale, float scale_log2,
+                         uint32_t* __restrict__ err) {
+  using C = BwdCfg<D, FUSE>;
   using TL = Tile<D>;
+  using TD = Tile<128>;  // the dS^T tile: 128 key rows x 128 query columns
   constexpr int ST = C::STAGES;
   constexpr bool SEP = C::SEP_DKDV;
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
-  const BwdSmem sm = bwd_smem_setup<D>(smem_raw, tmem_slot, abort);
+  const BwdSmem sm = bwd_smem_setup<D, FUSE>(smem_raw, tmem_slot, abort);
   const Abort ab{abort, err};
   const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -291,6 +352,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto sQ = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sdO = [&](int s) { return sQ(s) + TL::BYTES; };
   auto sL = [&](int s) { return sQ(s) + 2 * TL::BYTES; };  // 128 fp32 -LSE*log2e, then 128 fp32 D
+  const uint32_t sDS = sm.base + C::OFF_DS, sDQS = sm.base + C::OFF_DQS;
 
   if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
@@ -355,7 +417,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             issue_dP(s);
             mma_commit(sm.dp_full());
-            if (it == n_it - 1) mma_commit(sm.fix_empty());  // K_j, V_j are no longer read
+            // K_j, V_j are no longer read (with FUSE, K_j is read by the dQ MMAs of warp 18,
+            // which releases them)
+            if (!FUSE && it == n_it - 1) mma_commit(sm.fix_empty());
           }
         } else {
           // P^T / dS^T written over S^T / dP^T: same-thread issue order is the guard
@@ -419,18 +483,66 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(sm.dv_done());
           if (!(ok = mbar_wait(sm.ds_full(), g & 1, ab, kErrTimeoutMma))) break;
           tc_fence_after();
-          // dK += dS^T Q_i
-          mma_chain_ts<TL, false>(tDK, tmem + C::COL_DS, dQm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
-          mma_commit(sm.dk_done());
+          if constexpr (FUSE) {
+            // dK += dS^T Q_i, dS^T from shared memory (K-major: key rows, query columns)
+            const uint64_t a0 = TD::desc_kmajor0(sDS), b0 = dQm0 + (uint64_t)s * kStageOff;
+#pragma unroll
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ss(tDK, a0 + TD::kmajor_off(k), b0 + TL::mnmajor_off(k), idesc_acc, (it > 0 || k > 0) ? 1u : 0u);
+            // dQ_ij = dS K_j (M = queries, N = d, K = keys): the same tile as an M-major A
+            // operand; its TMEM columns must have been read out by the elementwise warps
+            if (g > 0 && !(ok = mbar_wait(sm.dq_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            constexpr uint32_t idesc_dq = idesc_bf16(128, D, 1, 1);
+            const uint64_t q0 = TD::desc_mnmajor0(sDS), k0 = TL::desc_mnmajor0(sK);
+#pragma unroll
+            for (int k = 0; k < kTileRows / 16; ++k)
+              mma_ss(tmem + C::COL_DQ, q0 + TD::mnmajor_off(k), k0 + TL::mnmajor_off(k), idesc_dq, k > 0 ? 1u : 0u);
+            mma_commit(sm.dq_done());  // dS^T tile and dQ_ij columns
+          } else {
+            // dK += dS^T Q_i
+            mma_chain_ts<TL, false>(tDK, tmem + C::COL_DS, dQm0 + (uint64_t)s * kStageOff, idesc_acc,
+                                    it > 0 ? 1u : 0u);
+            mma_commit(sm.dk_done());
+          }
           // S_i and dP_i (warp 17) were read out before P_i / dS_i were signalled, so this
           // commit covers every MMA that reads stage s
           mma_commit(sm.st_empty(s));
         }
         if (ok) mma_commit(sm.acc_full());
+        if (FUSE && ok) mma_commit(sm.fix_empty());  // K_j (dQ MMAs) and V_j are no longer read
       }
       if (!ok) {
         mma_commit(sm.drain2());
         mbar_wait_drain(sm.drain2(), 0, ab);
+      }
+    }
+  } else if (FUSE && warp == kWarpRed) {
+    // ------------------------------------------------------------ dQ reducer (fused)
+    // adds each staged dQ_ij to workspace tile (b, h, i) in key-tile order
+    if (lane == 0) {
+      bool ok = true;
+      int g = 0;
+      for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
+        const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
+        for (int it = 0; it < n_it; ++it, ++g) {
+          const int qi = i0 + it;
+          if (!(ok = mbar_wait(sm.dqs_full(), g & 1, ab, kErrTimeoutMma))) break;
+          int* cnt = dq_cnt + (size_t)bh * n_q + qi;
+          if (kt > 0 && !(ok = wait_turn(cnt, kt, ab))) break;
+          fence_proxy_async_global();
+          float* dst = dq_acc + ((size_t)bh * n_q + qi) * (kTileRows * D);
+          if (kt == 0)
+            bulk_store(dst, sDQS, C::DQS_BYTES);  // the first term of this tile
+          else
+            bulk_reduce_add_f32(dst, sDQS, C::DQS_BYTES);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(sm.dqs_free());
+          bulk_wait_all();
+          fence_proxy_async_global();
+          st_release_gpu(cnt, kt + 1);
+        }
       }
     }
   } else {
@@ -443,7 +555,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tP = tmem + lo + (SEP ? C::COL_P + 16u * hc : 32u * hc);
     const uint32_t tDS = tmem + lo + (SEP ? C::COL_DS + 16u * hc : 128u + 32u * hc);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+    // FUSE: this thread's part of the dS^T tile (key row r, query columns 32hc..32hc+31)
+    // is 16-byte granules 4(hc%2)..4(hc%2)+3 of row r in chunk hc/2, in the 128-byte
+    // swizzle (granule position XOR r%8) that the tensor core reads
+    const uint32_t ds_row = sDS + (uint32_t)(hc >> 1) * TD::CHUNK_BYTES + (uint32_t)r * 128u;
+    const uint32_t ds_g0 = 4u * (uint32_t)(hc & 1);
+    // FUSE: dQ_ij readout; here the TMEM lane r is a query row and the thread takes d
+    // columns [QW hc, QW hc + QW). The staging tile is [granule c4][row][4 floats], so a
+    // warp's 16-byte stores cover 512 contiguous bytes.
+    constexpr int QW = D / 4;
+    const uint32_t tDQ = tmem + lo + C::COL_DQ + (uint32_t)(QW * hc);
     bool ok = true;
+    auto dq_readout = [&](int x) {  // moves iteration x's dQ_ij into the staging tile
+      if (!(ok = mbar_wait_warp(sm.dq_done(), x & 1, ab, kErrTimeoutElem))) return;
+      tc_fence_after();
+      uint32_t v[QW];
+      if constexpr (QW == 32) tmem_ld32(tDQ, v);
+      else if constexpr (QW == 16) tmem_ld16(tDQ, v);
+      else tmem_ld8(tDQ, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(sm.dq_free());
+      if (x > 0 && !(ok = mbar_wait_warp(sm.dqs_free(), (x - 1) & 1, ab, kErrTimeoutElem))) return;
+#pragma unroll
+      for (int k = 0; k < QW / 4; ++k)
+        sts128(sDQS + (uint32_t)(((QW / 4) * hc + k) * kTileRows + r) * 16u, v[4 * k], v[4 * k + 1], v[4 * k + 2],
+               v[4 * k + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(sm.dqs_full());
+    };
     int g = 0;
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
       const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
@@ -496,6 +636,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(sm.p_full());
+        if (FUSE && g > 0) {
+          // the previous iteration's dQ_ij; this also frees the dS^T tile for this one
+          dq_readout(g - 1);
+          if (!ok) break;
+        }
         // ---- dS^T = P^T * (dP^T - D_i)
         if (!(ok = mbar_wait_warp(sm.dp_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
@@ -522,11 +667,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               pd[i] = pack_bf16(g0, g1);
             }
           }
-          if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
-          tc_fence_after();
-          tmem_st16(tDS, pd);
+          if constexpr (FUSE) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              sts128(ds_row + (((ds_g0 + (uint32_t)k) ^ (uint32_t)(r & 7)) << 4), pd[4 * k], pd[4 * k + 1],
+                     pd[4 * k + 2], pd[4 * k + 3]);
+            fence_proxy_async_smem();
+          } else {
+            if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dk_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
+            tc_fence_after();
+            tmem_st16(tDS, pd);
+          }
         }
-        tmem_wait_st();
+        if (!FUSE) tmem_wait_st();
         tc_fence_before();
         mbar_arrive(sm.ds_full());
       }
@@ -540,6 +693,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(sm.acc_free());
     }
+    if (FUSE && ok && g > 0) dq_readout(g - 1);  // the last iteration's dQ_ij
   }
 
   tc_fence_before();
@@ -765,6 +919,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// 4. fused dQ, last step: dQ = bf16(scale * workspace tile) for rows t < T
+// ---------------------------------------------------------------------------
+// The workspace tile of (b*h, i) holds 128 x d fp32 as [granule c4][row][4 floats]. A
+// thread converts 8 columns of one row; consecutive threads take consecutive rows, so the
+// reads of a warp are 512 contiguous bytes.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_dq_finish_kernel(const float* __restrict__ acc,
+                                                                 __nv_bfloat16* __restrict__ dq, int T, int T_pad,
+                                                                 int BH, float scale) {
+  constexpr int C8 = D / 8;
+  const int n_q = T_pad / kTileRows;
+  const long long total = (long long)BH * T_pad * C8;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(idx % kTileRows);
+    const long long rest = idx / kTileRows;
+    const int c8 = (int)(rest % C8);
+    const long long tile = rest / C8;  // bh * n_q + i
+    const int bh = (int)(tile / n_q), t = (int)(tile % n_q) * kTileRows + r;
+    if (t >= T) continue;
+    const float4* src = reinterpret_cast<const float4*>(acc + tile * (kTileRows * D));
+    const float4 x = src[(2 * c8) * kTileRows + r], y = src[(2 * c8 + 1) * kTileRows + r];
+    uint4 o;
+    o.x = pack_bf16(x.x * scale, x.y * scale);
+    o.y = pack_bf16(x.z * scale, x.w * scale);
+    o.z = pack_bf16(y.x * scale, y.y * scale);
+    o.w = pack_bf16(y.z * scale, y.w * scale);
+    *reinterpret_cast<uint4*>(dq + ((size_t)bh * T + t) * D + 8 * c8) = o;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 template <int D>
@@ -774,23 +960,35 @@ cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   const long long cap = (long long)a.num_sms * 8;  // grid-stride beyond 8 blocks per SM
   if (blocks > cap) blocks = cap;
+  const int n_cnt = a.dq_cnt ? a.BH * (a.T_pad / kTileRows) : 0;
   attn_bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.o, a.dO, a.lse, a.ws_nlse2, a.ws_D,
-                                                                      a.T, a.T_pad, a.BH);
+                                                                      a.dq_cnt, n_cnt, a.T, a.T_pad, a.BH);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FUSE>
 cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
-  auto kern = attn_bwd_dkdv_kernel<D, CAUSAL>;
+  using C = BwdCfg<D, FUSE>;
+  auto kern = attn_bwd_dkdv_kernel<D, CAUSAL, FUSE>;
   static uint32_t configured = 0;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), BwdCfg<D>::SMEM_BYTES, &configured);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
   // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
-  const int grid = BwdCfg<D>::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
-  kern<<<grid, kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
-      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.T, a.T_pad, a.BH, a.scale,
-      a.scale * kLog2e, a.err);
+  const int grid = C::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dk,
+                                                     a.dv, a.dq_acc, a.dq_cnt, a.T, a.T_pad, a.BH, a.scale,
+                                                     a.scale * kLog2e, a.err);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_finish(const BwdArgs& a, cudaStream_t stream) {
+  const long long total = (long long)a.BH * a.T_pad * (D / 8);
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)a.num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  attn_bwd_dq_finish_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.dq_acc, a.dq, a.T, a.T_pad, a.BH, a.scale);
   return cudaGetLastError();
 }
 
@@ -820,9 +1018,27 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {
   switch (a.d) {
-    case 32: return a.causal ? launch_dkdv<32, true>(a, stream) : launch_dkdv<32, false>(a, stream);
-    case 64: return a.causal ? launch_dkdv<64, true>(a, stream) : launch_dkdv<64, false>(a, stream);
-    case 128: return a.causal ? launch_dkdv<128, true>(a, stream) : launch_dkdv<128, false>(a, stream);
+    case 32: return a.causal ? launch_dkdv<32, true, false>(a, stream) : launch_dkdv<32, false, false>(a, stream);
+    case 64: return a.causal ? launch_dkdv<64, true, false>(a, stream) : launch_dkdv<64, false, false>(a, stream);
+    case 128: return a.causal ? launch_dkdv<128, true, false>(a, stream) : launch_dkdv<128, false, false>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_dkdv_dq(const BwdArgs& a, cudaStream_t stream) {
+  if (!a.dq_acc || !a.dq_cnt) return cudaErrorInvalidValue;
+  switch (a.d) {
+    case 32: return a.causal ? launch_dkdv<32, true, true>(a, stream) : launch_dkdv<32, false, true>(a, stream);
+    case 64: return a.causal ? launch_dkdv<64, true, true>(a, stream) : launch_dkdv<64, false, true>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_dq_finish(const BwdArgs& a, cudaStream_t stream) {
+  if (!a.dq_acc) return cudaErrorInvalidValue;
+  switch (a.d) {
+    case 32: return launch_dq_finish<32>(a, stream);
+    case 64: return launch_dq_finish<64>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

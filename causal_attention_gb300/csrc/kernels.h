@@ -22,7 +22,8 @@ struct FwdArgs {
 
 // Workspace of the backward: two fp32 arrays of [B*H, T_pad], T_pad = T rounded
 // up to 128. ws_nlse2 = -LSE * log2(e) (-inf on padding rows), ws_D = rowsum(dO*O)
-// (0 on padding rows).
+// (0 on padding rows). The fused dQ (d <= 64) adds dq_acc, one fp32 128 x d tile per
+// (b*h, query tile), and dq_cnt, one int32 ordering counter per such tile.
 struct BwdArgs {
   const CUtensorMap* tmQ;
   const CUtensorMap* tmK;
@@ -36,6 +37,8 @@ struct BwdArgs {
   __nv_bfloat16* dv;
   float* ws_nlse2;
   float* ws_D;
+  float* dq_acc;  // fused dQ only, else null
+  int* dq_cnt;    // fused dQ only, else null
   int T, T_pad, BH, d, causal;
   float scale;
   uint32_t* err;  // device error word
@@ -48,6 +51,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_dq(const BwdArgs& a, cudaStream_t stream);  // fused dK, dV, dQ (d <= 64)
+cudaError_t launch_bwd_dq_finish(const BwdArgs& a, cudaStream_t stream);
 
 // Sets the max dynamic shared memory of a kernel once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask);

@@ -21,6 +21,7 @@ enum : uint32_t {
   kErrTimeoutMma = 1u << 1,    // MMA issuer waited too long for operands
   kErrTimeoutElem = 1u << 2,   // softmax / elementwise warps waited too long
   kErrTimeoutDrain = 1u << 3,  // drain after an abort did not complete
+  kErrTimeoutOrder = 1u << 4,  // fused dQ: waited too long for an earlier key tile's turn
 };
 
 // Where a CTA reports a failed wait, and how its roles tell one another to stop.
@@ -115,6 +116,47 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, c
     }
   }
   return true;
+}
+
+// ---------------------------------------------------------------------------
+// Bulk copies shared -> global (fused dQ accumulation)
+// ---------------------------------------------------------------------------
+// Generic-proxy shared-memory writes become visible to the async proxy (tensor-core
+// operands, bulk copies) only after this fence.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// dst[0:bytes) = src[0:bytes) (16-byte aligned addresses, bytes a multiple of 16)
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+// dst[0:bytes) += src[0:bytes) as fp32, element by element
+__device__ __forceinline__ void bulk_reduce_add_f32(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all committed bulk copies have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all committed bulk copies have completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

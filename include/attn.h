@@ -72,6 +72,12 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
  * are invalid. */
 size_t attn_bwd_workspace_size(int B, int H, int T, int d);
 
+/* Bytes of device workspace the fused-dQ stages (attn_bwd_dkdv_dq, attn_bwd_dq_finish)
+ * need: the attn_bwd workspace, then B*H*T_pad*d fp32 dQ partial sums, then one int32
+ * counter per 128-row query tile (4*B*H*T_pad/128 bytes, rounded up to 256). 0 if the
+ * sizes are invalid or d > 64. */
+size_t attn_bwd_fused_workspace_size(int B, int H, int T, int d);
+
 /*
  * Backward. Cited definition: Forge RESEARCH.md section 6, "The D term is free"
  * and "Backward (training)"; the three-stage atomic-free structure of the Forge
@@ -90,7 +96,9 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      void* stream);
 
 /* Backward stage 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace
- * (Forge RESEARCH.md section 6, "The D term is free"). Memory-bound. */
+ * (Forge RESEARCH.md section 6, "The D term is free"). Memory-bound. With d <= 64 and a
+ * workspace of attn_bwd_fused_workspace_size bytes it also zeroes the fused dQ's
+ * counters, so it must run before every attn_bwd_dkdv_dq. */
 attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
                                 size_t workspace_bytes, int B, int H, int T, int d, void* stream);
 
@@ -107,6 +115,35 @@ attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const voi
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
                         const void* workspace, size_t workspace_bytes, int B, int H, int T, int d,
                         float scale, int causal, void* stream);
+
+/*
+ * Backward stage 2 with dQ fused (d <= 64 only; an alternative to attn_bwd_dkdv followed
+ * by attn_bwd_dq, which attn_bwd uses because it is faster on GB300): dK and dV as
+ * attn_bwd_dkdv, and the products dQ_ij = dS_ij K_j formed in the same kernel from the
+ * same dS tile, so the two GEMMs the separate dQ kernel recomputes (S and dP) are never
+ * run. Each dQ_ij is added
+ * to an fp32 tile of the workspace in the fixed order j = 0, 1, 2, ... (a per-tile
+ * counter, bounded waits), never with atomics, so the result is the same on every run
+ * (Iron "Kernel Engineering Guide", section 3.4 "Determinism": partial sums combined in a
+ * fixed order; Forge RESEARCH.md section 8, pitfall 20: no atomic gradient
+ * accumulation in deterministic mode). The ordering assumes the launch's CTAs (one per
+ * SM, at most the SM count) are resident together, as on an otherwise idle device; if
+ * they cannot be, a wait runs out and attn_check_device_error reports
+ * ATTN_ERR_DEVICE_TIMEOUT instead of hanging.
+ *   workspace : attn_bwd_fused_workspace_size(B, H, T, d) bytes (ATTN_ERR_WORKSPACE if
+ *               smaller), written by attn_bwd_preprocess just before
+ *   dk, dv    : bf16 [B, H, T, d] outputs; dQ is left in the workspace for
+ *               attn_bwd_dq_finish
+ * d = 128 returns ATTN_ERR_UNSUPPORTED. One kernel launch.
+ */
+attn_status attn_bwd_dkdv_dq(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                             void* dv, void* workspace, size_t workspace_bytes, int B, int H, int T,
+                             int d, float scale, int causal, void* stream);
+
+/* Backward, last step of the fused path: dq (bf16 [B, H, T, d]) = scale times the fp32
+ * dQ sums attn_bwd_dkdv_dq left in the workspace. d <= 64; memory-bound; one launch. */
+attn_status attn_bwd_dq_finish(void* dq, const void* workspace, size_t workspace_bytes, int B, int H,
+                               int T, int d, float scale, void* stream);
 
 /*
  * Backward without a workspace argument. The pages have no counterpart to this entry

@@ -50,11 +50,26 @@ def test_status_strings(lib):
     assert b"unknown" in lib.attn_status_string(99)
 
 
+def base_ws(B, H, T):
+    return 2 * 4 * B * H * ((T + 127) // 128 * 128)
+
+
 def test_workspace_size(lib):
-    assert lib.attn_bwd_workspace_size(2, 3, 200, 64) == 2 * 4 * 2 * 3 * 256
+    assert lib.attn_bwd_workspace_size(2, 3, 200, 64) == base_ws(2, 3, 200) == 2 * 4 * 2 * 3 * 256
     assert lib.attn_bwd_workspace_size(1, 1, 128, 128) == 2 * 4 * 128
     assert lib.attn_bwd_workspace_size(0, 1, 128, 64) == 0
     assert lib.attn_bwd_workspace_size(1, 1, 128, 48) == 0
+
+
+def test_fused_workspace_size(lib):
+    # base (two fp32 [B*H, T_pad] arrays) + fp32 dQ tiles + int32 counters per 128-row
+    # query tile rounded up to 256 bytes; no fused path at d = 128
+    f = lib.attn_bwd_fused_workspace_size
+    assert f(2, 3, 200, 64) == base_ws(2, 3, 200) + 6 * 256 * 64 * 4 + 256
+    assert f(1, 2, 1, 32) == base_ws(1, 2, 1) + 2 * 128 * 32 * 4 + 256
+    assert f(4, 64, 1024, 64) == base_ws(4, 64, 1024) + 256 * 1024 * 64 * 4 + 8192
+    assert f(1, 1, 128, 128) == 0
+    assert f(0, 1, 128, 64) == 0
 
 
 P = 0x10000  # a fake, 16-byte aligned address: never dereferenced when a check fails first
@@ -87,7 +102,25 @@ def test_bwd_rejects_invalid_calls(lib):
     assert lib.attn_bwd(*args(P + 4, ws)) == 3        # misaligned workspace
     assert lib.attn_bwd(*args(P, ws, d=40)) == 2
     assert lib.attn_bwd_preprocess(ctypes.c_void_p(P), ctypes.c_void_p(P), ctypes.c_void_p(P),
-                                   ctypes.c_void_p(P), ws - 1, 1, 1, 64, 64, ctypes.c_void_p(0)) == 4
+                                   ctypes.c_void_p(P), base_ws(1, 1, 64) - 1, 1, 1, 64, 64, ctypes.c_void_p(0)) == 4
+
+
+def test_fused_dq_stages_reject_invalid_calls(lib):
+    """The fused dK/dV/dQ stage needs d <= 64 and the full workspace."""
+    v = [ctypes.c_void_p(P)] * 6
+    ws = lib.attn_bwd_fused_workspace_size(1, 1, 64, 64)
+    call = lambda wsb, d=64: lib.attn_bwd_dkdv_dq(*v, ctypes.c_void_p(P), wsb, 1, 1, 64, d, ctypes.c_float(0.125),
+                                                   1, ctypes.c_void_p(0))
+    assert call(ws - 16) == 4                 # base-sized workspace: not enough for the fused path
+    assert call(base_ws(1, 1, 64) - 16) == 4
+    assert call(10 ** 9, d=128) == 2          # no fused path at d = 128
+    assert call(ws, d=48) == 2
+    fin = lambda wsb, d=64: lib.attn_bwd_dq_finish(ctypes.c_void_p(P), ctypes.c_void_p(P), wsb, 1, 1, 64, d,
+                                                    ctypes.c_float(0.125), ctypes.c_void_p(0))
+    assert fin(ws - 16) == 4
+    assert fin(10 ** 9, d=128) == 2
+    assert lib.attn_bwd_dq_finish(ctypes.c_void_p(P + 8), ctypes.c_void_p(P), ws, 1, 1, 64, 64,
+                                  ctypes.c_float(0.125), ctypes.c_void_p(0)) == 3
 
 
 def test_valid_call_without_gpu_fails_cleanly(lib):

@@ -148,6 +148,37 @@ def test_stage_entry_points_match_combined():
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
+@pytest.mark.parametrize("d,causal,T", [(64, True, 400), (32, True, 257), (64, False, 300), (64, True, 2048)])
+def test_fused_dq_stages(d, causal, T):
+    """The fused-dQ stages (preprocess, dK/dV with dQ, dQ conversion) against the oracle
+    and against attn_bwd: the same dK and dV bits, dQ equal up to the order of its fp32
+    sums; and bitwise the same over repeated runs (the ordered accumulation)."""
+    import causal_attention_gb300 as ca
+    w = si.Workload(f"fused{d}", 2, 3, T, d, causal=causal, seed=77 + d + T)
+    x = si.make_inputs(w)
+    q, k, v, do = (gu.to_device(x[n]) for n in ("q", "k", "v", "do"))
+    o, lse = ca.forward(q, k, v, w.scale, causal)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, w.scale, causal)
+    ws = ca.new_workspace(*w.shape, fused_dq=True)
+    first = None
+    for rep in range(12):
+        dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        ca.attn_bwd_preprocess(o, do, lse, ws)
+        ca.attn_bwd_dkdv_dq(q, k, v, do, dk2, dv2, ws, w.scale, causal)
+        ca.attn_bwd_dq_finish(dq2, ws, w.scale)
+        ca.check_device_error()
+        if first is None:
+            first = (dq2, dk2, dv2)
+            heads = None if T <= 512 else [(0, 0), (1, 2)]
+            ref = gu.run_oracle(w, x, heads=heads)
+            gpu = dict(o=o, lse=lse, dq=dq2, dk=dk2, dv=dv2)
+            gu.assert_within_tolerance(gu.compare(gpu, ref, heads), w.name)
+            assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+            assert gu.rel_rms(gu.to_f64(dq), gu.to_f64(dq2)) <= 2e-3
+        else:
+            assert all(torch.equal(a, b) for a, b in zip(first, (dq2, dk2, dv2))), rep
+
+
 def test_preprocess_D_against_oracle():
     import oracle
     w = si.Workload("pre", 2, 3, 333, 128, seed=9)
