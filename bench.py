@@ -173,10 +173,13 @@ def run_reference(args, rank, world):
 
 
 def kernels_for(d, fused_dq):
-    """The four launches of one step: attn_bwd's separate dK/dV and dQ kernels, or (the
-    fused-dQ stages, d <= 64) dK/dV with dQ formed inside and a conversion launch."""
+    """The launches of one step, in order: the forward, then attn_bwd's stages (d <= 64:
+    dQ, which also forms D, then dK/dV; d = 128: D, dK/dV, dQ), or with --fused-dq the
+    fused-dQ stages (D, dK/dV with dQ formed inside, dQ conversion)."""
     if fused_dq and d <= 64:
         return ("fwd", "bwd_preprocess", "bwd_dkdv_dq", "bwd_dq_finish")
+    if d <= 64:
+        return ("fwd", "bwd_dq", "bwd_dkdv")
     return ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 
 
@@ -227,7 +230,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
 
     KERNELS = kernels_for(d, args.fused_dq)
-    fused = KERNELS[2] == "bwd_dkdv_dq"
+    fused = "bwd_dkdv_dq" in KERNELS
     ws_bytes = (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d)
     per_set = 8 * B * H * T * d * 2 + B * H * T * 4 + ws_bytes
     n_sets = max(2, -(-3 * L2_BYTES // per_set))
@@ -242,34 +245,32 @@ def run_ours(args, rank, world, local):
         sets.append(s)
     stream = torch.cuda.current_stream()
 
+    launch = {
+        "fwd": lambda s: ca.attn_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], scale, causal, stream),
+        "bwd_preprocess": lambda s: ca.attn_bwd_preprocess(s["o"], s["do"], s["lse"], s["ws"], stream),
+        "bwd_dkdv": lambda s: ca.attn_bwd_dkdv(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"], scale,
+                                               causal, stream),
+        "bwd_dq": lambda s: ca.attn_bwd_dq(s["q"], s["k"], s["v"], s["o"], s["do"], s["lse"], s["dq"], s["ws"],
+                                           scale, causal, stream),
+        "bwd_dkdv_dq": lambda s: ca.attn_bwd_dkdv_dq(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"],
+                                                     scale, causal, stream),
+        "bwd_dq_finish": lambda s: ca.attn_bwd_dq_finish(s["dq"], s["ws"], scale, stream),
+    }
+
     def step(s, ev=None):
         # the stages attn_bwd runs, called one by one so that each can be timed
+        for j, k in enumerate(KERNELS):
+            if ev is not None:
+                ev[j].record(stream)
+            launch[k](s)
         if ev is not None:
-            ev[0].record(stream)
-        ca.attn_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], scale, causal, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        ca.attn_bwd_preprocess(s["o"], s["do"], s["lse"], s["ws"], stream)
-        if ev is not None:
-            ev[2].record(stream)
-        if fused:
-            ca.attn_bwd_dkdv_dq(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"], scale, causal, stream)
-        else:
-            ca.attn_bwd_dkdv(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"], scale, causal, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        if fused:
-            ca.attn_bwd_dq_finish(s["dq"], s["ws"], scale, stream)
-        else:
-            ca.attn_bwd_dq(s["q"], s["k"], s["v"], s["do"], s["dq"], s["ws"], scale, causal, stream)
-        if ev is not None:
-            ev[4].record(stream)
+            ev[len(KERNELS)].record(stream)
 
     for i in range(max(3, args.warmup)):
         step(sets[i % n_sets])
     ca.check_device_error(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -390,7 +391,7 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": len(KERNELS) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

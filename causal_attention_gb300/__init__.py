@@ -96,9 +96,11 @@ def attn_bwd_dkdv(q, k, v, do, dk, dv, workspace, scale, causal=True, stream=Non
                               ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_bwd_dkdv")
 
 
-def attn_bwd_dq(q, k, v, do, dq, workspace, scale, causal=True, stream=None):
+def attn_bwd_dq(q, k, v, o, do, lse, dq, workspace, scale, causal=True, stream=None):
+    """dQ; at d <= 64 it also writes D and -LSE*log2(e) into the workspace (no
+    attn_bwd_preprocess needed before it, and attn_bwd_dkdv may follow it)."""
     B, H, T, d = _shape(q)
-    _check(_dll.attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(workspace),
+    _check(_dll.attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), B, H, T, d,
                             ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_bwd_dq")
 

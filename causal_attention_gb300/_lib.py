@@ -39,7 +39,7 @@ SIGNATURES = {
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _S, _I, _I, _I, _I, _P]),
     "attn_bwd_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
-    "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_dkdv_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_dq_finish": (_I, [_P, _P, _S, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),

@@ -214,6 +214,15 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   return ATTN_OK;
 }
 
+// O as a fifth tensor map, for the d <= 64 dQ kernel that stages it to form D itself.
+attn_status bwd_map_o(BwdArgs* a, const void* o, CUtensorMap* map) {
+  if (a->d > 64) return ATTN_OK;
+  ATTN_TRY(make_map(map, o, a->BH, a->T, a->d));
+  a->tmO = map;
+  a->o = static_cast<const __nv_bfloat16*>(o);
+  return ATTN_OK;
+}
+
 attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : cuda_fail(e, ATTN_ERR_LAUNCH); }
 
 // ---------------------------------------------------------------------------
@@ -369,16 +378,18 @@ attn_status attn_bwd_dq_finish(void* dq, const void* workspace, size_t workspace
   return launched(launch_bwd_dq_finish(a, static_cast<cudaStream_t>(stream)));
 }
 
-attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
-                        const void* workspace, size_t workspace_bytes, int B, int H, int T, int d,
-                        float scale, int causal, void* stream) {
+attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                        const float* lse, void* dq, void* workspace, size_t workspace_bytes, int B, int H,
+                        int T, int d, float scale, int causal, void* stream) {
   ATTN_TRY(check_shape(B, H, T, d));
   ATTN_TRY(check_scale(scale, causal));
-  ATTN_TRY(check_ptrs({q, k, v, dO, dq}));
+  ATTN_TRY(check_ptrs({q, k, v, o, dO, lse, dq}));
   ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, T));
   BwdArgs a;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   ATTN_TRY(bwd_args(&a, q, k, v, dO, workspace, B, H, T, d, scale, causal, maps, true));
+  ATTN_TRY(bwd_map_o(&a, o, &maps[4]));
+  a.lse = lse;
   a.dq = static_cast<__nv_bfloat16*>(dq);
   return launched(launch_bwd_dq(a, static_cast<cudaStream_t>(stream)));
 }
@@ -392,8 +403,9 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   ATTN_TRY(check_ptrs({q, k, v, o, dO, lse, dq, dk, dv}));
   ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, T));
   BwdArgs a;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   ATTN_TRY(bwd_args(&a, q, k, v, dO, workspace, B, H, T, d, scale, causal, maps, true));
+  ATTN_TRY(bwd_map_o(&a, o, &maps[4]));
   a.o = static_cast<const __nv_bfloat16*>(o);
   a.dO = static_cast<const __nv_bfloat16*>(dO);
   a.lse = lse;
@@ -402,6 +414,11 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   a.dv = static_cast<__nv_bfloat16*>(dv);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   a.dq_cnt = nullptr;  // the fused dQ's counters are not used here
+  if (d <= 64) {
+    // the dQ kernel writes D and -LSE*log2(e) itself, then dK/dV reads them
+    ATTN_TRY(launched(launch_bwd_dq(a, s)));
+    return launched(launch_bwd_dkdv(a, s));
+  }
   ATTN_TRY(launched(launch_bwd_preprocess(a, s)));
   ATTN_TRY(launched(launch_bwd_dkdv(a, s)));
   return launched(launch_bwd_dq(a, s));

@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
 // ---------------------------------------------------------------------------
 // shared-memory plan of the two tensor-core kernels
 // ---------------------------------------------------------------------------
-template <int D, bool FUSE = false>
+// NFIX: tiles fixed for a whole work item (K_j, V_j for dK/dV; Q_i, dO_i and, when the
+// dQ kernel computes D itself, O_i).
+template <int D, bool FUSE = false, int NFIX = 2>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
@@ -105,7 +107,7 @@ struct BwdCfg {
   static constexpr int OFF_FIX = 0;
   // per stage: two tiles (+ for dK/dV, 128 fp32 -LSE*log2e and 128 fp32 D)
   static constexpr int STAGE_BYTES = 2 * TL::BYTES + 1024;
-  static constexpr int OFF_STAGE = OFF_FIX + 2 * TL::BYTES;
+  static constexpr int OFF_STAGE = OFF_FIX + NFIX * TL::BYTES;
   // fused dQ only: dS^T as a bf16 128x128 shared-memory tile (A operand of dK += dS^T Q_i
   // and, read transposed, of dQ_ij = dS K_j), then the fp32 staging tile of dQ_ij on its
   // way to the workspace
@@ -167,10 +169,12 @@ struct BwdSmem {
 
 constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
-template <int D, bool FUSE = false>
+// fix_empty_count: arrivals that release an item's fixed tiles (the MMA commit, plus the
+// elementwise threads where they read a fixed tile themselves).
+template <int D, bool FUSE = false, int NFIX = 2>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
-                                                  volatile int*& abort) {
-  using C = BwdCfg<D, FUSE>;
+                                                  volatile int*& abort, uint32_t fix_empty_count = 1) {
+  using C = BwdCfg<D, FUSE, NFIX>;
   BwdSmem s;
   const uint32_t raw = smem_u32(smem_raw);
   s.base = (raw + 1023u) & ~1023u;
@@ -181,7 +185,7 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
   abort = reinterpret_cast<volatile int*>(s.gbase + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
     mbar_init(s.fix_full(), 1);
-    mbar_init(s.fix_empty(), 1);
+    mbar_init(s.fix_empty(), fix_empty_count);
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(s.st_full(i), 1);
       mbar_init(s.st_empty(i), 1);
@@ -711,20 +715,26 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
 // j (j <= i when causal). Persistent, two MMA issuers:
 //   warp 17: S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
 //   warp 18: dQ += dS_j K_j once dS_j (its own 64 TMEM columns) is written.
-template <int D, bool CAUSAL>
+// PRE (d <= 64): the kernel also does the preprocess for its query tile, so that it runs
+// first and no separate D launch is needed: O_i is staged with Q_i and dO_i, the
+// elementwise threads form D_i = rowsum(dO_i * O_i) and -LSE_i * log2(e) themselves at the
+// start of the item and write both to the workspace for the dK/dV kernel that follows.
+template <int D, bool CAUSAL, bool PRE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
-                       __nv_bfloat16* __restrict__ dq, int T, int T_pad, int BH, float scale,
-                       float scale_log2, uint32_t* __restrict__ err) {
-  using C = BwdCfg<D>;
+                       const __grid_constant__ CUtensorMap tmO, const float* __restrict__ lse,
+                       float* __restrict__ ws_nlse2, float* __restrict__ ws_D, __nv_bfloat16* __restrict__ dq,
+                       int T, int T_pad, int BH, float scale, float scale_log2, uint32_t* __restrict__ err) {
+  constexpr int NFIX = PRE ? 3 : 2;
+  using C = BwdCfg<D, false, NFIX>;
   using TL = Tile<D>;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
-  const BwdSmem sm = bwd_smem_setup<D>(smem_raw, tmem_slot, abort);
+  // with PRE the elementwise threads read O_i and dO_i themselves: they release them too
+  const BwdSmem sm = bwd_smem_setup<D, false, NFIX>(smem_raw, tmem_slot, abort, PRE ? 1u + kEwThreads : 1u);
   const Abort ab{abort, err};
   const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -735,7 +745,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto query_tile = [&](int u) { return n_k - 1 - u / BH; };
   auto n_iters = [&](int u) { return CAUSAL ? query_tile(u) + 1 : n_k; };
 
-  const uint32_t sQ = sm.base + C::OFF_FIX, sdO = sQ + TL::BYTES;
+  const uint32_t sQ = sm.base + C::OFF_FIX, sdO = sQ + TL::BYTES, sO = sdO + TL::BYTES;
   auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sV = [&](int s) { return sK(s) + TL::BYTES; };
 
@@ -752,9 +762,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
         if (r > 0 && !(ok = mbar_wait(sm.fix_empty(), (r - 1) & 1, ab, kErrTimeoutLoad))) break;
         ++fix_issued;
-        mbar_arrive_expect_tx(sm.fix_full(), 2 * TL::BYTES);
+        mbar_arrive_expect_tx(sm.fix_full(), NFIX * TL::BYTES);
         TL::load(sQ, &tmQ, qt * kTileRows, bh, sm.fix_full());
         TL::load(sdO, &tmdO, qt * kTileRows, bh, sm.fix_full());
+        if (PRE) TL::load(sO, &tmO, qt * kTileRows, bh, sm.fix_full());
         for (int it = 0; it < n_it; ++it, ++g) {
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
@@ -842,8 +853,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
       const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
       const int row = qt * kTileRows + r;
-      const float nl = ws_nlse2[(size_t)bh * T_pad + row];
-      const float Dr = ws_D[(size_t)bh * T_pad + row];
+      float nl, Dr;
+      if constexpr (PRE) {
+        // D for this row from the staged O_i and dO_i rows (zero past T, as TMA fills them)
+        if (!(ok = mbar_wait_warp(sm.fix_full(), ri & 1, ab, kErrTimeoutElem))) break;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < TL::NCHUNK; ++c)
+#pragma unroll
+          for (int gi = 0; gi < TL::ROW_BYTES / 16; ++gi) {
+            const uint32_t off = TL::granule_off(r, c, gi);
+            const uint4 ov = lds128(sO + off), dv4 = lds128(sdO + off);
+            const uint32_t* ow = &ov.x;
+            const uint32_t* dw = &dv4.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              a0 = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), a0);
+              a1 = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), a1);
+            }
+          }
+        mbar_arrive(sm.fix_empty());  // O_i, dO_i read (the MMA commit is the other arrival)
+        Dr = a0 + a1;
+        nl = row < T ? -lse[(size_t)bh * T + row] * kLog2e : -INFINITY;
+        if (hc == 0) {
+          ws_nlse2[(size_t)bh * T_pad + row] = nl;
+          ws_D[(size_t)bh * T_pad + row] = Dr;
+        }
+      } else {
+        nl = ws_nlse2[(size_t)bh * T_pad + row];
+        Dr = ws_D[(size_t)bh * T_pad + row];
+      }
       const uint64_t nl2 = f2_pack(nl, nl), D2 = f2_pack(Dr, Dr);
       for (int it = 0; it < n_it; ++it, ++g) {
         if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
@@ -994,14 +1033,18 @@ cudaError_t launch_dq_finish(const BwdArgs& a, cudaStream_t stream) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
-  auto kern = attn_bwd_dq_kernel<D, CAUSAL>;
+  // d <= 64: the dQ kernel forms D itself (and runs before dK/dV)
+  constexpr bool PRE = D <= 64;
+  using C = BwdCfg<D, false, PRE ? 3 : 2>;
+  auto kern = attn_bwd_dq_kernel<D, CAUSAL, PRE>;
   static uint32_t configured = 0;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), BwdCfg<D>::SMEM_BYTES, &configured);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
+  if (PRE && (!a.tmO || !a.lse)) return cudaErrorInvalidValue;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
-  kern<<<min(n_items, a.num_sms), kBwdThreads, BwdCfg<D>::SMEM_BYTES, stream>>>(
-      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.scale,
-      a.scale * kLog2e, a.err);
+  kern<<<min(n_items, a.num_sms), kBwdThreads, C::SMEM_BYTES, stream>>>(
+      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH,
+      a.scale, a.scale * kLog2e, a.err);
   return cudaGetLastError();
 }
 

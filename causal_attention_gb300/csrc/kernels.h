@@ -29,6 +29,7 @@ struct BwdArgs {
   const CUtensorMap* tmK;
   const CUtensorMap* tmV;
   const CUtensorMap* tmdO;
+  const CUtensorMap* tmO;  // O as a tensor map (the d <= 64 dQ kernel stages it), else null
   const __nv_bfloat16* o;
   const __nv_bfloat16* dO;
   const float* lse;
@@ -50,6 +51,8 @@ inline int pad_rows(int T) { return (T + 127) / 128 * 128; }
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream);
+// dQ; at d <= 64 it also writes D and -LSE*log2(e) into the workspace (needs tmO, lse),
+// so it runs first and replaces the preprocess launch
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv_dq(const BwdArgs& a, cudaStream_t stream);  // fused dK, dV, dQ (d <= 64)
 cudaError_t launch_bwd_dq_finish(const BwdArgs& a, cudaStream_t stream);

@@ -57,6 +57,14 @@ struct Tile {
   // descriptor offset of a tile that starts `bytes` later
   static __host__ __device__ constexpr uint64_t bytes_off(uint32_t bytes) { return bytes >> 4; }
 
+  // Byte offset, within a tile written by TMA, of 16-byte granule g of row r in column
+  // chunk c: the 128-byte swizzle XORs the granule index with r mod 8, the 64-byte one
+  // (d = 32) with (r / 2) mod 4 (address bits 4-6 / 4-5 with bits 7-9 / 7-8).
+  static __device__ __forceinline__ uint32_t granule_off(int r, int c, int g) {
+    const uint32_t sw = ROW_BYTES == 128 ? (uint32_t)(r & 7) : (uint32_t)((r >> 1) & 3);
+    return (uint32_t)c * CHUNK_BYTES + (uint32_t)r * ROW_BYTES + (((uint32_t)g ^ sw) << 4);
+  }
+
   // Issue the TMA loads of one tile (rows row0..row0+127 of slice bh).
   static __device__ __forceinline__ void load(uint32_t dst, const CUtensorMap* m, int row0, int bh,
                                               uint32_t bar) {

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 typedef enum attn_status {
   ATTN_OK = 0,
@@ -81,14 +81,15 @@ size_t attn_bwd_fused_workspace_size(int B, int H, int T, int d);
 /*
  * Backward. Cited definition: Forge RESEARCH.md section 6, "The D term is free"
  * and "Backward (training)"; the three-stage atomic-free structure of the Forge
- * paper's "Ecosystem survey". Equivalent to attn_bwd_preprocess, then
- * attn_bwd_dkdv, then attn_bwd_dq, on the same stream.
+ * paper's "Ecosystem survey". Equivalent to, on the same stream: at d <= 64
+ * attn_bwd_dq (which also forms D) then attn_bwd_dkdv; at d = 128 attn_bwd_preprocess,
+ * attn_bwd_dkdv, attn_bwd_dq.
  *   q, k, v, o, dO : bf16 [B, H, T, d] (o and lse as written by attn_fwd)
  *   lse            : fp32 [B, H, T]
  *   dq, dk, dv     : bf16 [B, H, T, d] outputs
  *   workspace      : >= attn_bwd_workspace_size(B, H, T, d) bytes of device memory,
  *                    16-byte aligned; its contents on entry do not matter
- * Three kernel launches.
+ * Two kernel launches at d <= 64, three at d = 128.
  */
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                      const float* lse, void* dq, void* dk, void* dv, void* workspace,
@@ -104,17 +105,21 @@ attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse,
 
 /* Backward stage 2: dK and dV, one CTA per 128-key tile looping over query tiles
  * (Forge paper, "Attention kernel design": transposes by operand-role swap).
- * Reads the workspace written by stage 1. */
+ * Reads the D / LSE workspace written by stage 1 or, at d <= 64, by attn_bwd_dq. */
 attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
                           void* dv, const void* workspace, size_t workspace_bytes, int B, int H,
                           int T, int d, float scale, int causal, void* stream);
 
 /* Backward stage 3: dQ, one CTA per 128-query tile looping over key tiles
  * (deterministic; Forge RESEARCH.md section 6, "a dQ kernel with grid (NQ, H, B)").
- * Reads the workspace written by stage 1. */
-attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
-                        const void* workspace, size_t workspace_bytes, int B, int H, int T, int d,
-                        float scale, int causal, void* stream);
+ * At d = 128 it reads the workspace written by stage 1. At d <= 64 it does stage 1's
+ * work for its own query tile (D = rowsum(dO * O) from a staged O tile, -LSE * log2(e)
+ * from lse) and writes both into the workspace, so it needs no stage 1 before it and
+ * attn_bwd_dkdv may follow it; o and lse are read only at d <= 64 but are always
+ * checked. */
+attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                        const float* lse, void* dq, void* workspace, size_t workspace_bytes, int B, int H,
+                        int T, int d, float scale, int causal, void* stream);
 
 /*
  * Backward stage 2 with dQ fused (d <= 64 only; an alternative to attn_bwd_dkdv followed
