@@ -214,6 +214,16 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   return ATTN_OK;
 }
 
+// dK and dV as tensor maps, for the d <= 64 dK/dV kernel's TMA-store epilogue.
+attn_status bwd_map_dkdv(BwdArgs* a, const void* dk, const void* dv, CUtensorMap* maps) {
+  if (a->d > 64) return ATTN_OK;
+  ATTN_TRY(make_map(&maps[0], dk, a->BH, a->T, a->d));
+  ATTN_TRY(make_map(&maps[1], dv, a->BH, a->T, a->d));
+  a->tmdK = &maps[0];
+  a->tmdV = &maps[1];
+  return ATTN_OK;
+}
+
 // O as a fifth tensor map, for the d <= 64 dQ kernel that stages it to form D itself.
 attn_status bwd_map_o(BwdArgs* a, const void* o, CUtensorMap* map) {
   if (a->d > 64) return ATTN_OK;
@@ -340,8 +350,9 @@ attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const voi
   ATTN_TRY(check_ptrs({q, k, v, dO, dk, dv}));
   ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, T));
   BwdArgs a;
-  CUtensorMap maps[4];
+  CUtensorMap maps[6];
   ATTN_TRY(bwd_args(&a, q, k, v, dO, workspace, B, H, T, d, scale, causal, maps, true));
+  ATTN_TRY(bwd_map_dkdv(&a, dk, dv, &maps[4]));
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   return launched(launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)));
@@ -403,9 +414,10 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   ATTN_TRY(check_ptrs({q, k, v, o, dO, lse, dq, dk, dv}));
   ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, T));
   BwdArgs a;
-  CUtensorMap maps[5];
+  CUtensorMap maps[7];
   ATTN_TRY(bwd_args(&a, q, k, v, dO, workspace, B, H, T, d, scale, causal, maps, true));
   ATTN_TRY(bwd_map_o(&a, o, &maps[4]));
+  ATTN_TRY(bwd_map_dkdv(&a, dk, dv, &maps[5]));
   a.o = static_cast<const __nv_bfloat16*>(o);
   a.dO = static_cast<const __nv_bfloat16*>(dO);
   a.lse = lse;

@@ -98,8 +98,9 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
 // shared-memory plan of the two tensor-core kernels
 // ---------------------------------------------------------------------------
 // NFIX: tiles fixed for a whole work item (K_j, V_j for dK/dV; Q_i, dO_i and, when the
-// dQ kernel computes D itself, O_i).
-template <int D, bool FUSE = false, int NFIX = 2>
+// dQ kernel computes D itself, O_i). NEPI: bf16 output tiles staged in shared memory for
+// a TMA store in the epilogue (dV and dK).
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
@@ -115,8 +116,9 @@ struct BwdCfg {
   static constexpr int DQS_BYTES = FUSE ? kTileRows * D * 4 : 0;
   static constexpr int OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
-  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 14 + (FUSE ? 5 : 0);
+  static constexpr int OFF_EPI = OFF_DQS + DQS_BYTES;
+  static constexpr int OFF_BAR = OFF_EPI + NEPI * TL::BYTES;
+  static constexpr int NBAR = 1 + 2 * STAGES + 20;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -165,16 +167,18 @@ struct BwdSmem {
   __device__ uint32_t dqs_full() const { return bar0 + 8u * (16 + 2 * st); }
   __device__ uint32_t dqs_free() const { return bar0 + 8u * (17 + 2 * st); }
   __device__ uint32_t drain3() const { return bar0 + 8u * (18 + 2 * st); }
+  // epilogue through shared memory: the TMA stores of the previous item read its tiles
+  __device__ uint32_t epi_free() const { return bar0 + 8u * (19 + 2 * st); }
 };
 
 constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
 // fix_empty_count: arrivals that release an item's fixed tiles (the MMA commit, plus the
 // elementwise threads where they read a fixed tile themselves).
-template <int D, bool FUSE = false, int NFIX = 2>
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
                                                   volatile int*& abort, uint32_t fix_empty_count = 1) {
-  using C = BwdCfg<D, FUSE, NFIX>;
+  using C = BwdCfg<D, FUSE, NFIX, NEPI>;
   BwdSmem s;
   const uint32_t raw = smem_u32(smem_raw);
   s.base = (raw + 1023u) & ~1023u;
@@ -202,6 +206,7 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     mbar_init(s.acc_free(), kEwThreads);
     mbar_init(s.drain(), 1);
     mbar_init(s.drain2(), 1);
+    mbar_init(s.epi_free(), 1);
     if (FUSE) {
       mbar_init(s.dq_done(), 1);
       mbar_init(s.dq_free(), kEwThreads);
@@ -262,6 +267,28 @@ __device__ __forceinline__ void store_acc_quarter(uint32_t tacc, __nv_bfloat16* 
   }
 }
 
+// Epilogue through shared memory: the warpgroup hc of four converts its quarter of one
+// accumulator row (d fp32 TMEM columns from `tacc`, times `mul`) to bf16 and writes it
+// into row r of a Tile<D>-layout shared tile (the layout a TMA store of the tile reads).
+template <int D>
+__device__ __forceinline__ void stage_acc_quarter(uint32_t tacc, uint32_t tile, int r, int hc, float mul) {
+  using TL = Tile<D>;
+  constexpr int QW = D / 4;  // 8, 16 or 32 columns = 1, 2 or 4 granules of 16 bytes
+  uint32_t u[QW];
+  if constexpr (QW == 32) tmem_ld32(tacc + (uint32_t)(hc * QW), u);
+  else if constexpr (QW == 16) tmem_ld16(tacc + (uint32_t)(hc * QW), u);
+  else tmem_ld8(tacc + (uint32_t)(hc * QW), u);
+  tmem_wait_ld();
+  const int c = (hc * QW) / TL::CHUNK_ELEMS, g0 = ((hc * QW) % TL::CHUNK_ELEMS) / 8;
+#pragma unroll
+  for (int k = 0; k < QW / 8; ++k)
+    sts128(tile + TL::granule_off(r, c, g0 + k),
+           pack_bf16(__uint_as_float(u[8 * k + 0]) * mul, __uint_as_float(u[8 * k + 1]) * mul),
+           pack_bf16(__uint_as_float(u[8 * k + 2]) * mul, __uint_as_float(u[8 * k + 3]) * mul),
+           pack_bf16(__uint_as_float(u[8 * k + 4]) * mul, __uint_as_float(u[8 * k + 5]) * mul),
+           pack_bf16(__uint_as_float(u[8 * k + 6]) * mul, __uint_as_float(u[8 * k + 7]) * mul));
+}
+
 // Work items of a persistent kernel, sorted longest first, dealt to the CTAs in a snake
 // order (round r goes left to right when r is even, right to left when odd) so that every
 // CTA gets about the same total work.
@@ -273,6 +300,13 @@ struct Sched {
     return u < n_items ? u : -1;
   }
 };
+
+// Number of items the schedule gives this CTA.
+__device__ __forceinline__ int sched_count(const Sched& s) {
+  int n = 0;
+  while (s.item(n) >= 0) ++n;
+  return n;
+}
 
 // Producer drain after an abort: every copy issued must land before the CTA exits.
 __device__ __forceinline__ void drain_loads(const BwdSmem& sm, int fix_issued, int st_issued, int st,
@@ -329,11 +363,15 @@ template <int D, bool CAUSAL, bool FUSE>
 __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                          const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
                          __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dq_acc,
                          int* __restrict__ dq_cnt, int T, int T_pad, int BH, float scale, float scale_log2,
                          uint32_t* __restrict__ err) {
-  using C = BwdCfg<D, FUSE>;
+  // persistent d <= 64: dV and dK leave through shared memory and TMA stores
+  constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE;
+  constexpr int NEPI = EPI ? 2 : 0;
+  using C = BwdCfg<D, FUSE, 2, NEPI>;
   using TL = Tile<D>;
   using TD = Tile<128>;  // the dS^T tile: 128 key rows x 128 query columns
   constexpr int ST = C::STAGES;
@@ -341,7 +379,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
-  const BwdSmem sm = bwd_smem_setup<D, FUSE>(smem_raw, tmem_slot, abort);
+  const BwdSmem sm = bwd_smem_setup<D, FUSE, 2, NEPI>(smem_raw, tmem_slot, abort);
   const Abort ab{abort, err};
   const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -356,7 +394,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
   auto sQ = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sdO = [&](int s) { return sQ(s) + TL::BYTES; };
   auto sL = [&](int s) { return sQ(s) + 2 * TL::BYTES; };  // 128 fp32 -LSE*log2e, then 128 fp32 D
-  const uint32_t sDS = sm.base + C::OFF_DS, sDQS = sm.base + C::OFF_DQS;
+  const uint32_t sDS = sm.base + C::OFF_DS, sDQS = sm.base + C::OFF_DQS, sEPI = sm.base + C::OFF_EPI;
 
   if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
@@ -472,8 +510,19 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       const uint32_t tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
       const uint64_t dQm0 = TL::desc_mnmajor0(sQ(0)), dOm0 = TL::desc_mnmajor0(sdO(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
+      // EPI: the previous item's dV / dK tiles, staged by the elementwise warps before they
+      // arrived on acc_free, go out with TMA stores (rows past T are clipped by the maps)
+      auto store_epi = [&](int u_prev) {
+#pragma unroll
+        for (int c = 0; c < TL::NCHUNK; ++c) {
+          const int row0 = key_tile(u_prev) * kTileRows, bh_prev = u_prev % BH;
+          tma_store_3d(&tmdV, sEPI + c * TL::CHUNK_BYTES, c * TL::CHUNK_ELEMS, row0, bh_prev);
+          tma_store_3d(&tmdK, sEPI + TL::BYTES + c * TL::CHUNK_BYTES, c * TL::CHUNK_ELEMS, row0, bh_prev);
+        }
+        bulk_commit();
+      };
       bool ok = true;
-      int g = 0;
+      int g = 0, u_prev = -1;
       for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
         const int n_it = n_iters(u);
         for (int it = 0; it < n_it; ++it, ++g) {
@@ -481,6 +530,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
           if (!(ok = mbar_wait(sm.p_full(), g & 1, ab, kErrTimeoutMma))) break;
           // the accumulators still hold the previous item until its epilogue read them
           if (it == 0 && r > 0 && !(ok = mbar_wait(sm.acc_free(), (r - 1) & 1, ab, kErrTimeoutMma))) break;
+          if (EPI && it == 0 && r > 0) store_epi(u_prev);
           tc_fence_after();
           // dV += P^T dO_i (M = keys, N = d, K = queries)
           mma_chain_ts<TL, false>(tDV, tmem + C::COL_P, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
@@ -515,7 +565,19 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         }
         if (ok) mma_commit(sm.acc_full());
         if (FUSE && ok) mma_commit(sm.fix_empty());  // K_j (dQ MMAs) and V_j are no longer read
+        if (EPI && ok && r > 0) {
+          // the previous item's stores have read the staging tiles: the next epilogue may
+          // overwrite them
+          bulk_wait_read_all();
+          mbar_arrive(sm.epi_free());
+        }
+        u_prev = u;
       }
+      if (EPI && ok && u_prev >= 0) {
+        // the last item: wait for its epilogue to fill the staging tiles, store them
+        if ((ok = mbar_wait(sm.acc_free(), (sched_count(sched) - 1) & 1, ab, kErrTimeoutMma))) store_epi(u_prev);
+      }
+      if (EPI) bulk_wait_all();  // every store has landed before the CTA exits
       if (!ok) {
         mma_commit(sm.drain2());
         mbar_wait_drain(sm.drain2(), 0, ab);
@@ -692,10 +754,21 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       tc_fence_after();
       const int key = kt * kTileRows + r;
       const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)D;
-      store_acc_quarter<D>(tDV, dv + ((size_t)bh * T + key) * D, hc, 1.f, key < T);
-      store_acc_quarter<D>(tDK, dk + ((size_t)bh * T + key) * D, hc, scale, key < T);
-      tc_fence_before();
-      mbar_arrive(sm.acc_free());
+      if constexpr (EPI) {
+        // into the staging tiles (free once the previous item's TMA stores have read them);
+        // warp 18 stores them once acc_free says every thread has written its part
+        if (ri > 0 && !(ok = mbar_wait_warp(sm.epi_free(), (ri - 1) & 1, ab, kErrTimeoutElem))) break;
+        stage_acc_quarter<D>(tDV, sEPI, r, hc, 1.f);
+        stage_acc_quarter<D>(tDK, sEPI + TL::BYTES, r, hc, scale);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(sm.acc_free());
+      } else {
+        store_acc_quarter<D>(tDV, dv + ((size_t)bh * T + key) * D, hc, 1.f, key < T);
+        store_acc_quarter<D>(tDK, dk + ((size_t)bh * T + key) * D, hc, scale, key < T);
+        tc_fence_before();
+        mbar_arrive(sm.acc_free());
+      }
     }
     if (FUSE && ok && g > 0) dq_readout(g - 1);  // the last iteration's dQ_ij
   }
@@ -1007,7 +1080,8 @@ cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
 
 template <int D, bool CAUSAL, bool FUSE>
 cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
-  using C = BwdCfg<D, FUSE>;
+  constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE;
+  using C = BwdCfg<D, FUSE, 2, EPI ? 2 : 0>;
   auto kern = attn_bwd_dkdv_kernel<D, CAUSAL, FUSE>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
@@ -1015,7 +1089,9 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
   // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
   const int grid = C::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, a.ws_nlse2, a.ws_D, a.dk,
+  if (EPI && (!a.tmdK || !a.tmdV)) return cudaErrorInvalidValue;
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, EPI ? *a.tmdK : *a.tmQ,
+                                                     EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk,
                                                      a.dv, a.dq_acc, a.dq_cnt, a.T, a.T_pad, a.BH, a.scale,
                                                      a.scale * kLog2e, a.err);
   return cudaGetLastError();

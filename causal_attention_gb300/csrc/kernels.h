@@ -30,6 +30,8 @@ struct BwdArgs {
   const CUtensorMap* tmV;
   const CUtensorMap* tmdO;
   const CUtensorMap* tmO;  // O as a tensor map (the d <= 64 dQ kernel stages it), else null
+  const CUtensorMap* tmdK;  // dK, dV as tensor maps (the d <= 64 dK/dV kernel stores through
+  const CUtensorMap* tmdV;  // them), else null
   const __nv_bfloat16* o;
   const __nv_bfloat16* dO;
   const float* lse;
