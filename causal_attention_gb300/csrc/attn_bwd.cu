@@ -104,11 +104,14 @@ template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
-  // fixed tiles of a work item (K_j, V_j for dK/dV; Q_i, dO_i for dQ)
+  // fixed tiles of a work item (K_j, V_j for dK/dV; Q_i, dO_i for dQ), in NSLOT slots:
+  // with two (persistent kernels at d <= 64) the next item's tiles load during this one
+  static constexpr int NSLOT = (D <= 64 && !FUSE) ? 2 : 1;
   static constexpr int OFF_FIX = 0;
   // per stage: two tiles (+ for dK/dV, 128 fp32 -LSE*log2e and 128 fp32 D)
   static constexpr int STAGE_BYTES = 2 * TL::BYTES + 1024;
-  static constexpr int OFF_STAGE = OFF_FIX + NFIX * TL::BYTES;
+  static constexpr int SLOT_BYTES = NFIX * TL::BYTES;
+  static constexpr int OFF_STAGE = OFF_FIX + NSLOT * SLOT_BYTES;
   // fused dQ only: dS^T as a bf16 128x128 shared-memory tile (A operand of dK += dS^T Q_i
   // and, read transposed, of dQ_ij = dS K_j), then the fp32 staging tile of dQ_ij on its
   // way to the workspace
@@ -118,7 +121,7 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_EPI = OFF_DQS + DQS_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + NEPI * TL::BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 20;
+  static constexpr int NBAR = 1 + 2 * STAGES + 22;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -144,7 +147,7 @@ struct BwdSmem {
   uint8_t* gbase;
   uint32_t bar0;
   int st;
-  __device__ uint32_t fix_full() const { return bar0; }
+  __device__ uint32_t fix_full(int b) const { return b ? bar0 + 8u * (20 + 2 * st) : bar0; }
   __device__ uint32_t st_full(int s) const { return bar0 + 8u * (1 + s); }
   __device__ uint32_t st_empty(int s) const { return bar0 + 8u * (1 + st + s); }
   __device__ uint32_t s_full() const { return bar0 + 8u * (1 + 2 * st); }
@@ -158,7 +161,7 @@ struct BwdSmem {
   __device__ uint32_t dv_done() const { return bar0 + 8u * (9 + 2 * st); }
   __device__ uint32_t dk_done() const { return bar0 + 8u * (10 + 2 * st); }
   __device__ uint32_t drain2() const { return bar0 + 8u * (11 + 2 * st); }
-  __device__ uint32_t fix_empty() const { return bar0 + 8u * (12 + 2 * st); }
+  __device__ uint32_t fix_empty(int b) const { return bar0 + 8u * (b ? 21 + 2 * st : 12 + 2 * st); }
   __device__ uint32_t acc_free() const { return bar0 + 8u * (13 + 2 * st); }
   // fused dQ: the dQ_ij MMA finished (dS^T tile and TMEM columns read) / its TMEM columns
   // were read out / the staging tile is written / the staging tile was read by the copy
@@ -188,8 +191,10 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
   tmem_slot = reinterpret_cast<uint32_t*>(s.gbase + C::OFF_MISC);
   abort = reinterpret_cast<volatile int*>(s.gbase + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
-    mbar_init(s.fix_full(), 1);
-    mbar_init(s.fix_empty(), fix_empty_count);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s.fix_full(b), 1);
+      mbar_init(s.fix_empty(b), fix_empty_count);
+    }
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(s.st_full(i), 1);
       mbar_init(s.st_empty(i), 1);
@@ -309,9 +314,10 @@ __device__ __forceinline__ int sched_count(const Sched& s) {
 }
 
 // Producer drain after an abort: every copy issued must land before the CTA exits.
-__device__ __forceinline__ void drain_loads(const BwdSmem& sm, int fix_issued, int st_issued, int st,
+__device__ __forceinline__ void drain_loads(const BwdSmem& sm, int fix_issued, int nslot, int st_issued, int st,
                                             const Abort& ab) {
-  if (fix_issued > 0) mbar_wait_drain(sm.fix_full(), (fix_issued - 1) & 1, ab);
+  for (int x = max(0, fix_issued - nslot); x < fix_issued; ++x)
+    mbar_wait_drain(sm.fix_full(x % nslot), (x / nslot) & 1, ab);
   for (int g = max(0, st_issued - st); g < st_issued; ++g) mbar_wait_drain(sm.st_full(g % st), (g / st) & 1, ab);
 }
 
@@ -390,7 +396,8 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
   auto key_tile = [&](int u) { return u / BH; };
   auto n_iters = [&](int u) { return n_q - (CAUSAL ? key_tile(u) : 0); };
 
-  const uint32_t sK = sm.base + C::OFF_FIX, sV = sK + TL::BYTES;
+  constexpr int NS = C::NSLOT;
+  auto sKf = [&](int slot) { return sm.base + C::OFF_FIX + slot * C::SLOT_BYTES; };  // K_j, then V_j
   auto sQ = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sdO = [&](int s) { return sQ(s) + TL::BYTES; };
   auto sL = [&](int s) { return sQ(s) + 2 * TL::BYTES; };  // 128 fp32 -LSE*log2e, then 128 fp32 D
@@ -407,11 +414,12 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       int g = 0, r = 0, fix_issued = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
         const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
-        if (r > 0 && !(ok = mbar_wait(sm.fix_empty(), (r - 1) & 1, ab, kErrTimeoutLoad))) break;
+        const int slot = r % NS;
+        if (r >= NS && !(ok = mbar_wait(sm.fix_empty(slot), (r / NS - 1) & 1, ab, kErrTimeoutLoad))) break;
         ++fix_issued;
-        mbar_arrive_expect_tx(sm.fix_full(), 2 * TL::BYTES);
-        TL::load(sK, &tmK, kt * kTileRows, bh, sm.fix_full());
-        TL::load(sV, &tmV, kt * kTileRows, bh, sm.fix_full());
+        mbar_arrive_expect_tx(sm.fix_full(slot), 2 * TL::BYTES);
+        TL::load(sKf(slot), &tmK, kt * kTileRows, bh, sm.fix_full(slot));
+        TL::load(sKf(slot) + TL::BYTES, &tmV, kt * kTileRows, bh, sm.fix_full(slot));
         for (int it = 0; it < n_it; ++it, ++g) {
           const int s = g % ST, n = g / ST, qi = i0 + it;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
@@ -423,7 +431,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
           bulk_load(sL(s) + 512, ws_D + woff, 512, sm.st_full(s));
         }
       }
-      if (!ok) drain_loads(sm, fix_issued, g, ST, ab);
+      if (!ok) drain_loads(sm, fix_issued, C::NSLOT, g, ST, ab);
     }
   } else if (warp == kWarpMmaA) {
     // ------------------------------------------------------------ MMA issuer (S, dP)
@@ -431,8 +439,8 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
-      // K-step-0 descriptors, computed once; stage s adds s stages
-      const uint64_t dKk = TL::desc_kmajor0(sK), dVk = TL::desc_kmajor0(sV);
+      // K-step-0 descriptors: K_j / V_j per item (their slot), stage s adds s stages
+      uint64_t dKk = 0, dVk = 0;
       const uint64_t dQk0 = TL::desc_kmajor0(sQ(0)), dQm0 = TL::desc_mnmajor0(sQ(0));
       const uint64_t dOk0 = TL::desc_kmajor0(sdO(0)), dOm0 = TL::desc_mnmajor0(sdO(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
@@ -445,8 +453,10 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       bool ok = true;
       int g = 0;
       for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
-        const int n_it = n_iters(u);
-        if (!(ok = mbar_wait(sm.fix_full(), r & 1, ab, kErrTimeoutMma))) break;
+        const int n_it = n_iters(u), slot = r % NS;
+        if (!(ok = mbar_wait(sm.fix_full(slot), (r / NS) & 1, ab, kErrTimeoutMma))) break;
+        dKk = TL::desc_kmajor0(sKf(slot));
+        dVk = TL::desc_kmajor0(sKf(slot) + TL::BYTES);
         if constexpr (SEP) {
           for (int it = 0; it < n_it; ++it, ++g) {
             const int s = g % ST;
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
             mma_commit(sm.dp_full());
             // K_j, V_j are no longer read (with FUSE, K_j is read by the dQ MMAs of warp 18,
             // which releases them)
-            if (!FUSE && it == n_it - 1) mma_commit(sm.fix_empty());
+            if (!FUSE && it == n_it - 1) mma_commit(sm.fix_empty(slot));
           }
         } else {
           // P^T / dS^T written over S^T / dP^T: same-thread issue order is the guard
@@ -494,7 +504,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
             }
           }
           if (!ok) break;
-          mma_commit(sm.fix_empty());
+          mma_commit(sm.fix_empty(slot));
           mma_commit(sm.acc_full());
         }
       }
@@ -548,7 +558,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
             if (g > 0 && !(ok = mbar_wait(sm.dq_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;
             tc_fence_after();
             constexpr uint32_t idesc_dq = idesc_bf16(128, D, 1, 1);
-            const uint64_t q0 = TD::desc_mnmajor0(sDS), k0 = TL::desc_mnmajor0(sK);
+            const uint64_t q0 = TD::desc_mnmajor0(sDS), k0 = TL::desc_mnmajor0(sKf(0));  // FUSE: one slot
 #pragma unroll
             for (int k = 0; k < kTileRows / 16; ++k)
               mma_ss(tmem + C::COL_DQ, q0 + TD::mnmajor_off(k), k0 + TL::mnmajor_off(k), idesc_dq, k > 0 ? 1u : 0u);
@@ -564,7 +574,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
           mma_commit(sm.st_empty(s));
         }
         if (ok) mma_commit(sm.acc_full());
-        if (FUSE && ok) mma_commit(sm.fix_empty());  // K_j (dQ MMAs) and V_j are no longer read
+        if (FUSE && ok) mma_commit(sm.fix_empty(0));  // K_j (dQ MMAs) and V_j are no longer read
         if (EPI && ok && r > 0) {
           // the previous item's stores have read the staging tiles: the next epilogue may
           // overwrite them
@@ -818,7 +828,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto query_tile = [&](int u) { return n_k - 1 - u / BH; };
   auto n_iters = [&](int u) { return CAUSAL ? query_tile(u) + 1 : n_k; };
 
-  const uint32_t sQ = sm.base + C::OFF_FIX, sdO = sQ + TL::BYTES, sO = sdO + TL::BYTES;
+  constexpr int NS = C::NSLOT;
+  // fixed tiles of slot b: Q_i, dO_i (, O_i)
+  auto sQf = [&](int b) { return sm.base + C::OFF_FIX + b * C::SLOT_BYTES; };
   auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sV = [&](int s) { return sK(s) + TL::BYTES; };
 
@@ -833,12 +845,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int g = 0, r = 0, fix_issued = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
         const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
-        if (r > 0 && !(ok = mbar_wait(sm.fix_empty(), (r - 1) & 1, ab, kErrTimeoutLoad))) break;
+        const int slot = r % NS;
+        if (r >= NS && !(ok = mbar_wait(sm.fix_empty(slot), (r / NS - 1) & 1, ab, kErrTimeoutLoad))) break;
         ++fix_issued;
-        mbar_arrive_expect_tx(sm.fix_full(), NFIX * TL::BYTES);
-        TL::load(sQ, &tmQ, qt * kTileRows, bh, sm.fix_full());
-        TL::load(sdO, &tmdO, qt * kTileRows, bh, sm.fix_full());
-        if (PRE) TL::load(sO, &tmO, qt * kTileRows, bh, sm.fix_full());
+        mbar_arrive_expect_tx(sm.fix_full(slot), NFIX * TL::BYTES);
+        TL::load(sQf(slot), &tmQ, qt * kTileRows, bh, sm.fix_full(slot));
+        TL::load(sQf(slot) + TL::BYTES, &tmdO, qt * kTileRows, bh, sm.fix_full(slot));
+        if (PRE) TL::load(sQf(slot) + 2 * TL::BYTES, &tmO, qt * kTileRows, bh, sm.fix_full(slot));
         for (int it = 0; it < n_it; ++it, ++g) {
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
@@ -847,21 +860,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           TL::load(sV(s), &tmV, it * kTileRows, bh, sm.st_full(s));
         }
       }
-      if (!ok) drain_loads(sm, fix_issued, g, ST, ab);
+      if (!ok) drain_loads(sm, fix_issued, C::NSLOT, g, ST, ab);
     }
   } else if (warp == kWarpMmaA) {
     // ------------------------------------------------------------ MMA issuer (S, dP)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       const uint32_t tS = tmem, tDP = tmem + 128u;
-      const uint64_t dQk = TL::desc_kmajor0(sQ), dOk = TL::desc_kmajor0(sdO);
       const uint64_t dKk0 = TL::desc_kmajor0(sK(0)), dVk0 = TL::desc_kmajor0(sV(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       bool ok = true;
       int g = 0;
       for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
-        const int n_it = n_iters(u);
-        if (!(ok = mbar_wait(sm.fix_full(), r & 1, ab, kErrTimeoutMma))) break;
+        const int n_it = n_iters(u), slot = r % NS;
+        if (!(ok = mbar_wait(sm.fix_full(slot), (r / NS) & 1, ab, kErrTimeoutMma))) break;
+        const uint64_t dQk = TL::desc_kmajor0(sQf(slot)), dOk = TL::desc_kmajor0(sQf(slot) + TL::BYTES);
         for (int it = 0; it < n_it; ++it, ++g) {
           const int s = g % ST;
           if (g > 0 && !(ok = mbar_wait(sm.s_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // S read out
@@ -875,7 +888,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dP = dO_i V_j^T
           mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
           mma_commit(sm.dp_full());
-          if (it == n_it - 1) mma_commit(sm.fix_empty());  // Q_i, dO_i are no longer read
+          if (it == n_it - 1) mma_commit(sm.fix_empty(slot));  // Q_i, dO_i are no longer read
         }
       }
       if (!ok) {
@@ -929,7 +942,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       float nl, Dr;
       if constexpr (PRE) {
         // D for this row from the staged O_i and dO_i rows (zero past T, as TMA fills them)
-        if (!(ok = mbar_wait_warp(sm.fix_full(), ri & 1, ab, kErrTimeoutElem))) break;
+        const int slot = ri % NS;
+        if (!(ok = mbar_wait_warp(sm.fix_full(slot), (ri / NS) & 1, ab, kErrTimeoutElem))) break;
+        const uint32_t sdO = sQf(slot) + TL::BYTES, sO = sdO + TL::BYTES;
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int c = 0; c < TL::NCHUNK; ++c)
@@ -945,7 +960,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               a1 = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), a1);
             }
           }
-        mbar_arrive(sm.fix_empty());  // O_i, dO_i read (the MMA commit is the other arrival)
+        mbar_arrive(sm.fix_empty(slot));  // O_i, dO_i read (the MMA commit is the other arrival)
         Dr = a0 + a1;
         nl = row < T ? -lse[(size_t)bh * T + row] * kLog2e : -INFINITY;
         if (hc == 0) {
