@@ -1,8 +1,9 @@
 """Throughput of the fused causal attention forward + backward on GB300.
 
-One step = attn_fwd followed by attn_bwd (preprocess, dK/dV, dQ) over one batch of
-the workload, through the C ABI (with --fused-dq, at d <= 64: preprocess, dK/dV with
-dQ fused, dQ conversion). Prints ONE JSON line (rank 0).
+One step = attn_fwd followed by attn_bwd over one batch of the workload, through the
+C ABI (at d <= 64 the backward is the dQ kernel, which also forms D, then dK/dV; at
+d = 128 D, dK/dV, dQ; with --fused-dq, at d <= 64: D, dK/dV with dQ fused, dQ
+conversion). Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -10,11 +11,12 @@ dQ fused, dQ conversion). Prints ONE JSON line (rank 0).
   2.5x that), inputs resident in HBM; inputs rotate over several buffer sets whose
   total size exceeds L2 three times, so no step reads another's operands from L2.
 * e2e: the same metric through the public API with pinned host buffers: every step
-  copies Q, K, V, dO host->device and O, LSE, dQ, dK, dV device->host.
+  copies Q, K, V, dO host->device and O, LSE, dQ, dK, dV device->host; steps are
+  pipelined over two device buffer sets and three streams, as a caller would run them.
 * roofline: the kernel with the largest share of step time, its algorithmic FLOPs
   per launch over its mean CUDA-event duration, against the measured bf16 peak.
-* cpu_baseline: the CPU oracle timed on this host on a bounded sample (a few heads
-  of the same workload), as it stands.
+* cpu_baseline: the CPU oracle timed on this host on a bounded sample (whole heads of
+  the same workload until about 10 s of work), as it stands.
 * --impl reference: the CPU oracle as the reference arm (the pages publish no code
   that runs here), each step a bounded sample of the workload.
 
@@ -115,8 +117,9 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def oracle_sample(w, n_heads, x=None):
-    """Runs the CPU oracle fwd + bwd on n_heads heads; returns (credited FLOPs, seconds)."""
+def oracle_sample(w, n_heads, x=None, budget_s=None):
+    """Runs the CPU oracle fwd + bwd on up to n_heads heads (stopping once budget_s seconds
+    have passed, after at least one head); returns (credited FLOPs, seconds, heads run)."""
     import numpy as np  # noqa: F401
     import oracle
     import seeded_inputs as si
@@ -124,12 +127,16 @@ def oracle_sample(w, n_heads, x=None):
     heads = [(i // w.H % w.B, i % w.H) for i in range(n_heads)]
     q, k, v, do = (si.bf16_bits_to_f64(x[n]) for n in ("q", "k", "v", "do"))
     t0 = time.perf_counter()
+    done = 0
     for b, h in heads:
         oracle.head_forward(q[b, h], k[b, h], v[b, h], w.scale, w.causal)
         oracle.head_backward(q[b, h], k[b, h], v[b, h], do[b, h], w.scale, w.causal)
+        done += 1
+        if budget_s is not None and time.perf_counter() - t0 >= budget_s:
+            break
     dt = time.perf_counter() - t0
     fwd, bwd = oracle.credited_flops(1, 1, w.T, w.d)
-    return (fwd + bwd) * n_heads, dt
+    return (fwd + bwd) * (1.0 if w.causal else 2.0) * done, dt, done
 
 
 def blas_threads():
@@ -154,7 +161,7 @@ def run_reference(args, rank, world):
         oracle_sample(w, heads_per_step, x)
     flops = secs = 0.0
     for _ in range(args.steps):
-        f, s = oracle_sample(w, heads_per_step, x)
+        f, s, _ = oracle_sample(w, heads_per_step, x)
         flops += f
         secs += s
     value = flops / secs / 1e12
@@ -307,33 +314,61 @@ def run_ours(args, rank, world, local):
     value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
 
     # ------------------------------------------------------------------ e2e
+    # The public API with host buffers: every step copies its inputs in from pinned host
+    # memory, runs attn_fwd + attn_bwd and copies every output back. Steps are pipelined
+    # as a user of the API would run them: two device buffer sets, three streams (copies in,
+    # compute, copies out), so one step's copies overlap its neighbours' compute.
     pinned = {n: torch.from_numpy(x[n].view("int16")).view(torch.bfloat16).pin_memory() for n in ("q", "k", "v", "do")}
-    outs_h = {n: torch.empty((B, H, T, d), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
-    outs_h["lse"] = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
-    s0 = sets[0]
+
+    def host_outs():
+        o = {n: torch.empty((B, H, T, d), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
+        o["lse"] = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
+        return o
+    e2e_sets = [sets[0], sets[1 % n_sets]]
+    outs_h = [host_outs(), host_outs()]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h[0].values())
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    used = [False, False]
 
-    def e2e_step():
-        for n in ("q", "k", "v", "do"):
-            s0[n].copy_(pinned[n], non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        sb, oh = e2e_sets[b], outs_h[b]
+        if used[b]:
+            s_in.wait_event(ev_cmp[b])  # the compute two steps back has read these inputs
+        with torch.cuda.stream(s_in):
+            for n in ("q", "k", "v", "do"):
+                sb[n].copy_(pinned[n], non_blocking=True)
+        ev_in[b].record(s_in)
+        s_cmp.wait_event(ev_in[b])
+        if used[b]:
+            s_cmp.wait_event(ev_out[b])  # the outputs two steps back have been copied out
         if fused:
-            step(s0)  # the fused-dQ stages are called one by one, as a user of them would
+            ca.attn_fwd(sb["q"], sb["k"], sb["v"], sb["o"], sb["lse"], scale, causal, s_cmp)
+            ca.attn_bwd_preprocess(sb["o"], sb["do"], sb["lse"], sb["ws"], s_cmp)
+            ca.attn_bwd_dkdv_dq(sb["q"], sb["k"], sb["v"], sb["do"], sb["dk"], sb["dv"], sb["ws"], scale, causal, s_cmp)
+            ca.attn_bwd_dq_finish(sb["dq"], sb["ws"], scale, s_cmp)
         else:
-            ca.attn_fwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["lse"], scale, causal, stream)
-            ca.attn_bwd(s0["q"], s0["k"], s0["v"], s0["o"], s0["do"], s0["lse"], s0["dq"], s0["dk"], s0["dv"],
-                        s0["ws"], scale, causal, stream)
-        for n in ("o", "lse", "dq", "dk", "dv"):
-            outs_h[n].copy_(s0[n], non_blocking=True)
+            ca.attn_fwd(sb["q"], sb["k"], sb["v"], sb["o"], sb["lse"], scale, causal, s_cmp)
+            ca.attn_bwd(sb["q"], sb["k"], sb["v"], sb["o"], sb["do"], sb["lse"], sb["dq"], sb["dk"], sb["dv"],
+                        sb["ws"], scale, causal, s_cmp)
+        ev_cmp[b].record(s_cmp)
+        s_out.wait_event(ev_cmp[b])
+        with torch.cuda.stream(s_out):
+            for n in ("o", "lse", "dq", "dk", "dv"):
+                oh[n].copy_(sb[n], non_blocking=True)
+        ev_out[b].record(s_out)
+        used[b] = True
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    for i in range(args.e2e_steps):
+        e2e_step(i)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
     if world > 1:
@@ -372,8 +407,8 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n_heads = 2 if T >= 4096 else (4 if T >= 2048 else 16)
-        f, s = oracle_sample(wr, n_heads, x)
+        # a bounded sample: whole heads until about 10 s of CPU work
+        f, s, n_heads = oracle_sample(wr, B * H, x, budget_s=10.0)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{n_heads} of {B * H} heads, fwd+bwd, fp64 numpy oracle, {s:.1f} s"}
 
