@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--non-causal", action="store_true",
+                    help="the workload's shapes without the causal mask (credited FLOPs doubled)")
     ap.add_argument("--fused-dq", action="store_true",
                     help="time the fused-dQ backward stages (d <= 64) instead of attn_bwd's kernels")
     return ap.parse_args()
@@ -153,6 +155,8 @@ def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step a bounded sample (one head)."""
     import seeded_inputs as si
     w = si.WORKLOADS[args.workload]
+    if args.non_causal:
+        w = w.with_(causal=False)
     if rank != 0:
         return
     x = si.make_inputs(w)
@@ -229,6 +233,8 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = si.WORKLOADS[args.workload]
+    if args.non_causal:
+        w = w.with_(causal=False)
     # each rank: its own replica of the workload (different seed, same shape)
     wr = w.with_(seed=w.seed + 1000 * rank)
     x = si.make_inputs(wr)
