@@ -6,5 +6,6 @@ from .attention import (  # noqa: F401
     forward,
     head_backward,
     head_forward,
+    kv_head,
     preprocess_D,
 )

@@ -30,6 +30,11 @@ Readings where the pages leave a step open:
 * The O that feeds D is the oracle's own fp64 O.
 * Masked entries are excluded (exp of -inf = 0); with causal masking every row sees
   at least its own key, so no row is fully masked.
+* Grouped key/value heads (GQA / MQA): K and V may have H_kv heads with H_kv dividing
+  H; query head h attends with key/value head h // (H / H_kv), the index mapping of
+  Forge RESEARCH.md section 6 ("kv_head = q_head / (n_heads / n_kv_heads)", no repeated
+  copies). A key/value head's dK and dV are the sums of the contributions of the
+  query heads that use it (each contribution is the single-head backward above).
 """
 from __future__ import annotations
 
@@ -91,30 +96,53 @@ def _heads(B, H, heads):
     return list(heads)
 
 
-def forward(q, k, v, scale, causal=True, dtype=np.float64, heads=None):
-    """q, k, v: [B, H, T, d]. Returns O [B, H, T, d] and L [B, H, T].
+def kv_head(h, H, H_kv):
+    """The key/value head that query head h uses (RESEARCH.md's GQA mapping)."""
+    if H % H_kv:
+        raise ValueError("the number of key/value heads must divide the number of query heads")
+    return h // (H // H_kv)
 
-    With ``heads`` (a list of (b, h)) only those heads are computed; the other
+
+def forward(q, k, v, scale, causal=True, dtype=np.float64, heads=None):
+    """q: [B, H, T, d]; k, v: [B, H_kv, T, d] (H_kv = H, or a divisor of H for grouped
+    key/value heads). Returns O [B, H, T, d] and L [B, H, T].
+
+    With ``heads`` (a list of (b, h)) only those query heads are computed; the other
     entries of the outputs are NaN.
     """
     B, H, T, d = q.shape
+    H_kv = k.shape[1]
     o = np.full((B, H, T, d), np.nan, dtype=dtype)
     lse = np.full((B, H, T), np.nan, dtype=dtype)
     for b, h in _heads(B, H, heads):
-        o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, h], v[b, h], scale, causal, dtype)
+        g = kv_head(h, H, H_kv)
+        o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, g], v[b, g], scale, causal, dtype)
     return o, lse
 
 
 def backward(q, k, v, do, scale, causal=True, dtype=np.float64, heads=None):
-    """Returns dQ, dK, dV [B, H, T, d] and D [B, H, T] (NaN outside ``heads``)."""
+    """Returns dQ [B, H, T, d], dK, dV [B, H_kv, T, d] and D [B, H, T].
+
+    dK and dV of a key/value head sum the contributions of its query heads. With
+    ``heads`` (query heads), dQ and D are NaN outside them, and dK / dV are NaN for every
+    key/value head whose query heads are not all included.
+    """
     B, H, T, d = q.shape
+    H_kv = k.shape[1]
     dq = np.full((B, H, T, d), np.nan, dtype=dtype)
-    dk = np.full_like(dq, np.nan)
-    dv = np.full_like(dq, np.nan)
     D = np.full((B, H, T), np.nan, dtype=dtype)
+    dk = np.zeros((B, H_kv, T, d), dtype=dtype)
+    dv = np.zeros_like(dk)
+    seen = np.zeros((B, H_kv), dtype=np.int64)
     for b, h in _heads(B, H, heads):
-        dq[b, h], dk[b, h], dv[b, h], D[b, h] = head_backward(
-            q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, dtype)
+        g = kv_head(h, H, H_kv)
+        dq[b, h], dk_h, dv_h, D[b, h] = head_backward(q[b, h], k[b, g], v[b, g], do[b, h], scale, causal, dtype)
+        dk[b, g] += dk_h
+        dv[b, g] += dv_h
+        seen[b, g] += 1
+    incomplete = seen != H // H_kv
+    dk[incomplete] = np.nan
+    dv[incomplete] = np.nan
     return dq, dk, dv, D
 
 

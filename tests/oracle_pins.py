@@ -236,6 +236,54 @@ def check_fp32_instantiation(orc, w, tol=1e-4, heads=None):
         assert err <= tol, f"fp32 vs fp64 {name}: {err:.3e}"
 
 
+def check_gqa_finite_differences(orc, B=1, H=4, H_kv=2, T=10, d=4, seed=301, causal=True, tol=1e-6):
+    """Grouped key/value heads: central differences of L = sum(dO * O) w.r.t. every
+    element of the shared K and V (each feeds H / H_kv query heads) and of Q, against
+    the backward's dK, dV (sums over the group) and dQ."""
+    q = _rand(seed, (B, H, T, d))
+    k, v = _rand(seed + 1, (B, H_kv, T, d)), _rand(seed + 2, (B, H_kv, T, d))
+    do = _rand(seed + 3, (B, H, T, d))
+    scale = 1.0 / math.sqrt(d)
+    dq, dk, dv, _ = orc.backward(q, k, v, do, scale, causal)
+
+    def loss():
+        o, _ = orc.forward(q, k, v, scale, causal)
+        return float(np.sum(do * o))
+
+    for name, x, g in (("Q", q, dq), ("K", k, dk), ("V", v, dv)):
+        flat, fd = x.reshape(-1), np.zeros(x.size)
+        for n in range(flat.size):
+            x0 = flat[n]
+            h = 1e-6 * max(1.0, abs(x0))
+            flat[n] = x0 + h
+            lp = loss()
+            flat[n] = x0 - h
+            lm = loss()
+            flat[n] = x0
+            fd[n] = (lp - lm) / (2 * h)
+        rel = np.linalg.norm(g.reshape(-1) - fd) / max(np.linalg.norm(fd), 1e-300)
+        assert rel <= tol, f"GQA finite differences d{name}: rel {rel:.3e}"
+
+
+def check_gqa_against_torch_sdpa(orc, B=1, H=6, H_kv=2, T=24, d=8, seed=311, causal=True):
+    """torch scaled_dot_product_attention with enable_gqa (query head h reads key/value
+    head h // (H / H_kv)), float64 on the CPU, with autograd."""
+    import torch
+    q = _rand(seed, (B, H, T, d))
+    k, v = _rand(seed + 1, (B, H_kv, T, d)), _rand(seed + 2, (B, H_kv, T, d))
+    do = _rand(seed + 3, (B, H, T, d))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = orc.forward(q, k, v, scale, causal)
+    dq, dk, dv, _ = orc.backward(q, k, v, do, scale, causal)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale,
+                                                          enable_gqa=True)
+    to.backward(torch.tensor(do))
+    for name, a, b in (("O", o, to.detach()), ("dQ", dq, tq.grad), ("dK", dk, tk.grad), ("dV", dv, tv.grad)):
+        err = float(np.max(np.abs(a - b.numpy())))
+        assert err <= 1e-12, f"torch sdpa (GQA) {name}: {err}"
+
+
 ALL_FAST_CHECKS = (
     check_brute_force,
     check_finite_differences,
@@ -246,4 +294,6 @@ ALL_FAST_CHECKS = (
     check_first_row,
     check_gradient_sums,
     check_accumulator_cell,
+    check_gqa_finite_differences,
+    check_gqa_against_torch_sdpa,
 )

@@ -118,6 +118,28 @@ def test_flop_convention_matches_pages():
         assert bwd == 2.5 * fwd
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_gqa_finite_differences(causal):
+    pins.check_gqa_finite_differences(oracle, causal=causal)
+
+
+@pytest.mark.parametrize("H,H_kv", [(6, 2), (4, 1), (3, 3)])
+def test_gqa_against_torch_sdpa(H, H_kv):
+    pins.check_gqa_against_torch_sdpa(oracle, H=H, H_kv=H_kv)
+
+
+def test_gqa_heads_subset():
+    """dK / dV of a key/value head are NaN unless all its query heads are computed."""
+    q = np.random.default_rng(5).standard_normal((1, 4, 8, 4))
+    k = np.random.default_rng(6).standard_normal((1, 2, 8, 4))
+    do = np.random.default_rng(7).standard_normal((1, 4, 8, 4))
+    full = oracle.backward(q, k, k, do, 0.5)
+    part = oracle.backward(q, k, k, do, 0.5, heads=[(0, 0), (0, 1), (0, 2)])
+    assert np.array_equal(part[1][0, 0], full[1][0, 0]) and np.isnan(part[1][0, 1]).all()
+    with pytest.raises(ValueError):
+        oracle.forward(q, k[:, :1].repeat(3, axis=1), k[:, :1].repeat(3, axis=1), 0.5)
+
+
 def test_heads_subset_matches_full():
     w = si.WORKLOADS["gpt12m"].with_(B=2, H=3, T=40)
     x = si.make_inputs(w)
@@ -151,6 +173,9 @@ MUTATIONS = {
                                 "p = np.exp(s - m[:, None])  # softmax"),
     "D over the wrong axis": ("D = (do * np.asarray(o, dtype=dtype)).sum(axis=1)",
                               "D = (do * np.asarray(o, dtype=dtype)).sum(axis=1) * 0.5"),
+    "GQA head mapping modulo": ("return h // (H // H_kv)", "return h % H_kv"),
+    "GQA dK not summed over the group": ("dk[b, g] += dk_h", "dk[b, g] = dk_h"),
+    "GQA dV not summed over the group": ("dv[b, g] += dv_h", "dv[b, g] = dv_h"),
 }
 
 
