@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="grouped key/value heads: H_kv (dividing H); the step is attn_fwd + attn_bwd timed whole")
     ap.add_argument("--non-causal", action="store_true",
                     help="the workload's shapes without the causal mask (credited FLOPs doubled)")
     ap.add_argument("--fused-dq", action="store_true",
@@ -213,7 +215,8 @@ def captured_traffic(workload, kernel):
 def kernel_flops(w):
     """Algorithmic FLOPs per launch of each kernel (causal half of every T x T GEMM)."""
     g = w.B * w.H * w.T * w.T * w.d * (1.0 if w.causal else 2.0)  # one causal GEMM = B*H*T^2*d
-    return {"fwd": 2 * g, "bwd_dkdv": 4 * g, "bwd_dq": 3 * g, "bwd_dkdv_dq": 5 * g}
+    # "bwd": the whole attn_bwd (dQ kernel with its two recomputed GEMMs + dK/dV kernel)
+    return {"fwd": 2 * g, "bwd_dkdv": 4 * g, "bwd_dq": 3 * g, "bwd_dkdv_dq": 5 * g, "bwd": 7 * g}
 
 
 def kernel_bytes(w):
@@ -242,18 +245,25 @@ def run_ours(args, rank, world, local):
     scale, causal = wr.scale, wr.causal
     dev = torch.device("cuda", local)
 
-    KERNELS = kernels_for(d, args.fused_dq)
+    H_kv = args.kv_heads or H
+    if H % H_kv:
+        raise SystemExit(f"--kv-heads {H_kv} does not divide H = {H}")
+    gqa = H_kv != H
+    KERNELS = ("fwd", "bwd") if gqa else kernels_for(d, args.fused_dq)
     fused = "bwd_dkdv_dq" in KERNELS
     ws_bytes = (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d)
     per_set = 8 * B * H * T * d * 2 + B * H * T * 4 + ws_bytes
     n_sets = max(2, -(-3 * L2_BYTES // per_set))
+    if gqa:  # key/value heads: the seeded bytes of the first H_kv heads
+        import numpy as np
+        x = dict(x, k=np.ascontiguousarray(x["k"][:, :H_kv]), v=np.ascontiguousarray(x["v"][:, :H_kv]))
     base = {n: to_device(x[n]) for n in ("q", "k", "v", "do")}
     sets = []
     for i in range(n_sets):
         s = {n: base[n].clone() for n in base}
         s["o"] = torch.empty_like(s["q"])
         s["lse"] = torch.empty((B, H, T), dtype=torch.float32, device=dev)
-        s["dq"], s["dk"], s["dv"] = (torch.empty_like(s["q"]) for _ in range(3))
+        s["dq"], s["dk"], s["dv"] = torch.empty_like(s["q"]), torch.empty_like(s["k"]), torch.empty_like(s["v"])
         s["ws"] = ca.new_workspace(B, H, T, d, dev, fused_dq=fused)
         sets.append(s)
     stream = torch.cuda.current_stream()
@@ -268,6 +278,8 @@ def run_ours(args, rank, world, local):
         "bwd_dkdv_dq": lambda s: ca.attn_bwd_dkdv_dq(s["q"], s["k"], s["v"], s["do"], s["dk"], s["dv"], s["ws"],
                                                      scale, causal, stream),
         "bwd_dq_finish": lambda s: ca.attn_bwd_dq_finish(s["dq"], s["ws"], scale, stream),
+        "bwd": lambda s: ca.attn_bwd(s["q"], s["k"], s["v"], s["o"], s["do"], s["lse"], s["dq"], s["dk"], s["dv"],
+                                     s["ws"], scale, causal, stream),
     }
 
     def step(s, ev=None):
@@ -327,7 +339,8 @@ def run_ours(args, rank, world, local):
     pinned = {n: torch.from_numpy(x[n].view("int16")).view(torch.bfloat16).pin_memory() for n in ("q", "k", "v", "do")}
 
     def host_outs():
-        o = {n: torch.empty((B, H, T, d), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
+        o = {n: torch.empty((B, H, T, d), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq")}
+        o.update({n: torch.empty((B, H_kv, T, d), dtype=torch.bfloat16).pin_memory() for n in ("dk", "dv")})
         o["lse"] = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
         return o
     e2e_sets = [sets[0], sets[1 % n_sets]]
@@ -423,7 +436,7 @@ def run_ours(args, rank, world, local):
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wr.name, "B": B, "H": H, "T": T, "d": d, "causal": causal,
+        "config": {"workload": wr.name, "B": B, "H": H, "H_kv": H_kv, "T": T, "d": d, "causal": causal,
                    "parallelism": f"replicas x{world}", "l2": f"inputs rotate over {n_sets} sets ({n_sets * per_set / 2**20:.0f} MiB > L2)"},
         "frac_of_peak": round(value / peak_tf, 4),
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
@@ -432,7 +445,7 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": len(KERNELS) * args.steps,
+        "gpu_launches": (1 + (2 if d <= 64 else 3) if gqa else len(KERNELS)) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

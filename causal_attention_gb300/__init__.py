@@ -60,26 +60,41 @@ def attn_bwd_workspace_size(B, H, T, d) -> int:
     return int(_dll.attn_bwd_workspace_size(B, H, T, d))
 
 
-def attn_fwd(q, k, v, o, lse, scale, causal=True, stream=None):
-    """O = softmax(Q K^T * scale [causal]) V and the natural-log LSE, in place."""
+def _kv_heads(q, *kv):
+    """H_kv of k / v tensors [B, H_kv, T, d] that go with q [B, H, T, d]."""
     B, H, T, d = _shape(q)
+    H_kv = _shape(kv[0])[1]
+    for t in kv:
+        if _shape(t) != (B, H_kv, T, d):
+            raise ValueError(f"key/value tensors must be [B, H_kv, T, d] = {(B, H_kv, T, d)}, got {tuple(t.shape)}")
+    return H_kv
+
+
+def attn_fwd(q, k, v, o, lse, scale, causal=True, stream=None):
+    """O = softmax(Q K^T * scale [causal]) V and the natural-log LSE, in place. k and v
+    may have fewer heads than q (grouped key/value heads: query head h reads key/value
+    head h // (H / H_kv))."""
+    B, H, T, d = _shape(q)
+    H_kv = _kv_heads(q, k, v)
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
         _need(t, n, torch.bfloat16)
     _need(lse, "lse", torch.float32)
-    _check(_dll.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, T, d,
-                         ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_fwd")
+    _check(_dll.attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, T, d,
+                             ctypes.c_float(scale), int(causal), _stream_handle(stream)), "attn_fwd_gqa")
 
 
 def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal=True, stream=None):
-    """dQ, dK, dV in place (three kernels: preprocess, dK/dV, dQ)."""
+    """dQ, dK, dV in place. k, v, dk, dv may have fewer heads than q (grouped key/value
+    heads; dK / dV then sum over each key/value head's query heads)."""
     B, H, T, d = _shape(q)
+    H_kv = _kv_heads(q, k, v, dk, dv)
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
         _need(t, n, torch.bfloat16)
     _need(lse, "lse", torch.float32)
-    _check(_dll.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                         _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                         B, H, T, d, ctypes.c_float(scale), int(causal), _stream_handle(stream)),
-           "attn_bwd")
+    _check(_dll.attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             B, H, H_kv, T, d, ctypes.c_float(scale), int(causal), _stream_handle(stream)),
+           "attn_bwd_gqa")
 
 
 def attn_bwd_preprocess(o, do, lse, workspace, stream=None):

@@ -138,6 +138,12 @@ attn_status check_shape(int B, int H, int T, int d) {
   return ATTN_OK;
 }
 
+// Grouped key/value heads: 1 <= H_kv <= H and H_kv divides H.
+attn_status check_kv_heads(int H, int H_kv) {
+  if (H_kv < 1 || H_kv > H || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
 attn_status check_scale(float scale, int causal) {
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
@@ -188,6 +194,7 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   a->T = T;
   a->T_pad = pad_rows(T);
   a->BH = B * H;
+  a->G = 1;  // attn_bwd_gqa sets the group size
   a->d = d;
   a->causal = causal;
   a->scale = scale;
@@ -203,7 +210,7 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   if (a->num_sms <= 0) return cuda_fail(e, ATTN_ERR_CUDA);
   if (need_maps) {
     ATTN_TRY(make_map(&maps[0], q, a->BH, T, d));
-    ATTN_TRY(make_map(&maps[1], k, a->BH, T, d));
+    ATTN_TRY(make_map(&maps[1], k, a->BH, T, d));  // remade over B * H_kv slices for grouped heads
     ATTN_TRY(make_map(&maps[2], v, a->BH, T, d));
     ATTN_TRY(make_map(&maps[3], dO, a->BH, T, d));
     a->tmQ = &maps[0];
@@ -217,8 +224,8 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
 // dK and dV as tensor maps, for the d <= 64 dK/dV kernel's TMA-store epilogue.
 attn_status bwd_map_dkdv(BwdArgs* a, const void* dk, const void* dv, CUtensorMap* maps) {
   if (a->d > 64) return ATTN_OK;
-  ATTN_TRY(make_map(&maps[0], dk, a->BH, a->T, a->d));
-  ATTN_TRY(make_map(&maps[1], dv, a->BH, a->T, a->d));
+  ATTN_TRY(make_map(&maps[0], dk, a->BH / a->G, a->T, a->d));  // dK, dV: one per key/value slice
+  ATTN_TRY(make_map(&maps[1], dv, a->BH / a->G, a->T, a->d));
   a->tmdK = &maps[0];
   a->tmdV = &maps[1];
   return ATTN_OK;
@@ -292,15 +299,22 @@ int attn_abi_version(void) { return ATTN_ABI_VERSION; }
 
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int T, int d, float scale, int causal, void* stream) {
+  return attn_fwd_gqa(q, k, v, o, lse, B, H, H, T, d, scale, causal, stream);
+}
+
+attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int H_kv, int T, int d, float scale, int causal, void* stream) {
   ATTN_TRY(check_shape(B, H, T, d));
+  ATTN_TRY(check_kv_heads(H, H_kv));
   ATTN_TRY(check_scale(scale, causal));
   ATTN_TRY(check_ptrs({q, k, v, o, lse}));
   CUtensorMap maps[3];
   FwdArgs a;
   a.BH = B * H;
+  a.G = H / H_kv;
   ATTN_TRY(make_map(&maps[0], q, a.BH, T, d));
-  ATTN_TRY(make_map(&maps[1], k, a.BH, T, d));
-  ATTN_TRY(make_map(&maps[2], v, a.BH, T, d));
+  ATTN_TRY(make_map(&maps[1], k, B * H_kv, T, d));
+  ATTN_TRY(make_map(&maps[2], v, B * H_kv, T, d));
   a.tmQ = &maps[0];
   a.tmK = &maps[1];
   a.tmV = &maps[2];
@@ -409,13 +423,25 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, void* dq, void* dk, void* dv, void* workspace,
                      size_t workspace_bytes, int B, int H, int T, int d, float scale, int causal,
                      void* stream) {
+  return attn_bwd_gqa(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H, T, d, scale, causal,
+                      stream);
+}
+
+attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                         size_t workspace_bytes, int B, int H, int H_kv, int T, int d, float scale,
+                         int causal, void* stream) {
   ATTN_TRY(check_shape(B, H, T, d));
+  ATTN_TRY(check_kv_heads(H, H_kv));
   ATTN_TRY(check_scale(scale, causal));
   ATTN_TRY(check_ptrs({q, k, v, o, dO, lse, dq, dk, dv}));
   ATTN_TRY(check_workspace(workspace, workspace_bytes, B, H, T));
   BwdArgs a;
   CUtensorMap maps[7];
   ATTN_TRY(bwd_args(&a, q, k, v, dO, workspace, B, H, T, d, scale, causal, maps, true));
+  a.G = H / H_kv;
+  ATTN_TRY(make_map(&maps[1], k, B * H_kv, T, d));  // K, V: one slice per key/value head
+  ATTN_TRY(make_map(&maps[2], v, B * H_kv, T, d));
   ATTN_TRY(bwd_map_o(&a, o, &maps[4]));
   ATTN_TRY(bwd_map_dkdv(&a, dk, dv, &maps[5]));
   a.o = static_cast<const __nv_bfloat16*>(o);

@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                          const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
                          __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dq_acc,
-                         int* __restrict__ dq_cnt, int T, int T_pad, int BH, float scale, float scale_log2,
-                         uint32_t* __restrict__ err) {
+                         int* __restrict__ dq_cnt, int T, int T_pad, int BH, int G, float scale,
+                         float scale_log2, uint32_t* __restrict__ err) {
   // persistent d <= 64: dV and dK leave through shared memory and TMA stores
   constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE;
   constexpr int NEPI = EPI ? 2 : 0;
@@ -391,10 +391,13 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_q = (T + kTileRows - 1) / kTileRows;
+  // BH counts key/value slices; each is shared by G query heads (grouped key/value heads,
+  // G = 1 without), whose query tiles all feed its dK and dV
   const Sched sched{n_q * BH};
-  // item u: key tile u / BH (small j = most work first), slice u % BH
+  // item u: key tile u / BH (small j = most work first), key/value slice u % BH;
+  // iteration it: query head kv * G + it / n_per, query tile i0 + it % n_per
   auto key_tile = [&](int u) { return u / BH; };
-  auto n_iters = [&](int u) { return n_q - (CAUSAL ? key_tile(u) : 0); };
+  auto n_iters = [&](int u) { return G * (n_q - (CAUSAL ? key_tile(u) : 0)); };
 
   constexpr int NS = C::NSLOT;
   auto sKf = [&](int slot) { return sm.base + C::OFF_FIX + slot * C::SLOT_BYTES; };  // K_j, then V_j
@@ -420,15 +423,19 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         mbar_arrive_expect_tx(sm.fix_full(slot), 2 * TL::BYTES);
         TL::load(sKf(slot), &tmK, kt * kTileRows, bh, sm.fix_full(slot));
         TL::load(sKf(slot) + TL::BYTES, &tmV, kt * kTileRows, bh, sm.fix_full(slot));
-        for (int it = 0; it < n_it; ++it, ++g) {
-          const int s = g % ST, n = g / ST, qi = i0 + it;
+        for (int it = 0, qi = i0, bq = bh * G; it < n_it; ++it, ++g) {
+          const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES + 1024);
-          TL::load(sQ(s), &tmQ, qi * kTileRows, bh, sm.st_full(s));
-          TL::load(sdO(s), &tmdO, qi * kTileRows, bh, sm.st_full(s));
-          const size_t woff = (size_t)bh * T_pad + (size_t)qi * kTileRows;
+          TL::load(sQ(s), &tmQ, qi * kTileRows, bq, sm.st_full(s));
+          TL::load(sdO(s), &tmdO, qi * kTileRows, bq, sm.st_full(s));
+          const size_t woff = (size_t)bq * T_pad + (size_t)qi * kTileRows;
           bulk_load(sL(s), ws_nlse2 + woff, 512, sm.st_full(s));
           bulk_load(sL(s) + 512, ws_D + woff, 512, sm.st_full(s));
+          if (++qi == n_q) {  // the next query head of the group
+            qi = i0;
+            ++bq;
+          }
         }
       }
       if (!ok) drain_loads(sm, fix_issued, C::NSLOT, g, ST, ab);
@@ -663,8 +670,8 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     int g = 0;
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
       const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
-      for (int it = 0; it < n_it; ++it, ++g) {
-        const int s = g % ST, qi = i0 + it;
+      for (int it = 0, qi = i0; it < n_it; ++it, ++g, qi = (qi + 1 == n_q) ? i0 : qi + 1) {
+        const int s = g % ST;
         if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
         if (!(ok = mbar_wait_warp(sm.st_full(s), (g / ST) & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
@@ -808,7 +815,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmO, const float* __restrict__ lse,
                        float* __restrict__ ws_nlse2, float* __restrict__ ws_D, __nv_bfloat16* __restrict__ dq,
-                       int T, int T_pad, int BH, float scale, float scale_log2, uint32_t* __restrict__ err) {
+                       int T, int T_pad, int BH, int G, float scale, float scale_log2, uint32_t* __restrict__ err) {
   constexpr int NFIX = PRE ? 3 : 2;
   using C = BwdCfg<D, false, NFIX>;
   using TL = Tile<D>;
@@ -856,8 +863,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES);
-          TL::load(sK(s), &tmK, it * kTileRows, bh, sm.st_full(s));
-          TL::load(sV(s), &tmV, it * kTileRows, bh, sm.st_full(s));
+          // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
+          TL::load(sK(s), &tmK, it * kTileRows, bh / G, sm.st_full(s));
+          TL::load(sV(s), &tmV, it * kTileRows, bh / G, sm.st_full(s));
         }
       }
       if (!ok) drain_loads(sm, fix_issued, C::NSLOT, g, ST, ab);
@@ -1101,14 +1109,14 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
-  const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
+  const int n_items = (a.T + kTileRows - 1) / kTileRows * (a.BH / a.G);  // key tiles x key/value slices
   // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
   const int grid = C::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
   if (EPI && (!a.tmdK || !a.tmdV)) return cudaErrorInvalidValue;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, EPI ? *a.tmdK : *a.tmQ,
                                                      EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk,
-                                                     a.dv, a.dq_acc, a.dq_cnt, a.T, a.T_pad, a.BH, a.scale,
-                                                     a.scale * kLog2e, a.err);
+                                                     a.dv, a.dq_acc, a.dq_cnt, a.T, a.T_pad, a.BH / a.G, a.G,
+                                                     a.scale, a.scale * kLog2e, a.err);
   return cudaGetLastError();
 }
 
@@ -1135,7 +1143,7 @@ cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
   kern<<<min(n_items, a.num_sms), kBwdThreads, C::SMEM_BYTES, stream>>>(
       *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH,
-      a.scale, a.scale * kLog2e, a.err);
+      a.G, a.scale, a.scale * kLog2e, a.err);
   return cudaGetLastError();
 }
 

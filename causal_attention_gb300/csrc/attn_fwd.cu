@@ -82,7 +82,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse_out, int T, int BH, int n_pairs, float scale,
+                    float* __restrict__ lse_out, int T, int BH, int G, int n_pairs, float scale,
                     float scale_log2, uint32_t* __restrict__ err) {
   using C = FwdCfg<D>;
   using TL = Tile<D>;
@@ -174,11 +174,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(k_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(k_full(s), TL::BYTES);
-          TL::load(sK + s * TL::BYTES, &tmK, j * kTileRows, bh, k_full(s));
+          // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
+          TL::load(sK + s * TL::BYTES, &tmK, j * kTileRows, bh / G, k_full(s));
           ++k_issued;
           if (g >= ST && !(ok = mbar_wait(v_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(v_full(s), TL::BYTES);
-          TL::load(sV + s * TL::BYTES, &tmV, j * kTileRows, bh, v_full(s));
+          TL::load(sV + s * TL::BYTES, &tmV, j * kTileRows, bh / G, v_full(s));
           ++v_issued;
         }
       }
@@ -481,7 +482,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t stream) {
   const int n_items = n_pairs * a.BH;
   // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
   const int grid = C::SEP_P ? min(n_items, a.num_sms) : n_items;
-  kern<<<grid, kFwdThreads, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.o, a.lse, a.T, a.BH, n_pairs,
+  kern<<<grid, kFwdThreads, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.o, a.lse, a.T, a.BH, a.G, n_pairs,
                                                       a.scale, a.scale * 1.4426950408889634f, a.err);
   return cudaGetLastError();
 }

@@ -15,6 +15,7 @@ struct FwdArgs {
   __nv_bfloat16* o;
   float* lse;
   int T, BH, d, causal;
+  int G;          // query heads per key/value head (grouped key/value heads; 1 without)
   float scale;
   uint32_t* err;  // device error word
   int num_sms;    // streaming multiprocessors of the device (persistent grids)
@@ -42,7 +43,8 @@ struct BwdArgs {
   float* ws_D;
   float* dq_acc;  // fused dQ only, else null
   int* dq_cnt;    // fused dQ only, else null
-  int T, T_pad, BH, d, causal;
+  int T, T_pad, BH, d, causal;  // BH = B * H query slices
+  int G;                         // query heads per key/value head (1 without grouping)
   float scale;
   uint32_t* err;  // device error word
   int num_sms;    // streaming multiprocessors of the device (persistent grids)

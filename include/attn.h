@@ -67,6 +67,17 @@ int attn_abi_version(void);
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int T, int d, float scale, int causal, void* stream);
 
+/*
+ * Forward with grouped key/value heads (GQA; MQA when H_kv = 1). Cited mapping: Forge
+ * RESEARCH.md section 6, "kv_head = q_head / (n_heads / n_kv_heads)": query head h reads
+ * key/value head h / (H / H_kv), with no repeated copies of K and V.
+ *   q, o : bf16 [B, H, T, d];  k, v : bf16 [B, H_kv, T, d];  lse : fp32 [B, H, T]
+ *   H_kv : 1 <= H_kv <= H, dividing H (ATTN_ERR_INVALID_ARG otherwise)
+ * attn_fwd(...) is attn_fwd_gqa(..., H_kv = H, ...). One kernel launch.
+ */
+attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int H_kv, int T, int d, float scale, int causal, void* stream);
+
 /* Bytes of device workspace attn_bwd (and its stages) need: two fp32 arrays of
  * B*H*T_pad entries, T_pad = T rounded up to a multiple of 128. 0 if the sizes
  * are invalid. */
@@ -95,6 +106,21 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, void* dq, void* dk, void* dv, void* workspace,
                      size_t workspace_bytes, int B, int H, int T, int d, float scale, int causal,
                      void* stream);
+
+/*
+ * Backward with grouped key/value heads (the mapping of attn_fwd_gqa). dK and dV of a
+ * key/value head are the sums over its H / H_kv query heads, accumulated inside the
+ * dK/dV kernel (one CTA per key tile of each key/value head loops over the query tiles
+ * of all of them), so the result is deterministic.
+ *   q, o, dO, dq : bf16 [B, H, T, d];  k, v, dk, dv : bf16 [B, H_kv, T, d];  lse : [B, H, T]
+ *   workspace    : >= attn_bwd_workspace_size(B, H, T, d) bytes (query heads)
+ * attn_bwd(...) is attn_bwd_gqa(..., H_kv = H, ...). The stage entry points below are
+ * for H_kv = H.
+ */
+attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                         size_t workspace_bytes, int B, int H, int H_kv, int T, int d, float scale,
+                         int causal, void* stream);
 
 /* Backward stage 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace
  * (Forge RESEARCH.md section 6, "The D term is free"). Memory-bound. With d <= 64 and a

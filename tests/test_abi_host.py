@@ -130,3 +130,12 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
         pytest.skip("a GPU is present")
     assert fwd(lib) == 7
     assert lib.attn_last_cuda_error()
+
+
+@pytest.mark.parametrize("H,H_kv,code", [(6, 4, 1), (6, 0, 1), (6, 7, 1), (6, -2, 1)])
+def test_gqa_rejects_invalid_head_counts(lib, H, H_kv, code):
+    args = [ctypes.c_void_p(P)] * 5
+    assert lib.attn_fwd_gqa(*args, 1, H, H_kv, 64, 64, ctypes.c_float(0.125), 1, ctypes.c_void_p(0)) == code
+    ws = lib.attn_bwd_workspace_size(1, H, 64, 64)
+    bargs = [ctypes.c_void_p(P)] * 10
+    assert lib.attn_bwd_gqa(*bargs, ws, 1, H, H_kv, 64, 64, ctypes.c_float(0.125), 1, ctypes.c_void_p(0)) == code

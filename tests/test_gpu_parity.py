@@ -266,3 +266,37 @@ def test_persistent_stress_many_items_per_cta(d):
         ca.check_device_error()
         for name, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items():
             assert torch.equal(t, first[name]), name
+
+
+GQA = [
+    # (B, H, H_kv, T, d, causal)
+    (2, 6, 2, 300, 64, True), (1, 8, 1, 257, 64, True), (2, 4, 2, 200, 32, True),
+    (1, 4, 2, 385, 128, True), (2, 6, 3, 256, 64, False), (1, 16, 4, 1024, 64, True),
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,T,d,causal", GQA)
+def test_gqa_parity(B, H, H_kv, T, d, causal):
+    """Grouped key/value heads (MQA when H_kv = 1) against the oracle; the backward sums
+    each key/value head's query heads inside the dK/dV kernel, so repeated runs give the
+    same bits."""
+    import oracle
+    import causal_attention_gb300 as ca
+    seed = 500 + H * 10 + H_kv + d
+    bits = {"q": si.normal_bf16_bits(seed, 0, (B, H, T, d)), "k": si.normal_bf16_bits(seed, 1, (B, H_kv, T, d)),
+            "v": si.normal_bf16_bits(seed, 2, (B, H_kv, T, d)), "do": si.normal_bf16_bits(seed, 3, (B, H, T, d))}
+    scale = 1.0 / np.sqrt(d)
+    q, k, v, do = (gu.to_device(bits[n]) for n in ("q", "k", "v", "do"))
+    o, lse = ca.forward(q, k, v, scale, causal)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, causal)
+    ca.check_device_error()
+    assert dk.shape == (B, H_kv, T, d) and dv.shape == (B, H_kv, T, d)
+    qf, kf, vf, dof = (si.bf16_bits_to_f64(bits[n]) for n in ("q", "k", "v", "do"))
+    ro, rlse = oracle.forward(qf, kf, vf, scale, causal)
+    rdq, rdk, rdv, _ = oracle.backward(qf, kf, vf, dof, scale, causal)
+    err = gu.compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv))
+    print({k_: tuple(f"{e:.2e}" for e in v_) for k_, v_ in err.items()})
+    gu.assert_within_tolerance(err, f"gqa B{B} H{H} Hkv{H_kv} T{T} d{d}")
+    for _ in range(3):
+        dq2, dk2, dv2 = ca.backward(q, k, v, o, do, lse, scale, causal)
+        assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
