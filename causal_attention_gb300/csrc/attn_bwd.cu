@@ -805,6 +805,9 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
 // j (j <= i when causal). Persistent, two MMA issuers:
 //   warp 17: S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
 //   warp 18: dQ += dS_j K_j once dS_j (its own 64 TMEM columns) is written.
+// At d <= 64 the dQ accumulator has two TMEM buffers (items alternate), and the
+// elementwise warps store an item's dQ during the next item's first iteration, by when
+// its last dQ MMA has finished, instead of waiting for it at the end of the item.
 // PRE (d <= 64): the kernel also does the preprocess for its query tile, so that it runs
 // first and no separate D launch is needed: O_i is staged with Q_i and dO_i, the
 // elementwise threads form D_i = rowsum(dO_i * O_i) and -LSE_i * log2(e) themselves at the
@@ -838,6 +841,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int NS = C::NSLOT;
   // fixed tiles of slot b: Q_i, dO_i (, O_i)
   auto sQf = [&](int b) { return sm.base + C::OFF_FIX + b * C::SLOT_BYTES; };
+  // dQ accumulator buffers: [256, 256 + D) and, at d <= 64, [320 + D, 320 + 2D) after dS;
+  // buffer 1's full / free barriers are the ones the dK/dV kernel uses for dv_done / p_full
+  constexpr int NACC = D <= 64 ? 2 : 1;
+  auto acc_col = [&](int b) { return 256u + (b ? (uint32_t)D + 64u : 0u); };
+  auto acc_full_b = [&](int b) { return b ? sm.dv_done() : sm.acc_full(); };
+  auto acc_free_b = [&](int b) { return b ? sm.p_full() : sm.acc_free(); };
   auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto sV = [&](int s) { return sK(s) + TL::BYTES; };
 
@@ -908,25 +917,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer (dQ)
     if (lane == 0) {
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-      const uint32_t tDQ = tmem + 256u, tDS = tmem + 256u + (uint32_t)D;
+      const uint32_t tDS = tmem + 256u + (uint32_t)D;
       const uint64_t dKm0 = TL::desc_mnmajor0(sK(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       bool ok = true;
       int g = 0;
       for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
-        const int n_it = n_iters(u);
+        const int n_it = n_iters(u), b = r % NACC;
         for (int it = 0; it < n_it; ++it, ++g) {
           const int s = g % ST;
           if (!(ok = mbar_wait(sm.ds_full(), g & 1, ab, kErrTimeoutMma))) break;
-          if (it == 0 && r > 0 && !(ok = mbar_wait(sm.acc_free(), (r - 1) & 1, ab, kErrTimeoutMma))) break;
+          // this accumulator buffer still holds item r - NACC until its epilogue read it
+          if (it == 0 && r >= NACC && !(ok = mbar_wait(acc_free_b(b), (r / NACC - 1) & 1, ab, kErrTimeoutMma))) break;
           tc_fence_after();
           // dQ += dS K_j (M = queries, N = d, K = keys); dS has its own 64 columns
-          mma_chain_ts<TL, false>(tDQ, tDS, dKm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
+          mma_chain_ts<TL, false>(tmem + acc_col(b), tDS, dKm0 + (uint64_t)s * kStageOff, idesc_acc,
+                                  it > 0 ? 1u : 0u);
           mma_commit(sm.dk_done());  // "dQ_j done": the dS columns may be rewritten
           // S_j and dP_j (warp 17) were read out before dS_j was signalled
           mma_commit(sm.st_empty(s));
         }
-        if (ok) mma_commit(sm.acc_full());
+        if (ok) mma_commit(acc_full_b(b));
       }
       if (!ok) {
         mma_commit(sm.drain2());
@@ -944,6 +955,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
     int g = 0;
+    // the epilogue of an item: its dQ (x scale) to memory, then free its accumulator
+    auto epilogue = [&](int ri_e, int bh_e, int row_e) {
+      const int b = ri_e % NACC;
+      if (!(ok = mbar_wait_warp(acc_full_b(b), (ri_e / NACC) & 1, ab, kErrTimeoutElem))) return;
+      tc_fence_after();
+      store_acc_quarter<D>(tmem + lo + acc_col(b), dq + ((size_t)bh_e * T + row_e) * D, hc, scale, row_e < T);
+      tc_fence_before();
+      mbar_arrive(acc_free_b(b));
+    };
+    int pend_ri = -1, pend_bh = 0, pend_row = 0;  // an item whose epilogue is deferred (NACC = 2)
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
       const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
       const int row = qt * kTileRows + r;
@@ -1035,14 +1056,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(sm.ds_full());
+        if (NACC == 2 && it == 0 && pend_ri >= 0) {
+          // the previous item's dQ: its last MMA has finished while this iteration ran
+          epilogue(pend_ri, pend_bh, pend_row);
+          pend_ri = -1;
+          if (!ok) break;
+        }
       }
-      // ---- epilogue: dQ (x scale) of this query tile; then free the accumulator
-      if (!ok || !(ok = mbar_wait_warp(sm.acc_full(), ri & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-      store_acc_quarter<D>(tmem + lo + 256u, dq + ((size_t)bh * T + row) * D, hc, scale, row < T);
-      tc_fence_before();
-      mbar_arrive(sm.acc_free());
+      if (!ok) break;
+      // ---- epilogue: deferred into the next item's first iteration (two buffers), or now
+      if (NACC == 2) {
+        pend_ri = ri;
+        pend_bh = bh;
+        pend_row = row;
+      } else {
+        epilogue(ri, bh, row);
+        if (!ok) break;
+      }
     }
+    if (ok && pend_ri >= 0) epilogue(pend_ri, pend_bh, pend_row);  // the last item
   }
 
   tc_fence_before();
