@@ -251,7 +251,8 @@ def run_ours(args, rank, world, local):
     gqa = H_kv != H
     KERNELS = ("fwd", "bwd") if gqa else kernels_for(d, args.fused_dq)
     fused = "bwd_dkdv_dq" in KERNELS
-    ws_bytes = (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d)
+    ws_bytes = (ca.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) if gqa else
+                (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d))
     per_set = 8 * B * H * T * d * 2 + B * H * T * 4 + ws_bytes
     n_sets = max(2, -(-3 * L2_BYTES // per_set))
     if gqa:  # key/value heads: the seeded bytes of the first H_kv heads
@@ -264,7 +265,7 @@ def run_ours(args, rank, world, local):
         s["o"] = torch.empty_like(s["q"])
         s["lse"] = torch.empty((B, H, T), dtype=torch.float32, device=dev)
         s["dq"], s["dk"], s["dv"] = torch.empty_like(s["q"]), torch.empty_like(s["k"]), torch.empty_like(s["v"])
-        s["ws"] = ca.new_workspace(B, H, T, d, dev, fused_dq=fused)
+        s["ws"] = ca.new_workspace(B, H, T, d, dev, fused_dq=fused, kv_heads=H_kv)
         sets.append(s)
     stream = torch.cuda.current_stream()
 

@@ -159,9 +159,17 @@ def attn_bwd_fused_workspace_size(B, H, T, d) -> int:
     return int(_dll.attn_bwd_fused_workspace_size(B, H, T, d))
 
 
-def new_workspace(B, H, T, d, device=None, fused_dq=False):
-    """Device workspace for attn_bwd (or, with fused_dq, for the fused-dQ stages)."""
-    n = (attn_bwd_fused_workspace_size if fused_dq else attn_bwd_workspace_size)(B, H, T, d)
+def attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) -> int:
+    return int(_dll.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d))
+
+
+def new_workspace(B, H, T, d, device=None, fused_dq=False, kv_heads=None):
+    """Device workspace for attn_bwd (with fused_dq, for the fused-dQ stages; with kv_heads
+    fewer than H, for attn_bwd_gqa's split dK/dV)."""
+    if kv_heads is not None and kv_heads != H:
+        n = attn_bwd_gqa_workspace_size(B, H, kv_heads, T, d)
+    else:
+        n = (attn_bwd_fused_workspace_size if fused_dq else attn_bwd_workspace_size)(B, H, T, d)
     if n == 0:
         raise ValueError("invalid sizes" + (" (the fused dQ needs d <= 64)" if fused_dq else ""))
     return torch.empty(n // 4, dtype=torch.float32, device=device or "cuda")
@@ -183,7 +191,7 @@ def backward(q, k, v, o, do, lse, scale=None, causal=True, stream=None, workspac
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
-        workspace = new_workspace(B, H, T, d, q.device)
+        workspace = new_workspace(B, H, T, d, q.device, kv_heads=int(k.shape[1]))
     attn_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, stream)
     return dq, dk, dv
 

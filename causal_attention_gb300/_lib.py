@@ -37,6 +37,7 @@ SIGNATURES = {
     "attn_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_workspace_size": (_S, [_I, _I, _I, _I]),
     "attn_bwd_fused_workspace_size": (_S, [_I, _I, _I, _I]),
+    "attn_bwd_gqa_workspace_size": (_S, [_I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _P, _S, _I, _I, _I, _I, _P]),

@@ -1,5 +1,6 @@
 // C ABI of the attention library: argument checks, TMA descriptors, launches and
 // the device error word.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -170,6 +171,28 @@ size_t fused_workspace_bytes_for(int B, int H, int T, int d) {
   return workspace_bytes_for(B, H, T) + rows * (size_t)d * sizeof(float) + cnt;
 }
 
+// Grouped key/value heads with few key/value heads: when there are fewer dK/dV work items
+// (key tiles x key/value slices) than kSplitBelowItems (the SMs of a GB300), each item is
+// split over the G query heads of its slice until there are at least kMinDkdvItems of them,
+// so that the persistent kernel fills the device. Above one item per SM the fp32 partial
+// sums and their reduction cost more than the better balance gains (measured at 256 items:
+// 141.5 us split in two against 135 us unsplit). Fixed counts, not the device's, keep the
+// result the same on every device.
+constexpr int kSplitBelowItems = 152;
+constexpr int kMinDkdvItems = 304;
+int gqa_splits(int B, int H, int H_kv, int T) {
+  const int G = H / H_kv;
+  const long long items = (long long)B * H_kv * ((T + 127) / 128);
+  if (G == 1 || items >= kSplitBelowItems) return 1;
+  return (int)std::min<long long>(G, (kMinDkdvItems + items - 1) / items);
+}
+
+size_t gqa_workspace_bytes_for(int B, int H, int H_kv, int T, int d) {
+  const int S = gqa_splits(B, H, H_kv, T);
+  const size_t part = S > 1 ? 2 * (size_t)S * B * H_kv * (size_t)pad_rows(T) * d * sizeof(float) : 0;
+  return workspace_bytes_for(B, H, T) + part;
+}
+
 bool fused_dq_ok(int d, size_t workspace_bytes, int B, int H, int T) {
   return d <= 64 && workspace_bytes >= fused_workspace_bytes_for(B, H, T, d);
 }
@@ -195,6 +218,7 @@ attn_status bwd_args(BwdArgs* a, const void* q, const void* k, const void* v, co
   a->T_pad = pad_rows(T);
   a->BH = B * H;
   a->G = 1;  // attn_bwd_gqa sets the group size
+  a->S = 1;
   a->d = d;
   a->causal = causal;
   a->scale = scale;
@@ -337,6 +361,11 @@ size_t attn_bwd_workspace_size(int B, int H, int T, int d) {
   return workspace_bytes_for(B, H, T);
 }
 
+size_t attn_bwd_gqa_workspace_size(int B, int H, int H_kv, int T, int d) {
+  if (check_shape(B, H, T, d) != ATTN_OK || check_kv_heads(H, H_kv) != ATTN_OK) return 0;
+  return gqa_workspace_bytes_for(B, H, H_kv, T, d);
+}
+
 size_t attn_bwd_fused_workspace_size(int B, int H, int T, int d) {
   if (check_shape(B, H, T, d) != ATTN_OK || d > 64) return 0;
   return fused_workspace_bytes_for(B, H, T, d);
@@ -442,6 +471,12 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
   a.G = H / H_kv;
   ATTN_TRY(make_map(&maps[1], k, B * H_kv, T, d));  // K, V: one slice per key/value head
   ATTN_TRY(make_map(&maps[2], v, B * H_kv, T, d));
+  // few key/value heads: split dK/dV over the query heads when the workspace has room for
+  // the partial sums (else one work item per key tile and key/value head)
+  if (workspace_bytes >= gqa_workspace_bytes_for(B, H, H_kv, T, d)) {
+    a.S = gqa_splits(B, H, H_kv, T);
+    a.part = a.ws_D + (size_t)a.BH * a.T_pad;
+  }
   ATTN_TRY(bwd_map_o(&a, o, &maps[4]));
   ATTN_TRY(bwd_map_dkdv(&a, dk, dv, &maps[5]));
   a.o = static_cast<const __nv_bfloat16*>(o);

@@ -272,6 +272,21 @@ __device__ __forceinline__ void store_acc_quarter(uint32_t tacc, __nv_bfloat16* 
   }
 }
 
+// Epilogue of a split work item: the warpgroup hc of four stores its quarter of one
+// accumulator row (d fp32 TMEM columns from `tacc`) as fp32 to `dst_row` (a [d] row).
+template <int D>
+__device__ __forceinline__ void store_acc_quarter_f32(uint32_t tacc, float* dst_row, int hc) {
+  constexpr int QW = D / 4;  // 8, 16 or 32 columns
+  uint32_t u[QW];
+  if constexpr (QW == 32) tmem_ld32(tacc + (uint32_t)(hc * QW), u);
+  else if constexpr (QW == 16) tmem_ld16(tacc + (uint32_t)(hc * QW), u);
+  else tmem_ld8(tacc + (uint32_t)(hc * QW), u);
+  tmem_wait_ld();
+  uint4* d4 = reinterpret_cast<uint4*>(dst_row + hc * QW);
+#pragma unroll
+  for (int k = 0; k < QW / 4; ++k) d4[k] = make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+}
+
 // Epilogue through shared memory: the warpgroup hc of four converts its quarter of one
 // accumulator row (d fp32 TMEM columns from `tacc`, times `mul`) to bf16 and writes it
 // into row r of a Tile<D>-layout shared tile (the layout a TMA store of the tile reads).
@@ -365,17 +380,19 @@ __device__ __forceinline__ bool wait_turn(const int* cnt, int want, const Abort&
 // and the result is the same on every run. Items run longest (smallest j) first, so a
 // wait is only ever on an item that started no later; all CTAs of the persistent grid
 // are resident together (one per SM).
-template <int D, bool CAUSAL, bool FUSE>
+template <int D, bool CAUSAL, bool FUSE, bool SPLIT>
 __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                          const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                          const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
                          __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dq_acc,
-                         int* __restrict__ dq_cnt, int T, int T_pad, int BH, int G, float scale,
-                         float scale_log2, uint32_t* __restrict__ err) {
-  // persistent d <= 64: dV and dK leave through shared memory and TMA stores
-  constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE;
+                         int* __restrict__ dq_cnt, float* __restrict__ part, int T, int T_pad, int BH, int G,
+                         int S_, float scale, float scale_log2, uint32_t* __restrict__ err) {
+  // persistent d <= 64: dV and dK leave through shared memory and TMA stores (not when
+  // SPLIT: then each work item writes fp32 partial sums)
+  constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE && !SPLIT;
+  const int S = SPLIT ? S_ : 1;  // splits of each key/value head's query heads
   constexpr int NEPI = EPI ? 2 : 0;
   using C = BwdCfg<D, FUSE, 2, NEPI>;
   using TL = Tile<D>;
@@ -392,12 +409,20 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
 
   const int n_q = (T + kTileRows - 1) / kTileRows;
   // BH counts key/value slices; each is shared by G query heads (grouped key/value heads,
-  // G = 1 without), whose query tiles all feed its dK and dV
-  const Sched sched{n_q * BH};
-  // item u: key tile u / BH (small j = most work first), key/value slice u % BH;
-  // iteration it: query head kv * G + it / n_per, query tile i0 + it % n_per
-  auto key_tile = [&](int u) { return u / BH; };
-  auto n_iters = [&](int u) { return G * (n_q - (CAUSAL ? key_tile(u) : 0)); };
+  // G = 1 without), whose query tiles all feed its dK and dV. With S > 1 (few key/value
+  // heads) the G query heads are split over S work items, each writing fp32 partial sums
+  // that a second launch adds in split order.
+  const Sched sched{n_q * BH * S};
+  // item u: key tile u / (BH S) (small j = most work first), key/value slice
+  // (u % (BH S)) / S, split u % S over query heads [sp G / S, (sp + 1) G / S);
+  // iteration it: query head kv * G + h0 + it / n_per, query tile i0 + it % n_per
+  auto key_tile = [&](int u) { return u / (BH * S); };
+  auto kv_slice = [&](int u) { return (u % (BH * S)) / S; };
+  auto head0 = [&](int u) { return (u % S) * G / S; };
+  auto n_iters = [&](int u) {
+    return ((u % S + 1) * G / S - head0(u)) * (n_q - (CAUSAL ? key_tile(u) : 0));
+  };
+  constexpr bool epi = EPI;  // TMA-store epilogue (else plain or partial stores)
 
   constexpr int NS = C::NSLOT;
   auto sKf = [&](int slot) { return sm.base + C::OFF_FIX + slot * C::SLOT_BYTES; };  // K_j, then V_j
@@ -416,14 +441,14 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       bool ok = true;
       int g = 0, r = 0, fix_issued = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
-        const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
+        const int kt = key_tile(u), bh = kv_slice(u), i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
         const int slot = r % NS;
         if (r >= NS && !(ok = mbar_wait(sm.fix_empty(slot), (r / NS - 1) & 1, ab, kErrTimeoutLoad))) break;
         ++fix_issued;
         mbar_arrive_expect_tx(sm.fix_full(slot), 2 * TL::BYTES);
         TL::load(sKf(slot), &tmK, kt * kTileRows, bh, sm.fix_full(slot));
         TL::load(sKf(slot) + TL::BYTES, &tmV, kt * kTileRows, bh, sm.fix_full(slot));
-        for (int it = 0, qi = i0, bq = bh * G; it < n_it; ++it, ++g) {
+        for (int it = 0, qi = i0, bq = bh * G + head0(u); it < n_it; ++it, ++g) {
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES + 1024);
@@ -532,7 +557,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       auto store_epi = [&](int u_prev) {
 #pragma unroll
         for (int c = 0; c < TL::NCHUNK; ++c) {
-          const int row0 = key_tile(u_prev) * kTileRows, bh_prev = u_prev % BH;
+          const int row0 = key_tile(u_prev) * kTileRows, bh_prev = kv_slice(u_prev);
           tma_store_3d(&tmdV, sEPI + c * TL::CHUNK_BYTES, c * TL::CHUNK_ELEMS, row0, bh_prev);
           tma_store_3d(&tmdK, sEPI + TL::BYTES + c * TL::CHUNK_BYTES, c * TL::CHUNK_ELEMS, row0, bh_prev);
         }
@@ -547,7 +572,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
           if (!(ok = mbar_wait(sm.p_full(), g & 1, ab, kErrTimeoutMma))) break;
           // the accumulators still hold the previous item until its epilogue read them
           if (it == 0 && r > 0 && !(ok = mbar_wait(sm.acc_free(), (r - 1) & 1, ab, kErrTimeoutMma))) break;
-          if (EPI && it == 0 && r > 0) store_epi(u_prev);
+          if (epi && it == 0 && r > 0) store_epi(u_prev);
           tc_fence_after();
           // dV += P^T dO_i (M = keys, N = d, K = queries)
           mma_chain_ts<TL, false>(tDV, tmem + C::COL_P, dOm0 + (uint64_t)s * kStageOff, idesc_acc, it > 0 ? 1u : 0u);
@@ -582,7 +607,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         }
         if (ok) mma_commit(sm.acc_full());
         if (FUSE && ok) mma_commit(sm.fix_empty(0));  // K_j (dQ MMAs) and V_j are no longer read
-        if (EPI && ok && r > 0) {
+        if (epi && ok && r > 0) {
           // the previous item's stores have read the staging tiles: the next epilogue may
           // overwrite them
           bulk_wait_read_all();
@@ -590,7 +615,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         }
         u_prev = u;
       }
-      if (EPI && ok && u_prev >= 0) {
+      if (epi && ok && u_prev >= 0) {
         // the last item: wait for its epilogue to fill the staging tiles, store them
         if ((ok = mbar_wait(sm.acc_free(), (sched_count(sched) - 1) & 1, ab, kErrTimeoutMma))) store_epi(u_prev);
       }
@@ -607,7 +632,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       bool ok = true;
       int g = 0;
       for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
-        const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
+        const int kt = key_tile(u), bh = kv_slice(u), i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
         for (int it = 0; it < n_it; ++it, ++g) {
           const int qi = i0 + it;
           if (!(ok = mbar_wait(sm.dqs_full(), g & 1, ab, kErrTimeoutMma))) break;
@@ -669,7 +694,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     };
     int g = 0;
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
-      const int kt = key_tile(u), bh = u % BH, i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
+      const int kt = key_tile(u), bh = kv_slice(u), i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
       for (int it = 0, qi = i0; it < n_it; ++it, ++g, qi = (qi + 1 == n_q) ? i0 : qi + 1) {
         const int s = g % ST;
         if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
@@ -771,11 +796,19 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       tc_fence_after();
       const int key = kt * kTileRows + r;
       const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)D;
-      if constexpr (EPI) {
+      if constexpr (SPLIT) {
+        // fp32 partial sums of this split (unscaled), [S][key/value slice][T_pad][d] for dK
+        // then the same for dV; rows past T are written too and never read
+        const size_t off = (((size_t)(u % S) * BH + bh) * T_pad + key) * D;
+        store_acc_quarter_f32<D>(tDK, part + off, hc);
+        store_acc_quarter_f32<D>(tDV, part + (size_t)S * BH * T_pad * D + off, hc);
+        tc_fence_before();
+        mbar_arrive(sm.acc_free());
+      } else if constexpr (EPI) {
         // into the staging tiles (free once the previous item's TMA stores have read them);
         // warp 18 stores them once acc_free says every thread has written its part
         if (ri > 0 && !(ok = mbar_wait_warp(sm.epi_free(), (ri - 1) & 1, ab, kErrTimeoutElem))) break;
-        stage_acc_quarter<D>(tDV, sEPI, r, hc, 1.f);
+        stage_acc_quarter<D>(tDV, sEPI, r, hc, 1.f);  // (EPI: compile-time d <= 64)
         stage_acc_quarter<D>(tDK, sEPI + TL::BYTES, r, hc, scale);
         fence_proxy_async_smem();
         tc_fence_before();
@@ -1118,6 +1151,49 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_finish_kernel(const float* __
 }
 
 // ---------------------------------------------------------------------------
+// 5. split dK/dV (few key/value heads): dK = bf16(scale * sum_s part_K[s]), dV = bf16(
+//    sum_s part_V[s]), the splits added in order s = 0, 1, ... (deterministic)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_dkdv_reduce_kernel(const float* __restrict__ part,
+                                                                   __nv_bfloat16* __restrict__ dk,
+                                                                   __nv_bfloat16* __restrict__ dv, int T, int T_pad,
+                                                                   int BHkv, int S, float scale) {
+  constexpr int C8 = D / 8;  // 8 columns (two float4) per thread
+  const long long rows = (long long)BHkv * T;
+  const size_t plane = (size_t)BHkv * T_pad * D;  // one split's partial sums
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < rows * C8;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int c8 = (int)(idx % C8);
+    const long long rt = idx / C8;
+    const int bh = (int)(rt / T), t = (int)(rt % T);
+    const size_t off = ((size_t)bh * T_pad + t) * D + 8 * c8;
+    float ak[8] = {0, 0, 0, 0, 0, 0, 0, 0}, av[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int sp = 0; sp < S; ++sp) {
+      const float4* pk = reinterpret_cast<const float4*>(part + sp * plane + off);
+      const float4* pv = reinterpret_cast<const float4*>(part + (size_t)S * plane + sp * plane + off);
+      const float4 k0 = pk[0], k1 = pk[1], v0 = pv[0], v1 = pv[1];
+      ak[0] += k0.x; ak[1] += k0.y; ak[2] += k0.z; ak[3] += k0.w;
+      ak[4] += k1.x; ak[5] += k1.y; ak[6] += k1.z; ak[7] += k1.w;
+      av[0] += v0.x; av[1] += v0.y; av[2] += v0.z; av[3] += v0.w;
+      av[4] += v1.x; av[5] += v1.y; av[6] += v1.z; av[7] += v1.w;
+    }
+    uint4 ok4, ov4;
+    ok4.x = pack_bf16(ak[0] * scale, ak[1] * scale);
+    ok4.y = pack_bf16(ak[2] * scale, ak[3] * scale);
+    ok4.z = pack_bf16(ak[4] * scale, ak[5] * scale);
+    ok4.w = pack_bf16(ak[6] * scale, ak[7] * scale);
+    ov4.x = pack_bf16(av[0], av[1]);
+    ov4.y = pack_bf16(av[2], av[3]);
+    ov4.z = pack_bf16(av[4], av[5]);
+    ov4.w = pack_bf16(av[6], av[7]);
+    const size_t o = ((size_t)bh * T + t) * D + 8 * c8;
+    *reinterpret_cast<uint4*>(dk + o) = ok4;
+    *reinterpret_cast<uint4*>(dv + o) = ov4;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 template <int D>
@@ -1133,22 +1209,23 @@ cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool FUSE>
+template <int D, bool CAUSAL, bool FUSE, bool SPLIT = false>
 cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
-  constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE;
+  if (!SPLIT && a.S > 1) return launch_dkdv<D, CAUSAL, FUSE, true>(a, stream);
+  constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE && !SPLIT;
   using C = BwdCfg<D, FUSE, 2, EPI ? 2 : 0>;
-  auto kern = attn_bwd_dkdv_kernel<D, CAUSAL, FUSE>;
+  auto kern = attn_bwd_dkdv_kernel<D, CAUSAL, FUSE, SPLIT>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
-  const int n_items = (a.T + kTileRows - 1) / kTileRows * (a.BH / a.G);  // key tiles x key/value slices
+  const int n_items = (a.T + kTileRows - 1) / kTileRows * (a.BH / a.G) * a.S;  // key tiles x slices x splits
   // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
   const int grid = C::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
   if (EPI && (!a.tmdK || !a.tmdV)) return cudaErrorInvalidValue;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, EPI ? *a.tmdK : *a.tmQ,
                                                      EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk,
-                                                     a.dv, a.dq_acc, a.dq_cnt, a.T, a.T_pad, a.BH / a.G, a.G,
-                                                     a.scale, a.scale * kLog2e, a.err);
+                                                     a.dv, a.dq_acc, a.dq_cnt, a.part, a.T, a.T_pad, a.BH / a.G, a.G,
+                                                     a.S, a.scale, a.scale * kLog2e, a.err);
   return cudaGetLastError();
 }
 
@@ -1190,12 +1267,32 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
   }
 }
 
+template <int D>
+cudaError_t launch_dkdv_reduce(const BwdArgs& a, cudaStream_t stream) {
+  const long long total = (long long)(a.BH / a.G) * a.T * (D / 8);
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)a.num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  attn_bwd_dkdv_reduce_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.part, a.dk, a.dv, a.T, a.T_pad,
+                                                                       a.BH / a.G, a.S, a.scale);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {
+  if (a.S > 1 && !a.part) return cudaErrorInvalidValue;
+  cudaError_t e;
   switch (a.d) {
-    case 32: return a.causal ? launch_dkdv<32, true, false>(a, stream) : launch_dkdv<32, false, false>(a, stream);
-    case 64: return a.causal ? launch_dkdv<64, true, false>(a, stream) : launch_dkdv<64, false, false>(a, stream);
-    case 128: return a.causal ? launch_dkdv<128, true, false>(a, stream) : launch_dkdv<128, false, false>(a, stream);
+    case 32: e = a.causal ? launch_dkdv<32, true, false>(a, stream) : launch_dkdv<32, false, false>(a, stream); break;
+    case 64: e = a.causal ? launch_dkdv<64, true, false>(a, stream) : launch_dkdv<64, false, false>(a, stream); break;
+    case 128: e = a.causal ? launch_dkdv<128, true, false>(a, stream) : launch_dkdv<128, false, false>(a, stream); break;
     default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess || a.S <= 1) return e;
+  // split work items: add their partial sums
+  switch (a.d) {
+    case 32: return launch_dkdv_reduce<32>(a, stream);
+    case 64: return launch_dkdv_reduce<64>(a, stream);
+    default: return launch_dkdv_reduce<128>(a, stream);
   }
 }
 

@@ -45,6 +45,8 @@ struct BwdArgs {
   int* dq_cnt;    // fused dQ only, else null
   int T, T_pad, BH, d, causal;  // BH = B * H query slices
   int G;                         // query heads per key/value head (1 without grouping)
+  int S;                         // dK/dV splits of each key/value head's query heads (1: none)
+  float* part;                   // S > 1: fp32 partial dK then dV, [S][B*H/G][T_pad][d] each
   float scale;
   uint32_t* err;  // device error word
   int num_sms;    // streaming multiprocessors of the device (persistent grids)
@@ -54,7 +56,7 @@ inline int pad_rows(int T) { return (T + 127) / 128 * 128; }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream);  // + the partial-sum reduction when S > 1
 // dQ; at d <= 64 it also writes D and -LSE*log2(e) into the workspace (needs tmO, lse),
 // so it runs first and replaces the preprocess launch
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);

@@ -117,6 +117,14 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
  * attn_bwd(...) is attn_bwd_gqa(..., H_kv = H, ...). The stage entry points below are
  * for H_kv = H.
  */
+/* Bytes of device workspace for attn_bwd_gqa's fastest path: the attn_bwd workspace, plus,
+ * when the key/value heads are too few to fill the device with dK/dV work items (B * H_kv
+ * * ceil(T / 128) < 304), fp32 partial dK and dV for S splits of each key/value head's
+ * query heads (2 * S * B * H_kv * T_pad * d * 4 bytes, S = min(H / H_kv, ceil(304 / items))),
+ * which a last launch adds in split order (deterministic). With only the attn_bwd
+ * workspace, attn_bwd_gqa runs unsplit. 0 if the sizes are invalid. */
+size_t attn_bwd_gqa_workspace_size(int B, int H, int H_kv, int T, int d);
+
 attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
                          const float* lse, void* dq, void* dk, void* dv, void* workspace,
                          size_t workspace_bytes, int B, int H, int H_kv, int T, int d, float scale,

@@ -139,3 +139,19 @@ def test_gqa_rejects_invalid_head_counts(lib, H, H_kv, code):
     ws = lib.attn_bwd_workspace_size(1, H, 64, 64)
     bargs = [ctypes.c_void_p(P)] * 10
     assert lib.attn_bwd_gqa(*bargs, ws, 1, H, H_kv, 64, 64, ctypes.c_float(0.125), 1, ctypes.c_void_p(0)) == code
+
+
+def test_gqa_workspace_size(lib):
+    f = lib.attn_bwd_gqa_workspace_size
+    # at least one dK/dV work item per SM (B * H_kv * n_q >= 152): the attn_bwd workspace
+    assert f(4, 16, 16, 2048, 64) == base_ws(4, 16, 2048)
+    assert f(4, 64, 16, 2048, 64) == base_ws(4, 64, 2048)  # 4*16*16 = 1024 items
+    assert f(4, 16, 4, 2048, 64) == base_ws(4, 16, 2048)  # 256 items
+    assert f(1, 16, 4, 4864, 64) == base_ws(1, 16, 4864)  # exactly 152 items
+    # 151 items: split up to 304 items, ceil(304 / 151) = 3 splits
+    assert f(1, 16, 1, 151 * 128, 64) == base_ws(1, 16, 151 * 128) + 2 * 3 * 1 * 151 * 128 * 64 * 4
+    # MQA at B4 T2048: 64 items -> S = min(16, ceil(304 / 64)) = 5 splits of fp32 dK, dV
+    assert f(4, 16, 1, 2048, 64) == base_ws(4, 16, 2048) + 2 * 5 * 4 * 1 * 2048 * 64 * 4
+    # the split count is bounded by the group size
+    assert f(1, 2, 1, 128, 32) == base_ws(1, 2, 128) + 2 * 2 * 1 * 1 * 128 * 32 * 4
+    assert f(1, 6, 4, 128, 64) == 0 and f(1, 6, 0, 128, 64) == 0

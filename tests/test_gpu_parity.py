@@ -300,3 +300,11 @@ def test_gqa_parity(B, H, H_kv, T, d, causal):
     for _ in range(3):
         dq2, dk2, dv2 = ca.backward(q, k, v, o, do, lse, scale, causal)
         assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    # with only the attn_bwd workspace the dK/dV work items are not split over the query
+    # heads: the same dQ bits, dK / dV equal up to the order of their fp32 sums
+    base = ca.new_workspace(B, H, T, d)
+    dq3, dk3, dv3 = ca.backward(q, k, v, o, do, lse, scale, causal, workspace=base)
+    ca.check_device_error()
+    assert torch.equal(dq, dq3)
+    for a, b in ((dk, dk3), (dv, dv3)):
+        assert gu.rel_rms(gu.to_f64(a), gu.to_f64(b)) <= 2e-3
