@@ -2,7 +2,7 @@
 
 One step = attn_fwd followed by attn_bwd over one batch of the workload, through the
 C ABI (at d <= 64 the backward is the dQ kernel, which also forms D, then dK/dV; at
-d = 128 D, dK/dV, dQ; with --fused-dq, at d <= 64: D, dK/dV with dQ fused, dQ
+d = 80 and 128 D, dK/dV, dQ; with --fused-dq, at d <= 64: D, dK/dV with dQ fused, dQ
 conversion). Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
@@ -53,6 +53,8 @@ def parse():
                     help="grouped key/value heads: H_kv (dividing H); the step is attn_fwd + attn_bwd timed whole")
     ap.add_argument("--non-causal", action="store_true",
                     help="the workload's shapes without the causal mask (credited FLOPs doubled)")
+    ap.add_argument("--head-dim", type=int, default=0,
+                    help="the workload's shapes at another head dimension (32, 64, 80 or 128)")
     ap.add_argument("--fused-dq", action="store_true",
                     help="time the fused-dQ backward stages (d <= 64) instead of attn_bwd's kernels")
     return ap.parse_args()
@@ -157,8 +159,7 @@ def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step a bounded sample (one head)."""
     import seeded_inputs as si
     w = si.WORKLOADS[args.workload]
-    if args.non_causal:
-        w = w.with_(causal=False)
+    w = variant(w, args)
     if rank != 0:
         return
     x = si.make_inputs(w)
@@ -185,9 +186,18 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def variant(w, args):
+    """The workload as the flags change it (no causal mask; another head dimension)."""
+    if args.non_causal:
+        w = w.with_(causal=False)
+    if args.head_dim and args.head_dim != w.d:
+        w = w.with_(name=f"{w.name}_d{args.head_dim}", d=args.head_dim)
+    return w
+
+
 def kernels_for(d, fused_dq):
     """The launches of one step, in order: the forward, then attn_bwd's stages (d <= 64:
-    dQ, which also forms D, then dK/dV; d = 128: D, dK/dV, dQ), or with --fused-dq the
+    dQ, which also forms D, then dK/dV; d = 80, 128: D, dK/dV, dQ), or with --fused-dq the
     fused-dQ stages (D, dK/dV with dQ formed inside, dQ conversion)."""
     if fused_dq and d <= 64:
         return ("fwd", "bwd_preprocess", "bwd_dkdv_dq", "bwd_dq_finish")
@@ -235,9 +245,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = si.WORKLOADS[args.workload]
-    if args.non_causal:
-        w = w.with_(causal=False)
+    w = variant(si.WORKLOADS[args.workload], args)
     # each rank: its own replica of the workload (different seed, same shape)
     wr = w.with_(seed=w.seed + 1000 * rank)
     x = si.make_inputs(wr)
@@ -254,6 +262,10 @@ def run_ours(args, rank, world, local):
     ws_bytes = (ca.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) if gqa else
                 (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d))
     per_set = 8 * B * H * T * d * 2 + B * H * T * 4 + ws_bytes
+    # attn_bwd_gqa: 2 (d <= 64) or 3 launches, plus the sum of the split dK/dV when its
+    # workspace holds the partial sums
+    split = gqa and ws_bytes > ca.attn_bwd_workspace_size(B, H, T, d)
+    launches_per_step = 1 + (2 if d <= 64 else 3) + int(split) if gqa else len(KERNELS)
     n_sets = max(2, -(-3 * L2_BYTES // per_set))
     if gqa:  # key/value heads: the seeded bytes of the first H_kv heads
         import numpy as np
@@ -446,7 +458,7 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (1 + (2 if d <= 64 else 3) if gqa else len(KERNELS)) * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -135,7 +135,7 @@ attn_status check_shape(int B, int H, int T, int d) {
   if (B < 1 || H < 1 || T < 1) return ATTN_ERR_INVALID_ARG;
   const long long bh = (long long)B * H;
   if (bh > kMaxBH || T > kMaxT || bh * T * 128 > kMaxElems) return ATTN_ERR_INVALID_ARG;
-  if (d != 32 && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 80 && d != 128) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
@@ -539,7 +539,7 @@ const char* attn_status_string(attn_status status) {
   switch (status) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_INVALID_ARG: return "invalid argument";
-    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension (d must be 32, 64 or 128)";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension (d must be 32, 64, 80 or 128)";
     case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case ATTN_ERR_LAUNCH: return "kernel launch failed";

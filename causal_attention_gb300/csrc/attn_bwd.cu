@@ -53,8 +53,9 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
     const float* __restrict__ lse, float* __restrict__ ws_nlse2, float* __restrict__ ws_D, int* __restrict__ dq_cnt,
     int n_cnt, int T, int T_pad, int BH) {
-  constexpr int TPR = D / 8;           // threads per row, 16 bytes each
-  constexpr int RPW = 32 / TPR;        // rows per warp step
+  constexpr int NG = D / 8;                             // 16-byte granules per row
+  constexpr int TPR = (NG & (NG - 1)) == 0 ? NG : 8;    // threads per row (a power of two)
+  constexpr int RPW = 32 / TPR;                         // rows per warp step
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_cnt; i += gridDim.x * blockDim.x) dq_cnt[i] = 0;
   const int lane = threadIdx.x & 31;
   const int sub = lane % TPR;
@@ -69,8 +70,9 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
     if (in_range) {
       bh = (int)(row / T_pad);
       t = (int)(row % T_pad);
-      if (t < T) {
-        const size_t off = ((size_t)bh * T + t) * D + sub * 8;
+      // granules sub, sub + TPR, ... of the row (one each unless d = 80)
+      for (int gi = sub; in_range && t < T && gi < NG; gi += TPR) {
+        const size_t off = ((size_t)bh * T + t) * D + gi * 8;
         const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + off));
         const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + off));
         const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
 template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0>
 struct BwdCfg {
   using TL = Tile<D>;
-  static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
+  static constexpr int STAGES = (D > 64) ? 2 : (D == 64 ? 3 : 4);
   // fixed tiles of a work item (K_j, V_j for dK/dV; Q_i, dO_i for dQ), in NSLOT slots:
   // with two (persistent kernels at d <= 64) the next item's tiles load during this one
   static constexpr int NSLOT = (D <= 64 && !FUSE) ? 2 : 1;
@@ -248,7 +250,15 @@ template <int D>
 __device__ __forceinline__ void store_acc_quarter(uint32_t tacc, __nv_bfloat16* dst_row, int hc, float mul,
                                                   bool valid) {
   constexpr int QW = D / 4;  // 8, 16 or 32 columns
-  if constexpr (QW == 8) {
+  if constexpr (D % 64 != 0 && D > 32) {
+    // d = 80: five 16-column blocks; warpgroup hc takes block hc, warpgroup 0 also block 4
+    for (int b = hc; b < D / 16; b += 4) {
+      uint32_t u[16];
+      tmem_ld16(tacc + (uint32_t)(16 * b), u);
+      tmem_wait_ld();
+      if (valid) store_row16(dst_row + 16 * b, u, mul);
+    }
+  } else if constexpr (QW == 8) {
     uint32_t u[8];
     tmem_ld8(tacc + (uint32_t)(hc * QW), u);
     tmem_wait_ld();
@@ -276,15 +286,27 @@ __device__ __forceinline__ void store_acc_quarter(uint32_t tacc, __nv_bfloat16* 
 // accumulator row (d fp32 TMEM columns from `tacc`) as fp32 to `dst_row` (a [d] row).
 template <int D>
 __device__ __forceinline__ void store_acc_quarter_f32(uint32_t tacc, float* dst_row, int hc) {
-  constexpr int QW = D / 4;  // 8, 16 or 32 columns
-  uint32_t u[QW];
-  if constexpr (QW == 32) tmem_ld32(tacc + (uint32_t)(hc * QW), u);
-  else if constexpr (QW == 16) tmem_ld16(tacc + (uint32_t)(hc * QW), u);
-  else tmem_ld8(tacc + (uint32_t)(hc * QW), u);
-  tmem_wait_ld();
-  uint4* d4 = reinterpret_cast<uint4*>(dst_row + hc * QW);
+  if constexpr (D % 64 != 0 && D > 32) {
+    // d = 80: five 16-column blocks; warpgroup hc takes block hc, warpgroup 0 also block 4
+    for (int b = hc; b < D / 16; b += 4) {
+      uint32_t u[16];
+      tmem_ld16(tacc + (uint32_t)(16 * b), u);
+      tmem_wait_ld();
+      uint4* d4 = reinterpret_cast<uint4*>(dst_row + 16 * b);
 #pragma unroll
-  for (int k = 0; k < QW / 4; ++k) d4[k] = make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+      for (int k = 0; k < 4; ++k) d4[k] = make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+    }
+  } else {
+    constexpr int QW = D / 4;  // 8, 16 or 32 columns
+    uint32_t u[QW];
+    if constexpr (QW == 32) tmem_ld32(tacc + (uint32_t)(hc * QW), u);
+    else if constexpr (QW == 16) tmem_ld16(tacc + (uint32_t)(hc * QW), u);
+    else tmem_ld8(tacc + (uint32_t)(hc * QW), u);
+    tmem_wait_ld();
+    uint4* d4 = reinterpret_cast<uint4*>(dst_row + hc * QW);
+#pragma unroll
+    for (int k = 0; k < QW / 4; ++k) d4[k] = make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+  }
 }
 
 // Epilogue through shared memory: the warpgroup hc of four converts its quarter of one
@@ -470,7 +492,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-      const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
+      const uint32_t tS = tmem, tDP = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)TL::ACC_COLS;
       // K-step-0 descriptors: K_j / V_j per item (their slot), stage s adds s stages
       uint64_t dKk = 0, dVk = 0;
       const uint64_t dQk0 = TL::desc_kmajor0(sQ(0)), dQm0 = TL::desc_mnmajor0(sQ(0));
@@ -549,7 +571,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer (dV, dK)
     if (lane == 0 && SEP) {
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-      const uint32_t tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)D;
+      const uint32_t tDV = tmem + 256u, tDK = tmem + 256u + (uint32_t)TL::ACC_COLS;
       const uint64_t dQm0 = TL::desc_mnmajor0(sQ(0)), dOm0 = TL::desc_mnmajor0(sdO(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       // EPI: the previous item's dV / dK tiles, staged by the elementwise warps before they
@@ -675,6 +697,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     const uint32_t tDQ = tmem + lo + C::COL_DQ + (uint32_t)(QW * hc);
     bool ok = true;
     auto dq_readout = [&](int x) {  // moves iteration x's dQ_ij into the staging tile
+      if constexpr (FUSE) {
       if (!(ok = mbar_wait_warp(sm.dq_done(), x & 1, ab, kErrTimeoutElem))) return;
       tc_fence_after();
       uint32_t v[QW];
@@ -691,6 +714,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
                v[4 * k + 3]);
       fence_proxy_async_smem();
       mbar_arrive(sm.dqs_full());
+      }
     };
     int g = 0;
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
@@ -795,7 +819,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       if (!ok || !(ok = mbar_wait_warp(sm.acc_full(), ri & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
       const int key = kt * kTileRows + r;
-      const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)D;
+      const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)TL::ACC_COLS;
       if constexpr (SPLIT) {
         // fp32 partial sums of this split (unscaled), [S][key/value slice][T_pad][d] for dK
         // then the same for dV; rows past T are written too and never read
@@ -950,7 +974,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer (dQ)
     if (lane == 0) {
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-      const uint32_t tDS = tmem + 256u + (uint32_t)D;
+      const uint32_t tDS = tmem + 256u + (uint32_t)TL::ACC_COLS;
       const uint64_t dKm0 = TL::desc_mnmajor0(sK(0));
       constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       bool ok = true;
@@ -984,7 +1008,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = threadIdx.x & 127;
     const uint32_t lo = warp_lane_base();
     const uint32_t tSh = tmem + lo + 32u * hc, tDPh = tmem + lo + 128u + 32u * hc;
-    const uint32_t tDS = tmem + lo + 256u + (uint32_t)D + 16u * hc;
+    const uint32_t tDS = tmem + lo + 256u + (uint32_t)TL::ACC_COLS + 16u * hc;
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
     int g = 0;
@@ -1199,7 +1223,8 @@ __global__ void __launch_bounds__(256) attn_bwd_dkdv_reduce_kernel(const float* 
 template <int D>
 cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.BH * a.T_pad;
-  constexpr int rows_per_block = 256 / (D / 8);
+  constexpr int NG = D / 8;
+  constexpr int rows_per_block = 256 / ((NG & (NG - 1)) == 0 ? NG : 8);
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   const long long cap = (long long)a.num_sms * 8;  // grid-stride beyond 8 blocks per SM
   if (blocks > cap) blocks = cap;
@@ -1262,6 +1287,7 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t stream) {
   switch (a.d) {
     case 32: return launch_pre<32>(a, stream);
     case 64: return launch_pre<64>(a, stream);
+    case 80: return launch_pre<80>(a, stream);
     case 128: return launch_pre<128>(a, stream);
     default: return cudaErrorInvalidValue;
   }
@@ -1284,6 +1310,7 @@ cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {
   switch (a.d) {
     case 32: e = a.causal ? launch_dkdv<32, true, false>(a, stream) : launch_dkdv<32, false, false>(a, stream); break;
     case 64: e = a.causal ? launch_dkdv<64, true, false>(a, stream) : launch_dkdv<64, false, false>(a, stream); break;
+    case 80: e = a.causal ? launch_dkdv<80, true, false>(a, stream) : launch_dkdv<80, false, false>(a, stream); break;
     case 128: e = a.causal ? launch_dkdv<128, true, false>(a, stream) : launch_dkdv<128, false, false>(a, stream); break;
     default: return cudaErrorInvalidValue;
   }
@@ -1292,6 +1319,7 @@ cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {
   switch (a.d) {
     case 32: return launch_dkdv_reduce<32>(a, stream);
     case 64: return launch_dkdv_reduce<64>(a, stream);
+    case 80: return launch_dkdv_reduce<80>(a, stream);
     default: return launch_dkdv_reduce<128>(a, stream);
   }
 }
@@ -1318,6 +1346,7 @@ cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
   switch (a.d) {
     case 32: return a.causal ? launch_dq<32, true>(a, stream) : launch_dq<32, false>(a, stream);
     case 64: return a.causal ? launch_dq<64, true>(a, stream) : launch_dq<64, false>(a, stream);
+    case 80: return a.causal ? launch_dq<80, true>(a, stream) : launch_dq<80, false>(a, stream);
     case 128: return a.causal ? launch_dq<128, true>(a, stream) : launch_dq<128, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -12,13 +12,13 @@
 //   warps 0-3  softmax for Q0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax for Q1
 //   warp  8    TMA producer (Q per item; K_j, V_j through a STAGES-deep ring)
-//   warp  9    TMEM allocator and MMA issuer (tile 0, or both tiles at d = 128)
+//   warp  9    TMEM allocator and MMA issuer (tile 0, or both tiles at d >= 80)
 //   warp  10   MMA issuer of tile 1 (d <= 64)
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 and O1 from 256. P_q is
 // packed bf16, read by the PV MMA straight from tensor memory (A operand in TMEM):
 // at d <= 64 it has its own 64 columns (384 / 448), so S_{q,j+1} is issued as soon as
 // the softmax warps have read S_{q,j} into registers and runs while they compute;
-// at d = 128 (no free columns) P is written over S_q, S_{q,j+1} follows PV_{q,j}, and
+// at d = 80 and 128 (no free columns) P is written over S_q, S_{q,j+1} follows PV_{q,j}, and
 // the two tiles ping-pong on the tensor core. O is normalised by the sum of the
 // rounded P values (so O / l stays a convex combination of V rows whatever the
 // rounding), the logsumexp by the exact fp32 sum.
@@ -37,12 +37,12 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 template <int D>
 struct FwdCfg {
   using TL = Tile<D>;
-  static constexpr int STAGES = (D == 128) ? 2 : (D == 64 ? 3 : 4);
+  static constexpr int STAGES = (D > 64) ? 2 : (D == 64 ? 3 : 4);
   // P gets its own TMEM columns when they fit (d <= 64); then the kernel is persistent
-  // and each query tile has its own MMA issuer. At d = 128, S and O of both tiles fill
-  // all 512 columns, P is written over S and one thread issues every MMA.
+  // and each query tile has its own MMA issuer. At d = 80 and 128, S and O of both tiles
+  // leave no room for P: P is written over S and one thread issues every MMA.
   static constexpr bool SEP_P = D <= 64;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + TL::ACC_COLS;
   static constexpr uint32_t COL_P0 = SEP_P ? 384 : COL_S0, COL_P1 = SEP_P ? 448 : COL_S1;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * TL::BYTES;
@@ -428,6 +428,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
             tmem_st32(tO + 32u * cb, v);
           }
+          if constexpr (D % 32 != 0) {  // d = 80: the last 16 columns
+            uint32_t v[16];
+            tmem_ld16(tO + (uint32_t)(D - 16), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+            tmem_st16(tO + (uint32_t)(D - 16), v);
+          }
         }
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) tmem_st16(tP + 16u * cb, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * cb]));
@@ -454,6 +462,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cb);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+        }
+      }
+      if constexpr (D % 32 != 0) {  // d = 80: the last 16 columns
+        uint32_t v[16];
+        tmem_ld16(tO + (uint32_t)(D - 16), v);
+        tmem_wait_ld();
+        uint4 pkd[2];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pw[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+        if (row < T) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + (D - 16));
+          dst[0] = pkd[0];
+          dst[1] = pkd[1];
         }
       }
       if (row < T) lse_out[(size_t)bh * T + row] = (m * scale_log2 + __log2f(l)) * 0.69314718055994531f;
@@ -493,6 +516,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   switch (a.d) {
     case 32: return a.causal ? launch<32, true>(a, stream) : launch<32, false>(a, stream);
     case 64: return a.causal ? launch<64, true>(a, stream) : launch<64, false>(a, stream);
+    case 80: return a.causal ? launch<80, true>(a, stream) : launch<80, false>(a, stream);
     case 128: return a.causal ? launch<128, true>(a, stream) : launch<128, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }

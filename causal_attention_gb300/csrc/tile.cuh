@@ -5,7 +5,9 @@
 // bf16 values is split into column chunks of ROW_BYTES (128 B, or 64 B when
 // d = 32); chunk c of all 128 rows is stored contiguously ([chunk][row][elems]),
 // every chunk 1024-byte aligned so that the address-based swizzle of TMA and of
-// tcgen05 agree.
+// tcgen05 agree. At d = 80 the second chunk holds columns 64..79 and zeros (TMA fills
+// the columns past d with zeros), so the tile takes the space of a d = 128 tile; the
+// MMAs read only the first 80 columns (five K-steps, or N = 80).
 #pragma once
 #include "ptx.cuh"
 
@@ -15,12 +17,14 @@ constexpr int kTileRows = 128;  // rows per Q tile and per K/V tile
 
 template <int D>
 struct Tile {
-  static_assert(D == 32 || D == 64 || D == 128, "head dim");
+  static_assert(D == 32 || D == 64 || D == 80 || D == 128, "head dim");
   static constexpr int ROW_BYTES = (D * 2 >= 128) ? 128 : D * 2;  // swizzle width
   static constexpr int CHUNK_ELEMS = ROW_BYTES / 2;                // bf16 per chunk row
-  static constexpr int NCHUNK = D / CHUNK_ELEMS;
+  static constexpr int NCHUNK = (D + CHUNK_ELEMS - 1) / CHUNK_ELEMS;
   static constexpr int CHUNK_BYTES = kTileRows * ROW_BYTES;
-  static constexpr int BYTES = kTileRows * D * 2;
+  static constexpr int BYTES = NCHUNK * CHUNK_BYTES;  // shared-memory bytes (and TMA bytes) of a tile
+  // TMEM columns reserved for a d-column fp32 accumulator (d rounded up to 32)
+  static constexpr int ACC_COLS = (D + 31) / 32 * 32;
   static constexpr int KSTEPS_D = D / 16;  // MMA K-steps when contracting over d
 
   // Operand whose contraction dimension is d (K-major): Q or K as the A or B of

@@ -16,6 +16,9 @@
  * tensor [B, H, T, d] of bf16 (16-bit brain floats): element (b, h, t, c) is at
  * offset ((b*H + h)*T + t)*d + c. LSE is fp32 [B, H, T]. Pointers must be device
  * (or managed) memory visible to the current CUDA device and 16-byte aligned.
+ * Head dimensions: d = 32, 64, 80 or 128 (Forge RESEARCH.md section 6, the layout
+ * paragraph, lists 64, 80 and 128 as the head dimensions a fused kernel serves; 32 is
+ * the small case). Any T >= 1.
  *
  * Ownership. The caller allocates and owns every buffer, including the backward's
  * workspace. The library allocates no device memory and keeps no per-call state
@@ -44,7 +47,7 @@ extern "C" {
 typedef enum attn_status {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,     /* null pointer, B/H/T < 1, bad scale or causal flag, sizes too large */
-  ATTN_ERR_UNSUPPORTED = 2,     /* head dimension d not in {32, 64, 128} */
+  ATTN_ERR_UNSUPPORTED = 2,     /* head dimension d not in {32, 64, 80, 128} */
   ATTN_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,       /* workspace missing or smaller than attn_bwd_workspace_size() */
   ATTN_ERR_LAUNCH = 5,          /* the CUDA runtime rejected a launch (see attn_last_cuda_error) */
@@ -93,14 +96,14 @@ size_t attn_bwd_fused_workspace_size(int B, int H, int T, int d);
  * Backward. Cited definition: Forge RESEARCH.md section 6, "The D term is free"
  * and "Backward (training)"; the three-stage atomic-free structure of the Forge
  * paper's "Ecosystem survey". Equivalent to, on the same stream: at d <= 64
- * attn_bwd_dq (which also forms D) then attn_bwd_dkdv; at d = 128 attn_bwd_preprocess,
+ * attn_bwd_dq (which also forms D) then attn_bwd_dkdv; at d >= 80 attn_bwd_preprocess,
  * attn_bwd_dkdv, attn_bwd_dq.
  *   q, k, v, o, dO : bf16 [B, H, T, d] (o and lse as written by attn_fwd)
  *   lse            : fp32 [B, H, T]
  *   dq, dk, dv     : bf16 [B, H, T, d] outputs
  *   workspace      : >= attn_bwd_workspace_size(B, H, T, d) bytes of device memory,
  *                    16-byte aligned; its contents on entry do not matter
- * Two kernel launches at d <= 64, three at d = 128.
+ * Two kernel launches at d <= 64, three at d >= 80.
  */
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                      const float* lse, void* dq, void* dk, void* dv, void* workspace,
@@ -146,7 +149,7 @@ attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const voi
 
 /* Backward stage 3: dQ, one CTA per 128-query tile looping over key tiles
  * (deterministic; Forge RESEARCH.md section 6, "a dQ kernel with grid (NQ, H, B)").
- * At d = 128 it reads the workspace written by stage 1. At d <= 64 it does stage 1's
+ * At d >= 80 it reads the workspace written by stage 1. At d <= 64 it does stage 1's
  * work for its own query tile (D = rowsum(dO * O) from a staged O tile, -LSE * log2(e)
  * from lse) and writes both into the workspace, so it needs no stage 1 before it and
  * attn_bwd_dkdv may follow it; o and lse are read only at d <= 64 but are always
@@ -173,7 +176,7 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void*
  *               smaller), written by attn_bwd_preprocess just before
  *   dk, dv    : bf16 [B, H, T, d] outputs; dQ is left in the workspace for
  *               attn_bwd_dq_finish
- * d = 128 returns ATTN_ERR_UNSUPPORTED. One kernel launch.
+ * d > 64 returns ATTN_ERR_UNSUPPORTED. One kernel launch.
  */
 attn_status attn_bwd_dkdv_dq(const void* q, const void* k, const void* v, const void* dO, void* dk,
                              void* dv, void* workspace, size_t workspace_bytes, int B, int H, int T,

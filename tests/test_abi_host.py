@@ -59,6 +59,7 @@ def test_workspace_size(lib):
     assert lib.attn_bwd_workspace_size(1, 1, 128, 128) == 2 * 4 * 128
     assert lib.attn_bwd_workspace_size(0, 1, 128, 64) == 0
     assert lib.attn_bwd_workspace_size(1, 1, 128, 48) == 0
+    assert lib.attn_bwd_workspace_size(1, 1, 128, 80) == 2 * 4 * 128  # d = 80 is served
 
 
 def test_fused_workspace_size(lib):
@@ -68,7 +69,7 @@ def test_fused_workspace_size(lib):
     assert f(2, 3, 200, 64) == base_ws(2, 3, 200) + 6 * 256 * 64 * 4 + 256
     assert f(1, 2, 1, 32) == base_ws(1, 2, 1) + 2 * 128 * 32 * 4 + 256
     assert f(4, 64, 1024, 64) == base_ws(4, 64, 1024) + 256 * 1024 * 64 * 4 + 8192
-    assert f(1, 1, 128, 128) == 0
+    assert f(1, 1, 128, 128) == 0 and f(1, 1, 128, 80) == 0
     assert f(0, 1, 128, 64) == 0
 
 
@@ -82,7 +83,7 @@ def fwd(lib, B=1, H=1, T=64, d=64, scale=0.125, causal=1, ptrs=(P, P, P, P, P)):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(B=0), 1), (dict(H=-1), 1), (dict(T=0), 1), (dict(T=1 << 25), 1),
-    (dict(d=48), 2), (dict(d=256), 2), (dict(d=80), 2),
+    (dict(d=48), 2), (dict(d=256), 2), (dict(d=96), 2),
     (dict(scale=0.0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1), (dict(scale=-1.0), 1),
     (dict(causal=2), 1),
     (dict(ptrs=(0, P, P, P, P)), 1), (dict(ptrs=(P, P, P, P, 0)), 1),

@@ -53,6 +53,9 @@ EDGE = [
     (1, 1, 1, 128, True), (1, 2, 100, 128, True), (2, 1, 385, 128, True),
     (1, 2, 1, 64, False), (2, 2, 77, 64, False), (1, 2, 300, 64, False), (1, 2, 130, 32, False),
     (1, 2, 260, 128, False), (1, 1, 512, 64, False),
+    # d = 80: the second 64-column chunk of every tile is 16 columns of data and zeros
+    (1, 1, 1, 80, True), (1, 2, 100, 80, True), (2, 1, 385, 80, True), (1, 3, 300, 80, True),
+    (1, 2, 260, 80, False), (1, 1, 129, 80, False),
 ]
 
 
@@ -132,10 +135,10 @@ def test_accumulator_cell_fp32_accumulation():
     assert torch.equal(o, v)
 
 
-@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("d", [32, 64, 80, 128])
 def test_stage_entry_points_match_combined(d):
     """attn_bwd is its stages in order: at d <= 64 dQ (which also forms D) then dK/dV,
-    at d = 128 preprocess, dK/dV, dQ. Same bits when the stages are called one by one."""
+    at d = 80 and 128 preprocess, dK/dV, dQ. Same bits when the stages are called one by one."""
     w = si.WORKLOADS["gpt12m"].with_(B=2, T=300, d=d)
     x = si.make_inputs(w)
     import causal_attention_gb300 as ca
@@ -244,13 +247,13 @@ def test_autograd_function():
     gu.assert_within_tolerance(gu.compare(gpu, ref), "autograd")
 
 
-@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("d", [32, 64, 80, 128])
 def test_persistent_stress_many_items_per_cta(d):
     """Several work items per CTA and K/V stage reuse across items (the persistent
     schedules' barrier phases carry over item boundaries): 40 repeated launches must be
     bitwise identical and the first must match the oracle on sampled heads."""
     import causal_attention_gb300 as ca
-    H = 64 if d < 128 else 32
+    H = 64 if d <= 64 else 32
     w = si.Workload(f"stress{d}", 8, H, 640, d, seed=900 + d)
     x = si.make_inputs(w)
     q, k, v, do = (gu.to_device(x[n]) for n in ("q", "k", "v", "do"))
@@ -272,6 +275,7 @@ GQA = [
     # (B, H, H_kv, T, d, causal)
     (2, 6, 2, 300, 64, True), (1, 8, 1, 257, 64, True), (2, 4, 2, 200, 32, True),
     (1, 4, 2, 385, 128, True), (2, 6, 3, 256, 64, False), (1, 16, 4, 1024, 64, True),
+    (2, 4, 1, 300, 80, True),
 ]
 
 
@@ -308,3 +312,17 @@ def test_gqa_parity(B, H, H_kv, T, d, causal):
     assert torch.equal(dq, dq3)
     for a, b in ((dk, dk3), (dv, dv3)):
         assert gu.rel_rms(gu.to_f64(a), gu.to_f64(b)) <= 2e-3
+
+
+def test_head_dim_80_at_gpt205m_shape():
+    """d = 80 at the B4 H16 T2048 shape (the same seeded distributions as that workload),
+    compared with the oracle on sampled heads."""
+    w = si.WORKLOADS["gpt205m"].with_(name="gpt205m_d80", d=80)
+    x = si.make_inputs(w)
+    gpu = gu.run_gpu(w, x)
+    heads = SAMPLED_HEADS["gpt205m"]
+    err = gu.compare(gpu, gu.run_oracle(w, x, heads=heads), heads)
+    print({k: tuple(f"{e:.2e}" for e in v) for k, v in err.items()})
+    gu.assert_within_tolerance(err, w.name)
+    for t in gpu.values():
+        assert torch.isfinite(t).all()
