@@ -216,3 +216,164 @@ class CausalAttention(torch.autograd.Function):
 
 def attention(q, k, v, scale=None, causal=True):
     return CausalAttention.apply(q, k, v, scale, causal)
+
+
+# ---------------------------------------------------------------------------
+# Projections around the attention (the attention block's training GEMMs)
+# ---------------------------------------------------------------------------
+GEMM_LAYOUTS = {"nt": 0, "nn": 1, "tn": 2}
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size() if t is not None else 0
+
+
+def attn_gemm_workspace_size(M, N, K, layout) -> int:
+    return int(_dll.attn_gemm_workspace_size(M, N, K, GEMM_LAYOUTS[layout]))
+
+
+def attn_gemm(a, b, c, layout, workspace=None, stream=None):
+    """c = op(a) op(b) in place: "nt" a [M, K], b [N, K]; "nn" a [M, K], b [K, N]; "tn"
+    a [K, M], b [K, N] (c fp32 [M, N]; bf16 [M, N] otherwise)."""
+    lay = GEMM_LAYOUTS[layout]
+    if lay == 2:
+        (K, M), N = a.shape, b.shape[1]
+    else:
+        (M, K), N = a.shape, (b.shape[0] if lay == 0 else b.shape[1])
+    for n, t in (("a", a), ("b", b)):
+        _need(t, n, torch.bfloat16)
+    _need(c, "c", torch.float32 if lay == 2 else torch.bfloat16)
+    if tuple(c.shape) != (M, N):
+        raise ValueError(f"c must be [{M}, {N}]")
+    _check(_dll.attn_gemm(_ptr(a), _ptr(b), _ptr(c), M, N, K, lay, _ptr(workspace), _nbytes(workspace),
+                          _stream_handle(stream)), "attn_gemm")
+
+
+def gemm(a, b, layout, stream=None):
+    """Allocates and returns op(a) op(b) (bf16, or fp32 for "tn")."""
+    lay = GEMM_LAYOUTS[layout]
+    M = a.shape[1] if lay == 2 else a.shape[0]
+    N = b.shape[0] if lay == 0 else b.shape[1]
+    K = a.shape[0] if lay == 2 else a.shape[1]
+    c = torch.empty((M, N), dtype=torch.float32 if lay == 2 else torch.bfloat16, device=a.device)
+    n = attn_gemm_workspace_size(M, N, K, layout)
+    ws = torch.empty(n // 4, dtype=torch.float32, device=a.device) if n else None
+    attn_gemm(a, b, c, layout, ws, stream)
+    return c
+
+
+def rope_table(T, d, device=None, stream=None):
+    """fp32 [T, d/2, 2]: (cos, sin) of t * 10000^(-2k/d)."""
+    tab = torch.empty((T, d // 2, 2), dtype=torch.float32, device=device or "cuda")
+    _check(_dll.attn_rope_table(_ptr(tab), T, d, _stream_handle(stream)), "attn_rope_table")
+    return tab
+
+
+def attn_rope(x, y, tab, inverse=False, stream=None):
+    """y = RoPE(x) (inverse: the backward rotation) for [B, H, T, d] bf16 tensors."""
+    B, H, T, d = _shape(x)
+    _need(x, "x", torch.bfloat16)
+    _need(y, "y", torch.bfloat16)
+    _check(_dll.attn_rope(_ptr(x), _ptr(y), _ptr(tab), B, H, T, d, int(inverse), _stream_handle(stream)),
+           "attn_rope")
+
+
+def _proj_dims(x, w_qkv, H, H_kv, d):
+    B, T, C = (int(s) for s in x.shape)
+    if tuple(w_qkv.shape) != ((H + 2 * H_kv) * d, C):
+        raise ValueError(f"w_qkv must be [{(H + 2 * H_kv) * d}, {C}]")
+    return B, T, C
+
+
+def attn_qkv_proj(x, w_qkv, q, k, v, rope_tab=None, stream=None):
+    """q, k, v = split(x W_qkv^T) in place (q, k rotated when rope_tab is given)."""
+    B, H, T, d = _shape(q)
+    H_kv = _shape(k)[1]
+    _proj_dims(x, w_qkv, H, H_kv, d)
+    for n, t in (("x", x), ("w_qkv", w_qkv), ("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16)
+    C = int(x.shape[2])
+    _check(_dll.attn_qkv_proj(_ptr(x), _ptr(w_qkv), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_tab), B, T, C, H, H_kv, d,
+                              _stream_handle(stream)), "attn_qkv_proj")
+
+
+def attn_out_proj(o, w_o, y, stream=None):
+    """y [B, T, C] = merge(o) W_o^T in place."""
+    B, H, T, d = _shape(o)
+    C = int(w_o.shape[0])
+    for n, t in (("o", o), ("w_o", w_o), ("y", y)):
+        _need(t, n, torch.bfloat16)
+    _check(_dll.attn_out_proj(_ptr(o), _ptr(w_o), _ptr(y), B, T, H, d, C, _stream_handle(stream)), "attn_out_proj")
+
+
+def attn_proj_bwd_workspace_size(B, T, C, H, H_kv, d) -> int:
+    return int(_dll.attn_proj_bwd_workspace_size(B, T, C, H, H_kv, d))
+
+
+def new_proj_workspace(B, T, C, H, H_kv, d, device=None):
+    n = attn_proj_bwd_workspace_size(B, T, C, H, H_kv, d)
+    return torch.empty(max(n, 16) // 4, dtype=torch.float32, device=device or "cuda")
+
+
+def attn_out_proj_bwd(dy, o, w_o, d_o, dw_o, workspace, stream=None):
+    B, H, T, d = _shape(o)
+    C = int(w_o.shape[0])
+    for n, t in (("dy", dy), ("o", o), ("w_o", w_o), ("d_o", d_o)):
+        _need(t, n, torch.bfloat16)
+    _need(dw_o, "dw_o", torch.float32)
+    _check(_dll.attn_out_proj_bwd(_ptr(dy), _ptr(o), _ptr(w_o), _ptr(d_o), _ptr(dw_o), _ptr(workspace),
+                                  _nbytes(workspace), B, T, H, d, C, _stream_handle(stream)), "attn_out_proj_bwd")
+
+
+def attn_qkv_proj_bwd(dq, dk, dv, x, w_qkv, dx, dw_qkv, workspace, rope_tab=None, stream=None):
+    B, H, T, d = _shape(dq)
+    H_kv = _shape(dk)[1]
+    _, _, C = _proj_dims(x, w_qkv, H, H_kv, d)
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv), ("x", x), ("w_qkv", w_qkv), ("dx", dx)):
+        _need(t, n, torch.bfloat16)
+    _need(dw_qkv, "dw_qkv", torch.float32)
+    _check(_dll.attn_qkv_proj_bwd(_ptr(dq), _ptr(dk), _ptr(dv), _ptr(x), _ptr(w_qkv), _ptr(rope_tab), _ptr(dx),
+                                  _ptr(dw_qkv), _ptr(workspace), _nbytes(workspace), B, T, C, H, H_kv, d,
+                                  _stream_handle(stream)), "attn_qkv_proj_bwd")
+
+
+def qkv_projection(x, w_qkv, H, H_kv, d, rope_tab=None):
+    """Allocates and returns (q, k, v)."""
+    B, T, C = _proj_dims(x, w_qkv, H, H_kv, d)
+    q = torch.empty((B, H, T, d), dtype=torch.bfloat16, device=x.device)
+    k = torch.empty((B, H_kv, T, d), dtype=torch.bfloat16, device=x.device)
+    v = torch.empty_like(k)
+    attn_qkv_proj(x, w_qkv, q, k, v, rope_tab)
+    return q, k, v
+
+
+def out_projection(o, w_o):
+    B, H, T, d = _shape(o)
+    y = torch.empty((B, T, int(w_o.shape[0])), dtype=torch.bfloat16, device=o.device)
+    attn_out_proj(o, w_o, y)
+    return y
+
+
+def out_projection_backward(dy, o, w_o, workspace=None):
+    """Allocates and returns (dO, dW_o)."""
+    B, H, T, d = _shape(o)
+    C = int(w_o.shape[0])
+    d_o = torch.empty_like(o)
+    dw_o = torch.empty((C, H * d), dtype=torch.float32, device=o.device)
+    if workspace is None:
+        workspace = new_proj_workspace(B, T, C, H, H, d, o.device)
+    attn_out_proj_bwd(dy, o, w_o, d_o, dw_o, workspace)
+    return d_o, dw_o
+
+
+def qkv_projection_backward(dq, dk, dv, x, w_qkv, rope_tab=None, workspace=None):
+    """Allocates and returns (dX, dW_qkv)."""
+    B, H, T, d = _shape(dq)
+    H_kv = _shape(dk)[1]
+    C = int(x.shape[2])
+    dx = torch.empty_like(x)
+    dw = torch.empty(tuple(w_qkv.shape), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = new_proj_workspace(B, T, C, H, H_kv, d, x.device)
+    attn_qkv_proj_bwd(dq, dk, dv, x, w_qkv, dx, dw, workspace, rope_tab)
+    return dx, dw

@@ -47,6 +47,15 @@ SIGNATURES = {
     "attn_bwd_dq_finish": (_I, [_P, _P, _S, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "attn_check_device_error": (_I, [_P]),
+    "attn_gemm_workspace_size": (_S, [_I, _I, _I, _I]),
+    "attn_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
+    "attn_rope_table": (_I, [_P, _I, _I, _P]),
+    "attn_rope": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "attn_qkv_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "attn_out_proj": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "attn_proj_bwd_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
+    "attn_out_proj_bwd": (_I, [_P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _P]),
+    "attn_qkv_proj_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _I, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_cuda_error": (ctypes.c_char_p, []),
 }

@@ -1,6 +1,7 @@
 // C ABI of the attention library: argument checks, TMA descriptors, launches and
 // the device error word.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -300,6 +301,161 @@ void* noalloc_scratch_ptr(cudaError_t* e) {
   return ptrs[dev];
 }
 
+// ---------------------------------------------------------------------------
+// Projections (training GEMMs around the attention)
+// ---------------------------------------------------------------------------
+attn_status encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box) {
+  cudaError_t e = bind_device();
+  if (e != cudaSuccess) return cuda_fail(e, ATTN_ERR_CUDA);
+  EncodeTiledFn fn = encode_fn(&e);
+  if (!fn) return cuda_fail(e, ATTN_ERR_CUDA);
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+// A bf16 [Bn, Z, T, W] tensor as a 4-D map (W, T, Z, Bn) with boxes of 64 features x
+// box_t tokens (128-byte swizzle): one map of a token view.
+attn_status tok_map(CUtensorMap* m, const void* ptr, int W, int T, int Z, int Bn, int box_t) {
+  const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)Z, (cuuint64_t)Bn};
+  const cuuint64_t strides[3] = {(cuuint64_t)W * 2, (cuuint64_t)T * W * 2, (cuuint64_t)Z * T * W * 2};
+  const cuuint32_t box[4] = {64u, (cuuint32_t)box_t, 1u, 1u};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box);
+}
+
+// A bf16 row-major [rows, cols] matrix as a 2-D map with boxes of 64 columns x box_r rows.
+attn_status mat_map(CUtensorMap* m, const void* ptr, int cols, int rows, int box_r) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_r};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box);
+}
+
+// fp32 [S, M, N] partial sums (or the [M, N] result when S = 1) with 32 x 32 store boxes.
+attn_status f32_out_map(CUtensorMap* m, void* ptr, int N, int M, int S) {
+  const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)S};
+  const cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)M * N * 4};
+  const cuuint32_t box[3] = {32u, 32u, 1u};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box);
+}
+
+// A token view over one plain [Bn, T, F] activation.
+attn_status plain_view(CUtensorMap* maps, TokView* v, const void* ptr, int Bn, int T, int F, int box_t) {
+  v->W = F;
+  v->f1 = v->f2 = INT_MAX;
+  return tok_map(&maps[0], ptr, F, T, 1, Bn, box_t);
+}
+
+// A token view over head tensors: p0 [Bn, H0, T, d], then (optionally) p1 and p2
+// [Bn, H1, T, d]: features h*d + c of p0, then of p1, then of p2.
+attn_status head_view(CUtensorMap* maps, TokView* v, int Bn, int T, int d, int box_t, const void* p0, int H0,
+                      const void* p1 = nullptr, const void* p2 = nullptr, int H1 = 0) {
+  v->W = d;
+  v->f1 = p1 ? H0 * d : INT_MAX;
+  v->f2 = p2 ? (H0 + H1) * d : INT_MAX;
+  ATTN_TRY(tok_map(&maps[0], p0, d, T, H0, Bn, box_t));
+  if (p1) ATTN_TRY(tok_map(&maps[1], p1, d, T, H1, Bn, box_t));
+  if (p2) ATTN_TRY(tok_map(&maps[2], p2, d, T, H1, Bn, box_t));
+  return ATTN_OK;
+}
+
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
+// tn products with fewer output tiles than this (the SMs of a GB300) are split over K so
+// that the persistent grid fills the device. A fixed count, not the device's, keeps the
+// result the same on every device.
+constexpr int kGemmFillTiles = 152;
+
+// The split count of a tn product (M x N outputs, k_iters K-steps), and the K-steps of
+// each split: at most one split per whole multiple of the output tiles that fits in
+// kGemmFillTiles, at least 8 K-steps per split, at most 16 splits.
+int gemm_splits(int M, int N, int k_iters, int* k_per_split) {
+  const int tiles = ((M + kGemmBM - 1) / kGemmBM) * ((N + kGemmBN - 1) / kGemmBN);
+  int S = std::max(1, kGemmFillTiles / tiles);
+  S = std::min(S, std::max(1, k_iters / 8));
+  S = std::min(S, 16);
+  const int kps = (k_iters + S - 1) / S;
+  *k_per_split = kps;
+  return (k_iters + kps - 1) / kps;  // no empty split
+}
+
+size_t tn_workspace_bytes(int M, int N, int k_iters) {
+  int kps;
+  const int S = gemm_splits(M, N, k_iters, &kps);
+  return S > 1 ? (size_t)S * M * N * sizeof(float) : 0;
+}
+
+// Sizes, tile counts and the error word of a product; the caller fills the maps and views.
+attn_status gemm_params(GemmParams* p, int layout, int M, int N, int K, int T, int Bn, int* sms) {
+  memset(p, 0, sizeof(*p));
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->T = T;
+  p->splits = 1;
+  p->n_tiles = (N + kGemmBN - 1) / kGemmBN;
+  if (layout == kGemmTN) {
+    p->nT = (T + kGemmBK - 1) / kGemmBK;  // 64-token K-steps per sequence
+    p->m_tiles = (M + kGemmBM - 1) / kGemmBM;
+    p->k_iters = Bn * p->nT;
+    p->splits = gemm_splits(M, N, p->k_iters, &p->k_per_split);
+  } else {
+    p->nT = (T + kGemmBM - 1) / kGemmBM;  // 128-token row tiles per sequence
+    p->m_tiles = Bn * p->nT;
+    p->k_iters = (K + kGemmBK - 1) / kGemmBK;
+    p->k_per_split = p->k_iters;
+  }
+  cudaError_t e;
+  p->err = error_word_ptr(&e);
+  if (!p->err) return cuda_fail(e, ATTN_ERR_CUDA);
+  *sms = num_sms(&e);
+  if (*sms <= 0) return cuda_fail(e, ATTN_ERR_CUDA);
+  return ATTN_OK;
+}
+
+// Runs a tn product into out (fp32 [M, N]): straight, or through S partial slices in the
+// workspace and the in-order reduction.
+attn_status run_tn(GemmParams* p, void* out, void* ws, size_t ws_bytes, int sms, cudaStream_t s) {
+  const size_t need = p->splits > 1 ? (size_t)p->splits * p->M * p->N * sizeof(float) : 0;
+  if (need > 0 && (!ws || ws_bytes < need)) return ATTN_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(ws)) return ATTN_ERR_MISALIGNED;
+  ATTN_TRY(f32_out_map(&p->c[0], need > 0 ? ws : out, p->N, p->M, p->splits));
+  ATTN_TRY(launched(launch_gemm(kGemmTN, *p, sms, s)));
+  if (need > 0)
+    ATTN_TRY(launched(launch_splitk_reduce(static_cast<const float*>(ws), static_cast<float*>(out),
+                                           (long long)p->M * p->N, p->splits, sms, s)));
+  return ATTN_OK;
+}
+
+// Shape checks of the projections: every size >= 1, head dim 64 or 128 (a 64-feature box
+// never straddles two heads), model width a multiple of 8 (16-byte rows).
+attn_status check_proj(int B, int T, int C, int H, int H_kv, int d) {
+  if (B < 1 || T < 1 || C < 1 || H < 1) return ATTN_ERR_INVALID_ARG;
+  ATTN_TRY(check_kv_heads(H, H_kv));
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (C % 8 != 0) return ATTN_ERR_INVALID_ARG;
+  const long long tokens = (long long)B * T, feats = (long long)(H + 2 * H_kv) * d;
+  if (T > kMaxT || tokens > kMaxBH || feats > kMaxBH || C > kMaxBH || tokens * std::max<long long>(feats, C) > kMaxElems)
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+size_t proj_bwd_workspace_bytes(int B, int T, int C, int H, int H_kv, int d) {
+  const int k_iters = B * ((T + kGemmBK - 1) / kGemmBK);
+  const size_t dwo = tn_workspace_bytes(C, H * d, k_iters);
+  const size_t dwqkv = tn_workspace_bytes((H + 2 * H_kv) * d, C, k_iters);
+  // the rotated-back dQ and dK (bf16) come first when RoPE is used
+  const size_t rot = (size_t)B * (H + H_kv) * (size_t)T * d * 2;
+  const size_t rot_pad = (rot + 255) / 256 * 256;
+  return std::max(dwo, rot_pad + dwqkv);
+}
+
 }  // namespace
 
 cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask) {
@@ -539,7 +695,8 @@ const char* attn_status_string(attn_status status) {
   switch (status) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_INVALID_ARG: return "invalid argument";
-    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension (d must be 32, 64, 80 or 128)";
+    case ATTN_ERR_UNSUPPORTED:
+      return "unsupported head dimension (attention: d in {32, 64, 80, 128}; projections: d in {64, 128})";
     case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case ATTN_ERR_LAUNCH: return "kernel launch failed";
@@ -550,5 +707,159 @@ const char* attn_status_string(attn_status status) {
 }
 
 const char* attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+// ---------------------------------------------------------------------------
+// Projections
+// ---------------------------------------------------------------------------
+size_t attn_gemm_workspace_size(int M, int N, int K, int layout) {
+  if (M < 1 || N < 1 || K < 1 || layout < 0 || layout > 2) return 0;
+  if (layout != kGemmTN) return 0;
+  return tn_workspace_bytes(M, N, (K + kGemmBK - 1) / kGemmBK);
+}
+
+attn_status attn_gemm(const void* a, const void* b, void* c, int M, int N, int K, int layout, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || layout < 0 || layout > 2) return ATTN_ERR_INVALID_ARG;
+  if (M % 8 || N % 8 || K % 8) return ATTN_ERR_INVALID_ARG;
+  if ((long long)M * K > kMaxElems || (long long)N * K > kMaxElems || (long long)M * N > kMaxElems ||
+      M > kMaxT || N > kMaxT || K > kMaxT)
+    return ATTN_ERR_INVALID_ARG;
+  ATTN_TRY(check_ptrs({a, b, c}));
+  GemmParams p;
+  int sms = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (layout == kGemmTN) {
+    // A [K, M] and B [K, N]: K plays the token dimension (one sequence of K tokens)
+    ATTN_TRY(gemm_params(&p, layout, M, N, K, K, 1, &sms));
+    ATTN_TRY(plain_view(p.a, &p.va, a, 1, K, M, kGemmBK));
+    ATTN_TRY(plain_view(p.b, &p.vb, b, 1, K, N, kGemmBK));
+    return run_tn(&p, c, workspace, workspace_bytes, sms, s);
+  }
+  // A [M, K]: M plays the token dimension
+  ATTN_TRY(gemm_params(&p, layout, M, N, K, M, 1, &sms));
+  ATTN_TRY(plain_view(p.a, &p.va, a, 1, M, K, kGemmBM));
+  if (layout == kGemmNT)
+    ATTN_TRY(mat_map(&p.b[0], b, K, N, 128));  // B [N, K]
+  else
+    ATTN_TRY(mat_map(&p.b[0], b, N, K, 64));  // B [K, N]
+  ATTN_TRY(plain_view(p.c, &p.vc, c, 1, M, N, 32));
+  return launched(launch_gemm(layout, p, sms, s));
+}
+
+attn_status attn_rope_table(float* tab, int T, int d, void* stream) {
+  if (T < 1 || T > kMaxT || d < 2 || d % 8 != 0 || d > 1024) return ATTN_ERR_INVALID_ARG;
+  ATTN_TRY(check_ptrs({tab}));
+  cudaError_t e = bind_device();
+  if (e != cudaSuccess) return cuda_fail(e, ATTN_ERR_CUDA);
+  return launched(launch_rope_table(tab, T, d, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_rope(const void* x, void* y, const float* rope_tab, int B, int H, int T, int d, int inverse,
+                      void* stream) {
+  if (B < 1 || H < 1 || T < 1 || T > kMaxT || (long long)B * H > kMaxBH) return ATTN_ERR_INVALID_ARG;
+  if (d < 8 || d % 8 != 0 || (inverse != 0 && inverse != 1)) return ATTN_ERR_INVALID_ARG;
+  ATTN_TRY(check_ptrs({x, y, rope_tab}));
+  cudaError_t e;
+  const int sms = num_sms(&e);
+  if (sms <= 0) return cuda_fail(e, ATTN_ERR_CUDA);
+  return launched(launch_rope_apply(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), rope_tab,
+                                    (long long)B * H * T, T, d, inverse, sms, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_qkv_proj(const void* x, const void* w_qkv, void* q, void* k, void* v, const float* rope_tab, int B,
+                          int T, int C, int H, int H_kv, int d, void* stream) {
+  ATTN_TRY(check_proj(B, T, C, H, H_kv, d));
+  ATTN_TRY(check_ptrs({x, w_qkv, q, k, v}));
+  if (rope_tab && !aligned16(rope_tab)) return ATTN_ERR_MISALIGNED;
+  const int N = (H + 2 * H_kv) * d;
+  GemmParams p;
+  int sms = 0;
+  ATTN_TRY(gemm_params(&p, kGemmNT, B * T, N, C, T, B, &sms));
+  ATTN_TRY(plain_view(p.a, &p.va, x, B, T, C, kGemmBM));
+  ATTN_TRY(mat_map(&p.b[0], w_qkv, C, N, 128));
+  ATTN_TRY(head_view(p.c, &p.vc, B, T, d, 32, q, H, k, v, H_kv));
+  if (rope_tab) {
+    p.rope_features = (H + H_kv) * d;  // q and k
+    p.rope_half = d / 2;
+    p.rope_tab = rope_tab;
+  }
+  return launched(launch_gemm(kGemmNT, p, sms, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_out_proj(const void* o, const void* w_o, void* y, int B, int T, int H, int d, int C, void* stream) {
+  ATTN_TRY(check_proj(B, T, C, H, H, d));
+  ATTN_TRY(check_ptrs({o, w_o, y}));
+  GemmParams p;
+  int sms = 0;
+  ATTN_TRY(gemm_params(&p, kGemmNT, B * T, C, H * d, T, B, &sms));
+  ATTN_TRY(head_view(p.a, &p.va, B, T, d, kGemmBM, o, H));
+  ATTN_TRY(mat_map(&p.b[0], w_o, H * d, C, 128));
+  ATTN_TRY(plain_view(p.c, &p.vc, y, B, T, C, 32));
+  return launched(launch_gemm(kGemmNT, p, sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t attn_proj_bwd_workspace_size(int B, int T, int C, int H, int H_kv, int d) {
+  if (check_proj(B, T, C, H, H_kv, d) != ATTN_OK) return 0;
+  return proj_bwd_workspace_bytes(B, T, C, H, H_kv, d);
+}
+
+attn_status attn_out_proj_bwd(const void* dy, const void* o, const void* w_o, void* d_o, float* dw_o, void* workspace,
+                              size_t workspace_bytes, int B, int T, int H, int d, int C, void* stream) {
+  ATTN_TRY(check_proj(B, T, C, H, H, d));
+  ATTN_TRY(check_ptrs({dy, o, w_o, d_o, dw_o}));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemmParams p;
+  int sms = 0;
+  // dO = split(dY W_o): nn, M = tokens, N = H d, K = C
+  ATTN_TRY(gemm_params(&p, kGemmNN, B * T, H * d, C, T, B, &sms));
+  ATTN_TRY(plain_view(p.a, &p.va, dy, B, T, C, kGemmBM));
+  ATTN_TRY(mat_map(&p.b[0], w_o, H * d, C, 64));  // W_o [C, H d] as [K, N]
+  ATTN_TRY(head_view(p.c, &p.vc, B, T, d, 32, d_o, H));
+  ATTN_TRY(launched(launch_gemm(kGemmNN, p, sms, s)));
+  // dW_o = dY^T merge(O): tn, M = C, N = H d, K = tokens
+  ATTN_TRY(gemm_params(&p, kGemmTN, C, H * d, B * T, T, B, &sms));
+  ATTN_TRY(plain_view(p.a, &p.va, dy, B, T, C, kGemmBK));
+  ATTN_TRY(head_view(p.b, &p.vb, B, T, d, kGemmBK, o, H));
+  return run_tn(&p, dw_o, workspace, workspace_bytes, sms, s);
+}
+
+attn_status attn_qkv_proj_bwd(const void* dq, const void* dk, const void* dv, const void* x, const void* w_qkv,
+                              const float* rope_tab, void* dx, float* dw_qkv, void* workspace, size_t workspace_bytes,
+                              int B, int T, int C, int H, int H_kv, int d, void* stream) {
+  ATTN_TRY(check_proj(B, T, C, H, H_kv, d));
+  ATTN_TRY(check_ptrs({dq, dk, dv, x, w_qkv, dx, dw_qkv}));
+  if (rope_tab && !aligned16(rope_tab)) return ATTN_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int N = (H + 2 * H_kv) * d;
+  size_t rot_pad = 0;
+  if (rope_tab) {
+    // dQ and dK rotated back (the inverse rotation) into the front of the workspace
+    const size_t rq = (size_t)B * H * T * d, rk = (size_t)B * H_kv * T * d;
+    rot_pad = ((rq + rk) * 2 + 255) / 256 * 256;
+    if (!workspace || workspace_bytes < rot_pad) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+    __nv_bfloat16* wq = static_cast<__nv_bfloat16*>(workspace);
+    __nv_bfloat16* wk = wq + rq;
+    ATTN_TRY(attn_rope(dq, wq, rope_tab, B, H, T, d, 1, stream));
+    ATTN_TRY(attn_rope(dk, wk, rope_tab, B, H_kv, T, d, 1, stream));
+    dq = wq;
+    dk = wk;
+  }
+  GemmParams p;
+  int sms = 0;
+  // dX = merge(dQ, dK, dV) W_qkv: nn, M = tokens, N = C, K = (H + 2 H_kv) d
+  ATTN_TRY(gemm_params(&p, kGemmNN, B * T, C, N, T, B, &sms));
+  ATTN_TRY(head_view(p.a, &p.va, B, T, d, kGemmBM, dq, H, dk, dv, H_kv));
+  ATTN_TRY(mat_map(&p.b[0], w_qkv, C, N, 64));  // W_qkv [N, C] as [K, N]
+  ATTN_TRY(plain_view(p.c, &p.vc, dx, B, T, C, 32));
+  ATTN_TRY(launched(launch_gemm(kGemmNN, p, sms, s)));
+  // dW_qkv = merge(dQ, dK, dV)^T X: tn, M = (H + 2 H_kv) d, N = C, K = tokens
+  ATTN_TRY(gemm_params(&p, kGemmTN, N, C, B * T, T, B, &sms));
+  ATTN_TRY(head_view(p.a, &p.va, B, T, d, kGemmBK, dq, H, dk, dv, H_kv));
+  ATTN_TRY(plain_view(p.b, &p.vb, x, B, T, C, kGemmBK));
+  void* ws_tn = workspace ? static_cast<char*>(workspace) + rot_pad : nullptr;
+  const size_t ws_tn_bytes = workspace_bytes > rot_pad ? workspace_bytes - rot_pad : 0;
+  return run_tn(&p, dw_qkv, ws_tn, ws_tn_bytes, sms, s);
+}
 
 }  // extern "C"

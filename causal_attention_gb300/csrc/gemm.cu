@@ -1,0 +1,436 @@
+// Training GEMMs of the attention block for sm_103a: C = op(A) op(B) with bf16 operands
+// and fp32 accumulation in tensor memory, tcgen05 MMAs fed by a TMA ring.
+//
+// The three orientations a training step needs (Forge RESEARCH.md, section 5 "GEMM
+// design": nt for the forward X W^T, nn for dX = dY W, tn for dW = dY^T X; the Forge
+// paper's GEMM table in section "Results"), with the attention's layouts folded into the
+// TMA tensor maps instead of separate copy passes: the QKV projection stores Q, K and V
+// straight into their [B, H, T, d] tensors (head split), the output projection and the
+// backward GEMMs read the heads straight from them (head merge), and the QKV epilogue
+// can rotate q and k (RoPE, Forge RESEARCH.md section 7, model formulas) in fp32 before
+// rounding to bf16.
+//
+// Work item: a 128 x 256 output tile, accumulated over K-steps of 64 (one 128-byte
+// swizzle atom of bf16) through a 4-stage ring of 48 KB stages. Persistent: one CTA per
+// SM loops over the work items.
+//   warp 0      TMA producer
+//   warp 1      TMEM allocator (512 columns = two 256-column fp32 accumulators) and MMA
+//               issuer (M = 128, N = 256, K = 16 per instruction)
+//   warps 2-5   epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 of the
+//               finished accumulator, converts them, stages 32-row x 128-byte tiles in
+//               shared memory and writes them with TMA stores, while the MMAs of the next
+//               work item fill the other accumulator.
+// Split-K (tn, the dW shape: few output tiles, K = B T long): the work items also range
+// over S contiguous K ranges; each writes fp32 partial sums into its own [M, N] slice and
+// a second launch adds the slices in the order s = 0, 1, ... (no atomics: every run gives
+// the same bits; the split / reduce structure of RESEARCH.md section 5).
+#include <climits>
+
+#include "kernels.h"
+#include "tile.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kGM = 128, kGN = 256, kGK = 64, kGST = 4;
+constexpr int kGemmThreads = 192;
+constexpr int kGABytes = kGM * kGK * 2;  // 16 KB
+constexpr int kGBBytes = kGN * kGK * 2;  // 32 KB
+constexpr int kGStageBytes = kGABytes + kGBBytes;
+constexpr int kGChunk = kGK * 128;      // one MN-major chunk: 64 elements x 64 K-rows (8 KB)
+constexpr int kGEpiBytes = 32 * 128;    // one epilogue staging tile: 32 rows x 128 bytes
+constexpr int kGOffEpi = kGST * kGStageBytes;
+constexpr int kGOffBar = kGOffEpi + 4 * 2 * kGEpiBytes;
+constexpr int kGNBar = 2 * kGST + 5;
+constexpr int kGOffMisc = kGOffBar + kGNBar * 8;
+constexpr int kGemmSmem = kGOffMisc + 16 + 1024;  // + alignment slack
+static_assert(kGemmSmem <= 227 * 1024, "shared memory per CTA");
+
+// Which map holds feature f of a token view, and its (x, z) coordinates there.
+__device__ __forceinline__ void view_coord(const TokView& v, int f, int& map, int& x, int& z) {
+  map = f >= v.f2 ? 2 : (f >= v.f1 ? 1 : 0);
+  const int fl = f - (map == 2 ? v.f2 : (map == 1 ? v.f1 : 0));
+  x = fl % v.W;
+  z = fl / v.W;
+}
+
+// K-major operand (rows of 64 K-elements = 128 swizzled bytes, 8-row groups 1024 bytes
+// apart): K-step k (16 elements) starts 32 bytes further.
+__device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return smem_desc<128>(addr, 16, 1024); }
+// MN-major operand (64-element MN chunks of 64 K-rows, kGChunk bytes apart; 8 K-rows per
+// 1024 bytes): K-step k starts 16 rows (2 KB) further.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return smem_desc<128>(addr, kGChunk, 1024); }
+constexpr uint64_t kStepK = 32 >> 4, kStepMN = (16 * 128) >> 4;
+
+template <int LAYOUT, bool ROPE>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool A_MN = LAYOUT == kGemmTN, B_MN = LAYOUT != kGemmNT;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + kGOffBar;
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kGST + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kGST + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kGST + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * kGST + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kGOffMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + kGOffMisc + 4);
+  const Abort ab{abort, p.err};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGST; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // work item u: K range u % splits, output tile u / splits (n tiles fastest, so that
+  // neighbouring CTAs share the A rows)
+  const int n_items = p.m_tiles * p.n_tiles * p.splits;
+  auto item_k0 = [&](int u) { return (u % p.splits) * p.k_per_split; };
+  auto item_k1 = [&](int u) { return min(item_k0(u) + p.k_per_split, p.k_iters); };
+  auto item_mt = [&](int u) { return (u / p.splits) / p.n_tiles; };
+  auto item_nt = [&](int u) { return (u / p.splits) % p.n_tiles; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    // One thread issues every copy, so the coordinates are worked out once per work
+    // item and then advanced per K-step (no divisions in the K loop).
+    if (lane == 0) {
+      bool ok = true;
+      int g = 0;
+      for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x) {
+        const int mt = item_mt(u), nt = item_nt(u), k0 = item_k0(u), k1 = item_k1(u);
+        // NT / NN: A's token rows (fixed) and its K features 64 k0, 64 (k0 + 1), ...
+        int a_b = 0, a_t = 0, a_f = 0, a_map = 0, a_x = 0, a_z = 0;
+        // TN: the token K-step (b, t0) and the MN chunks' coordinates (fixed)
+        int k_b = 0, k_t = 0;
+        int am[2] = {0, 0}, ax[2] = {0, 0}, az[2] = {0, 0}, bm[4] = {0, 0, 0, 0}, bx[4] = {0, 0, 0, 0},
+            bz[4] = {0, 0, 0, 0};
+        if constexpr (!A_MN) {
+          a_b = mt / p.nT;
+          a_t = (mt % p.nT) * kGM;
+          a_f = k0 * kGK;
+          view_coord(p.va, a_f, a_map, a_x, a_z);
+        } else {
+          k_b = k0 / p.nT;
+          k_t = (k0 % p.nT) * kGK;
+#pragma unroll
+          for (int j = 0; j < kGM / 64; ++j) view_coord(p.va, mt * kGM + 64 * j, am[j], ax[j], az[j]);
+#pragma unroll
+          for (int j = 0; j < kGN / 64; ++j) view_coord(p.vb, nt * kGN + 64 * j, bm[j], bx[j], bz[j]);
+        }
+        for (int i = k0; i < k1; ++i, ++g) {
+          const int s = g % kGST;
+          if (g >= kGST && !(ok = mbar_wait(empty(s), (g / kGST - 1) & 1, ab, kErrTimeoutLoad))) break;
+          mbar_arrive_expect_tx(full(s), kGStageBytes);
+          const uint32_t sA = base + s * kGStageBytes, sB = sA + kGABytes;
+          if constexpr (!A_MN) {
+            // 128 tokens (one sequence's row tile) x features 64i .. 64i + 63
+            tma_load_4d(sA, &p.a[a_map], a_x, a_t, a_z, a_b, full(s));
+            a_f += kGK;
+            if (a_f == p.va.f1 || a_f == p.va.f2) {  // into the next tensor of the view
+              ++a_map;
+              a_x = a_z = 0;
+            } else if ((a_x += kGK) >= p.va.W) {  // into the next head
+              a_x = 0;
+              ++a_z;
+            }
+          } else {
+            // features 128 mt .. 128 mt + 127 (two MN chunks) x the 64 tokens of K-step i
+#pragma unroll
+            for (int j = 0; j < kGM / 64; ++j) tma_load_4d(sA + j * kGChunk, &p.a[am[j]], ax[j], k_t, az[j], k_b, full(s));
+          }
+          if constexpr (LAYOUT == kGemmNT) {
+            // rows 256 nt .. 256 nt + 255 of B [N, K] x K-columns 64i .. 64i + 63
+            tma_load_2d(sB, &p.b[0], i * kGK, nt * kGN, full(s));
+            tma_load_2d(sB + kGBBytes / 2, &p.b[0], i * kGK, nt * kGN + kGN / 2, full(s));
+          } else if constexpr (LAYOUT == kGemmNN) {
+            // K-rows 64i .. 64i + 63 of B [K, N] x four 64-column MN chunks
+#pragma unroll
+            for (int j = 0; j < kGN / 64; ++j) tma_load_2d(sB + j * kGChunk, &p.b[0], nt * kGN + 64 * j, i * kGK, full(s));
+          } else {
+#pragma unroll
+            for (int j = 0; j < kGN / 64; ++j) tma_load_4d(sB + j * kGChunk, &p.b[bm[j]], bx[j], k_t, bz[j], k_b, full(s));
+            if ((k_t += kGK) >= p.nT * kGK) {  // the next sequence
+              k_t = 0;
+              ++k_b;
+            }
+          }
+        }
+      }
+      if (!ok)  // every copy issued must land before the CTA exits
+        for (int x = max(0, g - kGST); x < g; ++x) mbar_wait_drain(full(x % kGST), (x / kGST) & 1, ab);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kGM, kGN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      constexpr uint64_t stepA = A_MN ? kStepMN : kStepK, stepB = B_MN ? kStepMN : kStepK;
+      constexpr uint64_t kStageOff = (uint64_t)(kGStageBytes >> 4);
+      const uint64_t da0 = A_MN ? desc_mn(base) : desc_k(base);
+      const uint64_t db0 = B_MN ? desc_mn(base + kGABytes) : desc_k(base + kGABytes);
+      bool ok = true;
+      int g = 0, r = 0;
+      for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x, ++r) {
+        const int b = r & 1, k0 = item_k0(u), k1 = item_k1(u);
+        // the accumulator still holds item r - 2 until the epilogue has read it
+        if (r >= 2 && !(ok = mbar_wait(acc_empty(b), ((r >> 1) - 1) & 1, ab, kErrTimeoutMma))) break;
+        tc_fence_after();
+        const uint32_t tacc = tmem + 256u * (uint32_t)b;
+        for (int i = k0; i < k1; ++i, ++g) {
+          const int s = g % kGST;
+          if (!(ok = mbar_wait(full(s), (g / kGST) & 1, ab, kErrTimeoutMma))) break;
+          tc_fence_after();
+          const uint64_t da = da0 + (uint64_t)s * kStageOff, db = db0 + (uint64_t)s * kStageOff;
+#pragma unroll
+          for (int k = 0; k < kGK / 16; ++k)
+            mma_ss(tacc, da + stepA * k, db + stepB * k, idesc, (i > k0 || k > 0) ? 1u : 0u);
+          mma_commit(empty(s));
+        }
+        if (!ok) break;
+        mma_commit(acc_full(b));
+      }
+      if (!ok) {
+        mma_commit(drain);  // completes once every MMA issued so far is done
+        mbar_wait_drain(drain, 0, ab);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int eq = warp & 3;  // the TMEM lane quarter this warp may access
+    const uint32_t lane_base = (uint32_t)(eq * 32) << 16;
+    const uint32_t stage0 = base + kGOffEpi + (uint32_t)eq * 2u * kGEpiBytes;
+    const uint32_t srow = (uint32_t)lane * 128u;
+    int cnt = 0;  // TMA stores this warp has issued (its two staging tiles alternate)
+    bool ok = true;
+    // a staging tile may be rewritten once the store issued two stores ago has read it
+    auto take_buffer = [&]() {
+      if (cnt >= 2) {
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+      }
+      return stage0 + (uint32_t)(cnt & 1) * kGEpiBytes;
+    };
+    int r = 0;
+    for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x, ++r) {
+      const int b = r & 1, mt = item_mt(u), nt = item_nt(u);
+      if (!(ok = mbar_wait_warp(acc_full(b), (r >> 1) & 1, ab, kErrTimeoutElem))) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem + lane_base + 256u * (uint32_t)b;
+      if constexpr (LAYOUT != kGemmTN) {
+        // bf16 tokens x features through the token view of C
+        const int bi = mt / p.nT, t0 = (mt % p.nT) * kGM + 32 * eq, t = t0 + lane;
+        const bool rows = t0 < p.T;
+#pragma unroll 1
+        for (int j = 0; j < kGN / 64; ++j) {
+          const int f = nt * kGN + 64 * j;
+          if (f >= p.N) break;
+          uint32_t v[64];
+          tmem_ld32(tacc + 64u * j, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tacc + 64u * j + 32u, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (!rows) continue;
+          int map, x, z;
+          view_coord(p.vc, f, map, x, z);
+          uint32_t pk[32];
+          if (ROPE && f < p.rope_features) {
+            // pairs (x + 2i, x + 2i + 1) of head z at position t: (cos, sin) entries x/2 + i
+            const float4* cs4 = reinterpret_cast<const float4*>(p.rope_tab) +
+                                (((size_t)min(t, p.T - 1) * p.rope_half + (x >> 1)) >> 1);
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) {
+              const float4 cs = __ldg(cs4 + i2);
+              const float a0 = __uint_as_float(v[4 * i2]), b0 = __uint_as_float(v[4 * i2 + 1]);
+              const float a1 = __uint_as_float(v[4 * i2 + 2]), b1 = __uint_as_float(v[4 * i2 + 3]);
+              pk[2 * i2] = pack_bf16(a0 * cs.x - b0 * cs.y, a0 * cs.y + b0 * cs.x);
+              pk[2 * i2 + 1] = pack_bf16(a1 * cs.z - b1 * cs.w, a1 * cs.w + b1 * cs.z);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          }
+          const uint32_t buf = take_buffer();
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            sts128(buf + srow + (((uint32_t)g ^ (uint32_t)(lane & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
+                   pk[4 * g + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&p.c[map], buf, x, t0, z, bi);  // rows past T are not written
+            bulk_commit();
+          }
+          ++cnt;
+        }
+      } else {
+        // fp32 [split][M][N] through the 3-D map of C
+        const int m0 = mt * kGM + 32 * eq, sp = u % p.splits;
+        const bool rows = m0 < p.M;
+#pragma unroll 1
+        for (int j = 0; j < kGN / 32; ++j) {
+          const int n = nt * kGN + 32 * j;
+          if (n >= p.N) break;
+          uint32_t v[32];
+          tmem_ld32(tacc + 32u * j, v);
+          tmem_wait_ld();
+          if (!rows) continue;
+          const uint32_t buf = take_buffer();
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            sts128(buf + srow + (((uint32_t)g ^ (uint32_t)(lane & 7)) << 4), v[4 * g], v[4 * g + 1], v[4 * g + 2],
+                   v[4 * g + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.c[0], buf, n, m0, sp);  // rows past M, columns past N are not written
+            bulk_commit();
+          }
+          ++cnt;
+        }
+      }
+      // this warp has read its lanes of the accumulator
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(b));
+    }
+    if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// out = sum over s of part[s] (fp32, added in split order), 4 values per thread
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __restrict__ part, float4* __restrict__ out,
+                                                            long long mn4, int splits) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < mn4;
+       i += (long long)gridDim.x * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = part[(long long)s * mn4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    out[i] = a;
+  }
+}
+
+// tab[t][k] = (cos, sin) of t * 10000^(-2k/d), in fp64, rounded to fp32
+__global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ tab, int T, int d) {
+  const int half = d / 2;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)T * half;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / half), k = (int)(i % half);
+    const double ang = (double)t * pow(10000.0, -2.0 * k / d);
+    double s, c;
+    sincos(ang, &s, &c);
+    tab[i] = make_float2((float)c, (float)s);
+  }
+}
+
+// dst = src with each pair (2k, 2k+1) of a row at position t rotated by sgn * t theta_k;
+// one thread takes one 16-byte granule (four pairs)
+__global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                         const float4* __restrict__ tab, long long n_rows, int T,
+                                                         int d, float sgn) {
+  const int gpr = d / 8, half = d / 2;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_rows * gpr;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / gpr;
+    const int gi = (int)(i % gpr), t = (int)(row % T);
+    const uint4 in = src[i];
+    const float4* cs4 = tab + (((size_t)t * half + 4 * gi) >> 1);
+    const float4 c01 = __ldg(cs4), c23 = __ldg(cs4 + 1);
+    const float cs[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a = __uint_as_float(w[q] << 16), b = __uint_as_float(w[q] & 0xFFFF0000u);
+      const float c = cs[2 * q], s = sgn * cs[2 * q + 1];
+      o[q] = pack_bf16(a * c - b * s, a * s + b * c);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+int grid_for(long long work, int per_block, int num_sms) {
+  long long blocks = (work + per_block - 1) / per_block;
+  const long long cap = (long long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+template <int LAYOUT, bool ROPE>
+cudaError_t launch_gemm_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
+  auto kern = gemm_kernel<LAYOUT, ROPE>;
+  static uint32_t configured = 0;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), kGemmSmem, &configured);
+  if (e != cudaSuccess) return e;
+  const int n_items = p.m_tiles * p.n_tiles * p.splits;
+  kern<<<min(n_items, num_sms), kGemmThreads, kGemmSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int layout, const GemmParams& p, int num_sms, cudaStream_t stream) {
+  if (p.m_tiles < 1 || p.n_tiles < 1 || p.k_iters < 1 || p.splits < 1) return cudaErrorInvalidValue;
+  switch (layout) {
+    case kGemmNT:
+      return p.rope_features > 0 ? launch_gemm_t<kGemmNT, true>(p, num_sms, stream)
+                                 : launch_gemm_t<kGemmNT, false>(p, num_sms, stream);
+    case kGemmNN: return launch_gemm_t<kGemmNN, false>(p, num_sms, stream);
+    case kGemmTN: return launch_gemm_t<kGemmTN, false>(p, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_splitk_reduce(const float* part, float* out, long long mn, int splits, int num_sms,
+                                 cudaStream_t stream) {
+  const long long mn4 = mn / 4;
+  splitk_reduce_kernel<<<grid_for(mn4, 256, num_sms), 256, 0, stream>>>(reinterpret_cast<const float4*>(part),
+                                                                       reinterpret_cast<float4*>(out), mn4, splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float* tab, int T, int d, cudaStream_t stream) {
+  const long long n = (long long)T * (d / 2);
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(reinterpret_cast<float2*>(tab), T, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_apply(const __nv_bfloat16* src, __nv_bfloat16* dst, const float* tab, long long n_rows,
+                              int T, int d, int inverse, int num_sms, cudaStream_t stream) {
+  const long long n = n_rows * (d / 8);
+  rope_apply_kernel<<<grid_for(n, 256, num_sms), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), reinterpret_cast<const float4*>(tab), n_rows,
+      T, d, inverse ? -1.f : 1.f);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -63,6 +63,52 @@ cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv_dq(const BwdArgs& a, cudaStream_t stream);  // fused dK, dV, dQ (d <= 64)
 cudaError_t launch_bwd_dq_finish(const BwdArgs& a, cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// Training GEMMs around the attention (QKV and output projections)
+// ---------------------------------------------------------------------------
+// Orientation of C = op(A) op(B): NT C = A B^T (A [M, K], B [N, K]); NN C = A B (A [M, K],
+// B [K, N]); TN C = A^T B (A [K, M], B [K, N]).
+enum GemmLayout : int { kGemmNT = 0, kGemmNN = 1, kGemmTN = 2 };
+
+// A token x feature operand stored as one to three 4-D tensors [Bn, Z, T, W] (dims W, T,
+// Z, Bn for TMA): feature f of token (b, t) is element (b, f' / W, t, f' % W) of map
+// m(f), f' = f - first feature of that map. A plain [Bn, T, F] activation is one map with
+// W = F, Z = 1; the heads of Q / K / V ([Bn, H, T, d]) are W = d, Z = H, up to three
+// maps (Q, K, V) for the concatenated QKV features.
+struct TokView {
+  int W;       // features per row of a map
+  int f1, f2;  // first feature of map 1 and of map 2 (INT_MAX where absent)
+};
+
+struct GemmParams {
+  CUtensorMap a[3];  // A: token view (NT / NN: K-major boxes of 64 features x 128 tokens;
+                     // TN: MN-major boxes of 64 features x 64 tokens)
+  CUtensorMap b[3];  // B: NT a 2-D [N, K] map (64 x 128 boxes); NN a 2-D [K, N] map (64 x 64);
+                     // TN a token view (64 features x 64 tokens)
+  CUtensorMap c[3];  // C: NT / NN a token view (bf16 stores of 64 features x 32 tokens);
+                     // TN a 3-D fp32 [S, M, N] map (stores of 32 x 32)
+  TokView va, vb, vc;
+  int M, N, K;        // logical sizes of the product
+  int T;              // tokens per sequence (the token dimension of the views)
+  int nT;             // NT / NN: 128-token row tiles per sequence; TN: 64-token K-steps
+  int m_tiles, n_tiles, k_iters, splits, k_per_split;
+  int rope_features;  // NT epilogue: features below this are rotated (RoPE), 0 for none
+  int rope_half;      // d / 2: entries of one position's row of the rotation table
+  const float* rope_tab;  // [T][d/2][2] fp32 (cos, sin), or null
+  uint32_t* err;          // device error word
+};
+
+// C = op(A) op(B); with p.splits > 1 (TN only) C is the [splits, M, N] partial-sum stack.
+cudaError_t launch_gemm(int layout, const GemmParams& p, int num_sms, cudaStream_t stream);
+// out[m, n] = sum over s = 0, 1, ... of part[s, m, n] (fp32, in split order)
+cudaError_t launch_splitk_reduce(const float* part, float* out, long long mn, int splits, int num_sms,
+                                 cudaStream_t stream);
+// tab[t][k] = (cos, sin)(t * 10000^(-2k/d)), computed in fp64 and rounded to fp32
+cudaError_t launch_rope_table(float* tab, int T, int d, cudaStream_t stream);
+// dst = rope(src) (inverse: the rotation by -t theta_k) over [n_rows / T sequences, T, d] bf16
+cudaError_t launch_rope_apply(const __nv_bfloat16* src, __nv_bfloat16* dst, const float* tab, long long n_rows,
+                              int T, int d, int inverse, int num_sms, cudaStream_t stream);
+
 // Sets the max dynamic shared memory of a kernel once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask);
 

@@ -42,12 +42,12 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 typedef enum attn_status {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,     /* null pointer, B/H/T < 1, bad scale or causal flag, sizes too large */
-  ATTN_ERR_UNSUPPORTED = 2,     /* head dimension d not in {32, 64, 80, 128} */
+  ATTN_ERR_UNSUPPORTED = 2,     /* head dimension d not in {32, 64, 80, 128} (projections: {64, 128}) */
   ATTN_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,       /* workspace missing or smaller than attn_bwd_workspace_size() */
   ATTN_ERR_LAUNCH = 5,          /* the CUDA runtime rejected a launch (see attn_last_cuda_error) */
@@ -221,6 +221,75 @@ const char* attn_status_string(attn_status status);
 
 /* Text of the last CUDA error seen by this thread inside the library ("" if none). */
 const char* attn_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------------------
+ * Projections around the attention: the training GEMMs of the attention block.
+ *
+ * Cited definitions: the GEMM orientations a training step needs, nt (forward
+ * Y = X W^T), nn (dX = dY W) and tn (dW = dY^T X), with split-K for the dW shape into
+ * fp32 partials and a separate reduction, no atomics (Forge RESEARCH.md section 5 "GEMM
+ * design"; the Forge paper's GEMM table, section "Results"); rotary position embedding
+ * on q and k, interleaved pairs (2k, 2k+1) of a head row at position t rotated by
+ * t * 10000^(-2k/d), backward = the rotation by minus that angle (Forge RESEARCH.md
+ * section 7, model formulas).
+ *
+ * The attention block: x [B, T, C] bf16 -> q [B, H, T, d], k, v [B, H_kv, T, d] =
+ * split(x W_qkv^T) (W_qkv bf16 [(H + 2 H_kv) d, C]: the rows of Q's heads, then K's,
+ * then V's) -> attention -> o [B, H, T, d] -> y [B, T, C] = merge(o) W_o^T (W_o bf16
+ * [C, H d]). split / merge move between token rows and [B, heads, T, d] through the
+ * TMA tensor maps: no copy pass. Weight gradients are fp32; every other tensor is bf16
+ * with fp32 accumulation. Projections need d in {64, 128} (else ATTN_ERR_UNSUPPORTED),
+ * C a multiple of 8 (else ATTN_ERR_INVALID_ARG). Asynchronous on `stream`; pointers
+ * 16-byte aligned; the caller owns every buffer. Results are bitwise deterministic.
+ * ---------------------------------------------------------------------------------- */
+
+/* Layouts of attn_gemm. */
+#define ATTN_GEMM_NT 0 /* C [M, N] bf16 = A [M, K] . B [N, K]^T */
+#define ATTN_GEMM_NN 1 /* C [M, N] bf16 = A [M, K] . B [K, N] */
+#define ATTN_GEMM_TN 2 /* C [M, N] fp32 = A [K, M]^T . B [K, N] (split over K when M x N is small) */
+
+/* Bytes of workspace attn_gemm needs (the tn split-K partial sums; 0 for nt / nn, or
+ * when the tn product is not split, or for invalid sizes). */
+size_t attn_gemm_workspace_size(int M, int N, int K, int layout);
+
+/* A plain GEMM: row-major bf16 operands, M, N, K multiples of 8. C is bf16 for nt / nn
+ * and fp32 for tn. One launch (two when a tn product is split over K). */
+attn_status attn_gemm(const void* a, const void* b, void* c, int M, int N, int K, int layout, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* The rotation table of RoPE: tab fp32 [T][d/2][2] = (cos, sin) of t * 10000^(-2k/d),
+ * computed in fp64 and rounded. d a multiple of 8. One launch; make it once per (T, d). */
+attn_status attn_rope_table(float* tab, int T, int d, void* stream);
+
+/* y = RoPE(x) (inverse = 1: the rotation by the negative angle, i.e. the backward) for
+ * bf16 [B, H, T, d] tensors; y may be x. One launch. */
+attn_status attn_rope(const void* x, void* y, const float* rope_tab, int B, int H, int T, int d, int inverse,
+                      void* stream);
+
+/* Forward QKV projection: q, k, v = split(x W_qkv^T), and with rope_tab (non-null) q and k
+ * rotated in the GEMM's epilogue before rounding to bf16. One launch. */
+attn_status attn_qkv_proj(const void* x, const void* w_qkv, void* q, void* k, void* v, const float* rope_tab, int B,
+                          int T, int C, int H, int H_kv, int d, void* stream);
+
+/* Forward output projection: y = merge(o) W_o^T. One launch. */
+attn_status attn_out_proj(const void* o, const void* w_o, void* y, int B, int T, int H, int d, int C, void* stream);
+
+/* Bytes of workspace attn_out_proj_bwd and attn_qkv_proj_bwd need (either may use all of
+ * it; calls on one stream may share it). 0 for invalid sizes. */
+size_t attn_proj_bwd_workspace_size(int B, int T, int C, int H, int H_kv, int d);
+
+/* Backward of the output projection given dy [B, T, C]: d_o [B, H, T, d] = split(dy W_o)
+ * (nn) and dw_o fp32 [C, H d] = dy^T merge(o) (tn). Two or three launches. */
+attn_status attn_out_proj_bwd(const void* dy, const void* o, const void* w_o, void* d_o, float* dw_o, void* workspace,
+                              size_t workspace_bytes, int B, int T, int H, int d, int C, void* stream);
+
+/* Backward of the QKV projection given dq [B, H, T, d], dk, dv [B, H_kv, T, d] (the
+ * gradients of the tensors attn_qkv_proj wrote): with rope_tab, dq and dk are rotated
+ * back first (into the workspace); then dx [B, T, C] = merge(dq, dk, dv) W_qkv (nn) and
+ * dw_qkv fp32 [(H + 2 H_kv) d, C] = merge(dq, dk, dv)^T x (tn). Up to five launches. */
+attn_status attn_qkv_proj_bwd(const void* dq, const void* dk, const void* dv, const void* x, const void* w_qkv,
+                              const float* rope_tab, void* dx, float* dw_qkv, void* workspace, size_t workspace_bytes,
+                              int B, int T, int C, int H, int H_kv, int d, void* stream);
 
 #ifdef __cplusplus
 }

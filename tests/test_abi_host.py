@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for n in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_preprocess", "attn_bwd_dkdv",
-              "attn_bwd_dq", "attn_check_device_error", "attn_status_string", "attn_abi_version"):
+              "attn_bwd_dq", "attn_check_device_error", "attn_status_string", "attn_abi_version",
+              "attn_gemm", "attn_qkv_proj", "attn_out_proj", "attn_out_proj_bwd", "attn_qkv_proj_bwd"):
         assert n in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with attn.h"
 
@@ -41,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert lib.attn_abi_version() == 2
+    assert lib.attn_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -156,3 +157,72 @@ def test_gqa_workspace_size(lib):
     # the split count is bounded by the group size
     assert f(1, 2, 1, 128, 32) == base_ws(1, 2, 128) + 2 * 2 * 1 * 1 * 128 * 32 * 4
     assert f(1, 6, 4, 128, 64) == 0 and f(1, 6, 0, 128, 64) == 0
+
+
+# ---------------------------------------------------------------------------
+# projections
+# ---------------------------------------------------------------------------
+def _cp(x):
+    return ctypes.c_void_p(x)
+
+
+def gemm_call(lib, M=128, N=256, K=64, layout=0, ptrs=(P, P, P)):
+    return lib.attn_gemm(*[_cp(p) for p in ptrs], M, N, K, layout, _cp(0), 0, _cp(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=0), 1), (dict(N=-8), 1), (dict(K=0), 1), (dict(M=100), 1), (dict(K=12), 1), (dict(layout=3), 1),
+    (dict(layout=-1), 1), (dict(M=1 << 25), 1),
+    (dict(ptrs=(0, P, P)), 1), (dict(ptrs=(P, P, 0)), 1), (dict(ptrs=(P + 8, P, P)), 3), (dict(ptrs=(P, P + 4, P)), 3),
+])
+def test_gemm_rejects_invalid_calls(lib, kw, code):
+    assert gemm_call(lib, **kw) == code
+
+
+def test_gemm_workspace_size(lib):
+    f = lib.attn_gemm_workspace_size
+    assert f(1024, 1024, 8192, 0) == 0 and f(1024, 1024, 8192, 1) == 0  # nt / nn never split
+    # tn: 8 x 4 = 32 output tiles of 128 x 256 -> floor(152 / 32) = 4 splits of 32 K-steps of 64
+    assert f(1024, 1024, 8192, 2) == 4 * 1024 * 1024 * 4
+    # 24 x 4 = 96 tiles -> one split, no workspace
+    assert f(3072, 1024, 8192, 2) == 0
+    # at least 8 K-steps per split: K = 256 is 4 K-steps -> no split
+    assert f(128, 256, 256, 2) == 0
+    # at most 16 splits: one tile, K = 64 * 1024 -> 16 splits of 64 K-steps
+    assert f(128, 256, 65536, 2) == 16 * 128 * 256 * 4
+    # 152 / 1 = 152 -> capped at 16; K = 64 * 20 -> min(16, 20 // 8 = 2) = 2 splits of 10 K-steps
+    assert f(64, 64, 1280, 2) == 2 * 64 * 64 * 4
+    assert f(0, 64, 64, 2) == 0 and f(64, 64, 64, 3) == 0
+
+
+def test_proj_bwd_workspace_size(lib):
+    f = lib.attn_proj_bwd_workspace_size
+    # B4 T2048 C1024 H16 d64: dW_o is 1024 x 1024 over K = 8192 -> 4 splits (16 MiB); dW_qkv
+    # 3072 x 1024 -> no split; the rotated dQ, dK take 2 * 4 * 16 * 2048 * 64 * 2 bytes
+    rot = 2 * 4 * 16 * 2048 * 64 * 2
+    assert f(4, 2048, 1024, 16, 16, 64) == max(4 * 1024 * 1024 * 4, rot)
+    assert f(4, 2048, 1024, 16, 16, 32) == 0  # d must be 64 or 128
+    assert f(4, 2048, 1000, 16, 16, 64) > 0 and f(4, 2048, 1004, 16, 16, 64) == 0  # C % 8
+    assert f(1, 64, 64, 6, 4, 64) == 0  # H_kv must divide H
+
+
+def test_projections_reject_invalid_calls(lib):
+    ten = [_cp(P)] * 10
+    ok_sizes = (2, 64, 128, 2, 2, 64)  # B, T, C, H, H_kv, d
+    # qkv: (x, w, q, k, v, rope_tab, B, T, C, H, H_kv, d, stream)
+    assert lib.attn_qkv_proj(*ten[:5], _cp(0), 2, 64, 128, 2, 2, 32, _cp(0)) == 2  # d = 32
+    assert lib.attn_qkv_proj(*ten[:5], _cp(0), 2, 64, 100, 2, 2, 64, _cp(0)) == 1  # C % 8
+    assert lib.attn_qkv_proj(*ten[:5], _cp(0), 2, 64, 128, 4, 3, 64, _cp(0)) == 1  # H_kv
+    assert lib.attn_qkv_proj(_cp(0), *ten[:4], _cp(0), *ok_sizes, _cp(0)) == 1
+    assert lib.attn_qkv_proj(*ten[:5], _cp(P + 4), *ok_sizes, _cp(0)) == 3  # misaligned table
+    # out: (o, w_o, y, B, T, H, d, C, stream)
+    assert lib.attn_out_proj(*ten[:3], 2, 64, 2, 80, 128, _cp(0)) == 2
+    assert lib.attn_out_proj(*ten[:2], _cp(P + 2), 2, 64, 2, 64, 128, _cp(0)) == 3
+    # out bwd: (dy, o, w_o, d_o, dw_o, ws, ws_bytes, B, T, H, d, C, stream)
+    assert lib.attn_out_proj_bwd(*ten[:4], _cp(0), _cp(0), 0, 2, 64, 2, 64, 128, _cp(0)) == 1
+    # qkv bwd with RoPE needs the workspace for the rotated dQ, dK
+    assert lib.attn_qkv_proj_bwd(*ten[:5], _cp(P), _cp(P), _cp(P), _cp(0), 0, *ok_sizes, _cp(0)) == 4
+    # rope: (x, y, tab, B, H, T, d, inverse, stream)
+    assert lib.attn_rope(*ten[:3], 1, 1, 8, 12, 0, _cp(0)) == 1
+    assert lib.attn_rope(*ten[:3], 1, 1, 8, 64, 2, _cp(0)) == 1
+    assert lib.attn_rope_table(_cp(P), 8, 6, _cp(0)) == 1
