@@ -55,6 +55,9 @@ def parse():
                     help="the workload's shapes without the causal mask (credited FLOPs doubled)")
     ap.add_argument("--head-dim", type=int, default=0,
                     help="the workload's shapes at another head dimension (32, 64, 80 or 128)")
+    ap.add_argument("--block", action="store_true",
+                    help="the attention block's training step: QKV projection (RoPE) -> attention -> output "
+                         "projection, and the backward of all three (model width C = H d)")
     ap.add_argument("--fused-dq", action="store_true",
                     help="time the fused-dQ backward stages (d <= 64) instead of attn_bwd's kernels")
     return ap.parse_args()
@@ -472,7 +475,190 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
+    if args.block:
+        run_block(args, rank, world, local)
+        return
     run_ours(args, rank, world, local)
+
+
+BLOCK_STAGES = ("qkv_proj", "attn_fwd", "out_proj", "out_proj_bwd", "attn_bwd", "qkv_proj_bwd")
+
+
+def block_flops(B, H, H_kv, T, d, C, causal):
+    """Credited FLOPs per stage: the attention's (forward 2 B H T^2 d, backward 2.5x, causal
+    halves counted as in the attention line) and 2 M N K per GEMM."""
+    import oracle
+    fwd, bwd = oracle.credited_flops(B, H, T, d)
+    mul = 1.0 if causal else 2.0
+    n_qkv, tok = (H + 2 * H_kv) * d, B * T
+    return {"qkv_proj": 2.0 * tok * n_qkv * C, "attn_fwd": fwd * mul, "out_proj": 2.0 * tok * C * H * d,
+            "out_proj_bwd": 2 * 2.0 * tok * C * H * d, "attn_bwd": bwd * mul, "qkv_proj_bwd": 2 * 2.0 * tok * n_qkv * C}
+
+
+def run_block(args, rank, world, local):
+    """One training step of the attention block on the workload's shapes, every stage through
+    the C ABI: q, k, v = split(x W_qkv^T) with RoPE on q, k; o = attention(q, k, v); y =
+    merge(o) W_o^T; then dO, dW_o from dy; dQ, dK, dV from dO; dX, dW_qkv from those."""
+    import torch
+    import torch.distributed as dist
+    import causal_attention_gb300 as ca
+    import seeded_inputs as si
+    from tests.gpu_util import to_device
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = variant(si.WORKLOADS[args.workload], args)
+    wr = w.with_(seed=w.seed + 1000 * rank)
+    B, H, T, d = wr.shape
+    H_kv = args.kv_heads or H
+    C = H * d
+    scale, causal = wr.scale, wr.causal
+    dev = torch.device("cuda", local)
+    n_qkv = (H + 2 * H_kv) * d
+    # seeded inputs: activations N(0, 1), weights N(0, 0.02^2) (the pages' initialisation),
+    # upstream gradient N(0, sigma_do^2)
+    x_bits = si.normal_bf16_bits(wr.seed, 10, (B, T, C))
+    dy_bits = si.normal_bf16_bits(wr.seed, 11, (B, T, C), wr.sigma_do)
+    w_qkv = to_device(si.normal_bf16_bits(wr.seed, 12, (n_qkv, C), 0.02))
+    w_o = to_device(si.normal_bf16_bits(wr.seed, 13, (C, H * d), 0.02))
+    tab = ca.rope_table(T, d, dev)
+    n_sets = 2  # one step's tensors alone exceed L2; two sets alternate all the same
+
+    def new_set():
+        s = {"x": to_device(x_bits), "dy": to_device(dy_bits)}
+        s["q"] = torch.empty((B, H, T, d), dtype=torch.bfloat16, device=dev)
+        for n in ("k", "v", "dk", "dv"):
+            s[n] = torch.empty((B, H_kv, T, d), dtype=torch.bfloat16, device=dev)
+        for n in ("o", "do", "dq"):
+            s[n] = torch.empty_like(s["q"])
+        s["lse"] = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        s["y"], s["dx"] = torch.empty_like(s["x"]), torch.empty_like(s["x"])
+        s["dw_o"] = torch.empty((C, H * d), dtype=torch.float32, device=dev)
+        s["dw_qkv"] = torch.empty((n_qkv, C), dtype=torch.float32, device=dev)
+        s["ws"] = ca.new_workspace(B, H, T, d, dev, kv_heads=H_kv)
+        s["wsp"] = ca.new_proj_workspace(B, T, C, H, H_kv, d, dev)
+        return s
+    sets = [new_set() for _ in range(n_sets)]
+    stream = torch.cuda.current_stream()
+    launch = {
+        "qkv_proj": lambda s, st: ca.attn_qkv_proj(s["x"], w_qkv, s["q"], s["k"], s["v"], tab, st),
+        "attn_fwd": lambda s, st: ca.attn_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], scale, causal, st),
+        "out_proj": lambda s, st: ca.attn_out_proj(s["o"], w_o, s["y"], st),
+        "out_proj_bwd": lambda s, st: ca.attn_out_proj_bwd(s["dy"], s["o"], w_o, s["do"], s["dw_o"], s["wsp"], st),
+        "attn_bwd": lambda s, st: ca.attn_bwd(s["q"], s["k"], s["v"], s["o"], s["do"], s["lse"], s["dq"], s["dk"],
+                                              s["dv"], s["ws"], scale, causal, st),
+        "qkv_proj_bwd": lambda s, st: ca.attn_qkv_proj_bwd(s["dq"], s["dk"], s["dv"], s["x"], w_qkv, s["dx"],
+                                                           s["dw_qkv"], s["wsp"], tab, st),
+    }
+
+    def step(s, ev=None, st=stream):
+        for j, k in enumerate(BLOCK_STAGES):
+            if ev is not None:
+                ev[j].record(st)
+            launch[k](s, st)
+        if ev is not None:
+            ev[len(BLOCK_STAGES)].record(st)
+
+    for i in range(max(3, args.warmup)):
+        step(sets[i % n_sets])
+    ca.check_device_error(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(BLOCK_STAGES) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(sets[i % n_sets], evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ca.check_device_error(stream)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    mean_ms = {k: statistics.fmean(ev[j].elapsed_time(ev[j + 1]) for ev in evs) for j, k in enumerate(BLOCK_STAGES)}
+    flops = block_flops(B, H, H_kv, T, d, C, causal)
+    step_flops = sum(flops.values())
+    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+
+    # e2e: host buffers through the public API, every step copying x and dy in from pinned
+    # memory and y, dx, dW_qkv, dW_o out (one stream: copies, then the step)
+    x_h = torch.from_numpy(x_bits.view("int16")).view(torch.bfloat16).pin_memory()
+    dy_h = torch.from_numpy(dy_bits.view("int16")).view(torch.bfloat16).pin_memory()
+    outs = {n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in ("y", "dx", "dw_qkv", "dw_o")}
+    h2d = 2 * x_h.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def e2e_step(i):
+        s = sets[i % n_sets]
+        s["x"].copy_(x_h, non_blocking=True)
+        s["dy"].copy_(dy_h, non_blocking=True)
+        step(s)
+        for n, t in outs.items():
+            t.copy_(s[n], non_blocking=True)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    ca.check_device_error(stream)
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peak_tf, _, peak_kind = load_peaks()
+    stages = {k: {"ms": round(mean_ms[k], 5), "share": round(mean_ms[k] / sum(mean_ms.values()), 4),
+                  "tflops": round(flops[k] / (mean_ms[k] * 1e-3) / 1e12, 2)} for k in BLOCK_STAGES}
+    top = max(mean_ms, key=mean_ms.get)
+    achieved = flops[top] / (mean_ms[top] * 1e-3) / 1e12
+    # kernel launches per step: qkv 1; attention fwd 1; out 1; out bwd 2 (+1 split-K sum);
+    # attention bwd 2 (d <= 64) or 3 (+1 split dK/dV sum); qkv bwd 2 rotations + 2 (+1)
+    # (the projections' tn products take B * ceil(T / 64) K-steps of 64 tokens)
+    k_tok = B * ((T + 63) // 64) * 64
+    n_red_o = int(ca.attn_gemm_workspace_size(C, H * d, k_tok, "tn") > 0)
+    n_red_q = int(ca.attn_gemm_workspace_size(n_qkv, C, k_tok, "tn") > 0)
+    split_kv = H_kv != H and ca.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) > ca.attn_bwd_workspace_size(B, H, T, d)
+    launches = 1 + 1 + 1 + 2 + n_red_o + (2 if d <= 64 else 3) + int(split_kv) + 2 + 2 + n_red_q
+    line = {
+        "metric": "attention block training step TFLOP/s (bf16): QKV projection + RoPE, causal attention, "
+                  "output projection, forward and backward",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wr.name}_block", "B": B, "H": H, "H_kv": H_kv, "T": T, "d": d, "C": C,
+                   "causal": causal, "rope": True, "parallelism": f"replicas x{world}",
+                   "l2": f"one step's tensors exceed L2; {n_sets} sets alternate"},
+        "frac_of_peak": round(value / peak_tf, 4),
+        "stages": stages,
+        "roofline": {"bound": "tensor", "kernel": top, "achieved": round(achieved, 2), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": None,
+                     "peak_kind": f"bf16 dense burst, {peak_kind}"},
+        "cpu_baseline": None,
+        "e2e": {"value": round(step_flops * args.e2e_steps * world / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
