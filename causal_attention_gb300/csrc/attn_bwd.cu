@@ -716,6 +716,38 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       mbar_arrive(sm.dqs_full());
       }
     };
+    // ---- epilogue of item ri_e (work item u_e): dV, dK (x scale) out of the accumulators,
+    // then free them. In the persistent kernel (not split: its fp32 partials would spill
+    // there) it is deferred into the next item's first iteration (after that iteration's P
+    // is computed, before it is written), so that the wait for the item's last dK MMA
+    // overlaps that computation.
+    constexpr bool DEFER = SEP && !FUSE && !SPLIT;
+    auto epilogue = [&](int ri_e, int u_e) {
+      if (!(ok = mbar_wait_warp(sm.acc_full(), ri_e & 1, ab, kErrTimeoutElem))) return;
+      tc_fence_after();
+      const int bh_e = kv_slice(u_e), key = key_tile(u_e) * kTileRows + r;
+      const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)TL::ACC_COLS;
+      if constexpr (SPLIT) {
+        // fp32 partial sums of this split (unscaled), [S][key/value slice][T_pad][d] for dK
+        // then the same for dV; rows past T are written too and never read
+        const size_t off = (((size_t)(u_e % S) * BH + bh_e) * T_pad + key) * D;
+        store_acc_quarter_f32<D>(tDK, part + off, hc);
+        store_acc_quarter_f32<D>(tDV, part + (size_t)S * BH * T_pad * D + off, hc);
+      } else if constexpr (EPI) {
+        // into the staging tiles (free once the previous item's TMA stores have read them);
+        // warp 18 stores them once acc_free says every thread has written its part
+        if (ri_e > 0 && !(ok = mbar_wait_warp(sm.epi_free(), (ri_e - 1) & 1, ab, kErrTimeoutElem))) return;
+        stage_acc_quarter<D>(tDV, sEPI, r, hc, 1.f);  // (EPI: compile-time d <= 64)
+        stage_acc_quarter<D>(tDK, sEPI + TL::BYTES, r, hc, scale);
+        fence_proxy_async_smem();
+      } else {
+        store_acc_quarter<D>(tDV, dv + ((size_t)bh_e * T + key) * D, hc, 1.f, key < T);
+        store_acc_quarter<D>(tDK, dk + ((size_t)bh_e * T + key) * D, hc, scale, key < T);
+      }
+      tc_fence_before();
+      mbar_arrive(sm.acc_free());
+    };
+    int pend_ri = -1, pend_u = 0;  // an item whose epilogue is deferred (DEFER)
     int g = 0;
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
       const int kt = key_tile(u), bh = kv_slice(u), i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
@@ -760,6 +792,11 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
           uint32_t pp[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) pp[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+          if (DEFER && it == 0 && pend_ri >= 0) {
+            epilogue(pend_ri, pend_u);  // the previous item's dV, dK (warp 18 waits for them
+            pend_ri = -1;               // before this item's first dV MMA)
+            if (!ok) break;
+          }
           // the previous dV read the P^T columns: it must be complete before they are rewritten
           if (SEP && g > 0 && !(ok = mbar_wait_warp(sm.dv_done(), (g - 1) & 1, ab, kErrTimeoutElem))) break;
           tc_fence_after();
@@ -815,35 +852,16 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(sm.ds_full());
       }
-      // ---- epilogue: dV, dK (x scale) of this key tile; then free the accumulators
-      if (!ok || !(ok = mbar_wait_warp(sm.acc_full(), ri & 1, ab, kErrTimeoutElem))) break;
-      tc_fence_after();
-      const int key = kt * kTileRows + r;
-      const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)TL::ACC_COLS;
-      if constexpr (SPLIT) {
-        // fp32 partial sums of this split (unscaled), [S][key/value slice][T_pad][d] for dK
-        // then the same for dV; rows past T are written too and never read
-        const size_t off = (((size_t)(u % S) * BH + bh) * T_pad + key) * D;
-        store_acc_quarter_f32<D>(tDK, part + off, hc);
-        store_acc_quarter_f32<D>(tDV, part + (size_t)S * BH * T_pad * D + off, hc);
-        tc_fence_before();
-        mbar_arrive(sm.acc_free());
-      } else if constexpr (EPI) {
-        // into the staging tiles (free once the previous item's TMA stores have read them);
-        // warp 18 stores them once acc_free says every thread has written its part
-        if (ri > 0 && !(ok = mbar_wait_warp(sm.epi_free(), (ri - 1) & 1, ab, kErrTimeoutElem))) break;
-        stage_acc_quarter<D>(tDV, sEPI, r, hc, 1.f);  // (EPI: compile-time d <= 64)
-        stage_acc_quarter<D>(tDK, sEPI + TL::BYTES, r, hc, scale);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(sm.acc_free());
+      if (!ok) break;
+      if constexpr (DEFER) {
+        pend_ri = ri;
+        pend_u = u;
       } else {
-        store_acc_quarter<D>(tDV, dv + ((size_t)bh * T + key) * D, hc, 1.f, key < T);
-        store_acc_quarter<D>(tDK, dk + ((size_t)bh * T + key) * D, hc, scale, key < T);
-        tc_fence_before();
-        mbar_arrive(sm.acc_free());
+        epilogue(ri, u);
+        if (!ok) break;
       }
     }
+    if (DEFER && ok && pend_ri >= 0) epilogue(pend_ri, pend_u);  // the last item
     if (FUSE && ok && g > 0) dq_readout(g - 1);  // the last iteration's dQ_ij
   }
 
