@@ -9,7 +9,11 @@ conversion). Prints ONE JSON line (rank 0).
 
 * value: credited causal TFLOP/s of the whole job (forward 2*B*H*T^2*d, backward
   2.5x that), inputs resident in HBM; inputs rotate over several buffer sets whose
-  total size exceeds L2 three times, so no step reads another's operands from L2.
+  total size exceeds L2 three times, so no step reads another's operands from L2. The
+  K timed steps are launched as one CUDA graph (captured after the warm-up, replayed once
+  before the measurement; --eager launches them one by one). The per-kernel durations
+  (the roofline's) come from a second pass over the same K steps right after, launched
+  one by one with a CUDA event before and after every kernel.
 * e2e: the same metric through the public API with pinned host buffers: every step
   copies Q, K, V, dO host->device and O, LSE, dQ, dK, dV device->host; steps are
   pipelined over two device buffer sets and three streams, as a caller would run them.
@@ -58,6 +62,8 @@ def parse():
     ap.add_argument("--block", action="store_true",
                     help="the attention block's training step: QKV projection (RoPE) -> attention -> output "
                          "projection, and the backward of all three (model width C = H d)")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the timed steps one by one instead of replaying them as one CUDA graph")
     ap.add_argument("--fused-dq", action="store_true",
                     help="time the fused-dQ backward stages (d <= 64) instead of attn_bwd's kernels")
     return ap.parse_args()
@@ -237,6 +243,46 @@ def kernel_bytes(w):
     return {"bwd_preprocess": 2 * n * w.d * 2 + 4 * n + 8 * n, "bwd_dq_finish": n * w.d * (4 + 2)}
 
 
+def timed_steps(args, step, sets, n_events, stream):
+    """The K timed steps, measured twice back to back on `stream`:
+    1. throughput: the K steps captured as one CUDA graph (after the warm-up; replayed once
+       before the measurement) and replayed between two events, so the timed region holds
+       no host launch overhead (--eager: launched one by one instead);
+    2. per-kernel durations: the same K steps launched one by one with a timing event before
+       and after every kernel (events inside a graph would cost more than the launches).
+    Returns (elapsed ms of pass 1, the per-step event lists of pass 2, launch mode)."""
+    import torch
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph, mode = None, "eager"
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(args.steps):
+                    step(sets[i % len(sets)], None, stream)
+            with torch.cuda.stream(stream):
+                graph.replay()
+            torch.cuda.synchronize()
+            mode = "cuda graph of the K timed steps (per-kernel durations: an eager pass with events)"
+        except RuntimeError as e:
+            torch.cuda.synchronize()
+            graph, mode = None, f"eager (graph capture failed: {e})"
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)] for _ in range(args.steps)]
+    t0.record(stream)
+    if graph is not None:
+        with torch.cuda.stream(stream):
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            step(sets[i % len(sets)], evs[i], stream)
+    t1.record(stream)
+    if graph is not None:
+        for i in range(args.steps):
+            step(sets[i % len(sets)], evs[i], stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), evs, mode
+
+
 def run_ours(args, rank, world, local):
     import torch
     import torch.distributed as dist
@@ -282,7 +328,7 @@ def run_ours(args, rank, world, local):
         s["dq"], s["dk"], s["dv"] = torch.empty_like(s["q"]), torch.empty_like(s["k"]), torch.empty_like(s["v"])
         s["ws"] = ca.new_workspace(B, H, T, d, dev, fused_dq=fused, kv_heads=H_kv)
         sets.append(s)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)
 
     launch = {
         "fwd": lambda s: ca.attn_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], scale, causal, stream),
@@ -298,7 +344,7 @@ def run_ours(args, rank, world, local):
                                      s["ws"], scale, causal, stream),
     }
 
-    def step(s, ev=None):
+    def step(s, ev=None, st=None):
         # the stages attn_bwd runs, called one by one so that each can be timed
         for j, k in enumerate(KERNELS):
             if ev is not None:
@@ -311,7 +357,6 @@ def run_ours(args, rank, world, local):
         step(sets[i % n_sets])
     ca.check_device_error(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -319,18 +364,11 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(sets[i % n_sets], evs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms, evs, launch_mode = timed_steps(args, step, sets, len(KERNELS) + 1, stream)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ca.check_device_error(stream)
-    elapsed_ms = t_start.elapsed_time(t_end)
 
     per_kernel = {k: [] for k in KERNELS}
     for ev in evs:
@@ -453,7 +491,8 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wr.name, "B": B, "H": H, "H_kv": H_kv, "T": T, "d": d, "causal": causal,
-                   "parallelism": f"replicas x{world}", "l2": f"inputs rotate over {n_sets} sets ({n_sets * per_set / 2**20:.0f} MiB > L2)"},
+                   "parallelism": f"replicas x{world}", "l2": f"inputs rotate over {n_sets} sets ({n_sets * per_set / 2**20:.0f} MiB > L2)",
+                   "launch": launch_mode},
         "frac_of_peak": round(value / peak_tf, 4),
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
         "fwd_frac": round(fwd_tf / peak_tf, 4), "bwd_frac": round(bwd_tf / peak_tf, 4),
@@ -540,7 +579,7 @@ def run_block(args, rank, world, local):
         s["wsp"] = ca.new_proj_workspace(B, T, C, H, H_kv, d, dev)
         return s
     sets = [new_set() for _ in range(n_sets)]
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)
     launch = {
         "qkv_proj": lambda s, st: ca.attn_qkv_proj(s["x"], w_qkv, s["q"], s["k"], s["v"], tab, st),
         "attn_fwd": lambda s, st: ca.attn_fwd(s["q"], s["k"], s["v"], s["o"], s["lse"], scale, causal, st),
@@ -563,7 +602,6 @@ def run_block(args, rank, world, local):
     for i in range(max(3, args.warmup)):
         step(sets[i % n_sets])
     ca.check_device_error(stream)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(BLOCK_STAGES) + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -571,17 +609,11 @@ def run_block(args, rank, world, local):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(sets[i % n_sets], evs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms, evs, launch_mode = timed_steps(args, step, sets, len(BLOCK_STAGES) + 1, stream)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ca.check_device_error(stream)
-    elapsed_ms = t_start.elapsed_time(t_end)
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -601,11 +633,12 @@ def run_block(args, rank, world, local):
 
     def e2e_step(i):
         s = sets[i % n_sets]
-        s["x"].copy_(x_h, non_blocking=True)
-        s["dy"].copy_(dy_h, non_blocking=True)
-        step(s)
-        for n, t in outs.items():
-            t.copy_(s[n], non_blocking=True)
+        with torch.cuda.stream(stream):
+            s["x"].copy_(x_h, non_blocking=True)
+            s["dy"].copy_(dy_h, non_blocking=True)
+            step(s)
+            for n, t in outs.items():
+                t.copy_(s[n], non_blocking=True)
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -644,7 +677,7 @@ def run_block(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{wr.name}_block", "B": B, "H": H, "H_kv": H_kv, "T": T, "d": d, "C": C,
                    "causal": causal, "rope": True, "parallelism": f"replicas x{world}",
-                   "l2": f"one step's tensors exceed L2; {n_sets} sets alternate"},
+                   "l2": f"one step's tensors exceed L2; {n_sets} sets alternate", "launch": launch_mode},
         "frac_of_peak": round(value / peak_tf, 4),
         "stages": stages,
         "roofline": {"bound": "tensor", "kernel": top, "achieved": round(achieved, 2), "peak": peak_tf,

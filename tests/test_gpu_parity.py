@@ -326,3 +326,42 @@ def test_head_dim_80_at_gpt205m_shape():
     gu.assert_within_tolerance(err, w.name)
     for t in gpu.values():
         assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("name,kv_heads", [("gpt12m", None), ("gpt205m", None), ("gpt205m", 4), ("long8k", None)])
+def test_cuda_graph_capture_matches_eager(name, kv_heads):
+    """The C ABI is capturable into a CUDA graph (every launch goes to the caller's stream;
+    nothing synchronises or allocates): a replayed graph of attn_fwd + attn_bwd writes the
+    same bits as the eager calls, into buffers poisoned with NaN before the replay."""
+    import causal_attention_gb300 as ca
+    w = si.WORKLOADS[name]
+    x = si.make_inputs(w)
+    B, H, T, d = w.shape
+    H_kv = kv_heads or H
+    q = gu.to_device(x["q"])
+    k, v = gu.to_device(x["k"][:, :H_kv].copy()), gu.to_device(x["v"][:, :H_kv].copy())
+    do = gu.to_device(x["do"])
+    ws = ca.new_workspace(B, H, T, d, kv_heads=H_kv)
+    bufs = {"o": torch.empty_like(q), "lse": torch.empty((B, H, T), dtype=torch.float32, device="cuda"),
+            "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v)}
+    st = torch.cuda.Stream()
+
+    def step():
+        ca.attn_fwd(q, k, v, bufs["o"], bufs["lse"], w.scale, True, st)
+        ca.attn_bwd(q, k, v, bufs["o"], do, bufs["lse"], bufs["dq"], bufs["dk"], bufs["dv"], ws, w.scale, True, st)
+    with torch.cuda.stream(st):
+        step()
+    torch.cuda.synchronize()
+    ca.check_device_error()
+    eager = {n: t.clone() for n, t in bufs.items()}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        step()
+    for t in bufs.values():
+        t.fill_(float("nan"))
+    with torch.cuda.stream(st):
+        g.replay()
+    torch.cuda.synchronize()
+    ca.check_device_error()
+    for n in bufs:
+        assert torch.equal(bufs[n], eager[n]), n

@@ -197,3 +197,52 @@ def test_block_shapes_of_the_b4_t2048_workload():
     r_dx, r_dw = orc.qkv_projection_backward(dq64, dk64, dv64, x64, w64, use_rope=True)
     _check_bf16(dx, r_dx, "block dX", TOL_ROPE_BWD_REL_RMS)
     _check_f32(dw, r_dw, "block dW_qkv", TOL_ROPE_BWD_REL_RMS)
+
+
+def test_block_cuda_graph_matches_eager():
+    """The projection entry points are capturable into a CUDA graph too: QKV projection
+    with RoPE, attention, output projection and the backward of all three, replayed into
+    NaN-poisoned buffers, give the eager bits."""
+    import causal_attention_gb300 as ca
+    B, T, C, H, H_kv, d = 2, 300, 256, 4, 2, 64
+    x, _, w, _, w_o, _ = _proj_inputs(B, T, C, H, H_kv, d, 555)
+    dy, _ = _pair(556, 4, (B, T, C))
+    tab = ca.rope_table(T, d)
+    out = {"q": torch.empty((B, H, T, d), dtype=torch.bfloat16, device="cuda")}
+    for n in ("k", "v", "dk", "dv"):
+        out[n] = torch.empty((B, H_kv, T, d), dtype=torch.bfloat16, device="cuda")
+    for n in ("o", "do", "dq"):
+        out[n] = torch.empty_like(out["q"])
+    out["lse"] = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    out["y"], out["dx"] = torch.empty_like(x), torch.empty_like(x)
+    out["dw_o"] = torch.empty((C, H * d), dtype=torch.float32, device="cuda")
+    out["dw"] = torch.empty(tuple(w.shape), dtype=torch.float32, device="cuda")
+    ws = ca.new_workspace(B, H, T, d, kv_heads=H_kv)
+    wsp = ca.new_proj_workspace(B, T, C, H, H_kv, d)
+    scale = 1.0 / np.sqrt(d)
+    st = torch.cuda.Stream()
+
+    def step():
+        ca.attn_qkv_proj(x, w, out["q"], out["k"], out["v"], tab, st)
+        ca.attn_fwd(out["q"], out["k"], out["v"], out["o"], out["lse"], scale, True, st)
+        ca.attn_out_proj(out["o"], w_o, out["y"], st)
+        ca.attn_out_proj_bwd(dy, out["o"], w_o, out["do"], out["dw_o"], wsp, st)
+        ca.attn_bwd(out["q"], out["k"], out["v"], out["o"], out["do"], out["lse"], out["dq"], out["dk"], out["dv"], ws,
+                    scale, True, st)
+        ca.attn_qkv_proj_bwd(out["dq"], out["dk"], out["dv"], x, w, out["dx"], out["dw"], wsp, tab, st)
+    with torch.cuda.stream(st):
+        step()
+    torch.cuda.synchronize()
+    ca.check_device_error()
+    eager = {n: t.clone() for n, t in out.items()}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        step()
+    for t in out.values():
+        t.fill_(float("nan"))
+    with torch.cuda.stream(st):
+        g.replay()
+    torch.cuda.synchronize()
+    ca.check_device_error()
+    for n in out:
+        assert torch.equal(out[n], eager[n]), n
