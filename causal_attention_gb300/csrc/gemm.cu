@@ -238,25 +238,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         // bf16 tokens x features through the token view of C
         const int bi = mt / p.nT, t0 = (mt % p.nT) * kGM + 32 * eq, t = t0 + lane;
         const bool rows = t0 < p.T;
+        // RoPE: the (cos, sin) entries of this row for head columns cs_x .. cs_x + 63; every
+        // 64-column chunk of a head at that offset reuses them (at d = 64, all chunks)
+        float4 csv[16];
+        int cs_x = -1;
 #pragma unroll 1
         for (int j = 0; j < kGN / 64; ++j) {
           const int f = nt * kGN + 64 * j;
           if (f >= p.N) break;
+          int map, x, z;
+          view_coord(p.vc, f, map, x, z);
+          const bool rot = ROPE && f < p.rope_features;
+          if (rot && x != cs_x) {
+            // pairs (x + 2i, x + 2i + 1) of a head at position t: entries x/2 + i (issued
+            // before the accumulator loads, so that the two latencies overlap)
+            const float4* cs4 = reinterpret_cast<const float4*>(p.rope_tab) +
+                                (((size_t)min(t, p.T - 1) * p.rope_half + (x >> 1)) >> 1);
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) csv[i2] = __ldg(cs4 + i2);
+            cs_x = x;
+          }
           uint32_t v[64];
           tmem_ld32(tacc + 64u * j, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           tmem_ld32(tacc + 64u * j + 32u, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_wait_ld();
           if (!rows) continue;
-          int map, x, z;
-          view_coord(p.vc, f, map, x, z);
           uint32_t pk[32];
-          if (ROPE && f < p.rope_features) {
-            // pairs (x + 2i, x + 2i + 1) of head z at position t: (cos, sin) entries x/2 + i
-            const float4* cs4 = reinterpret_cast<const float4*>(p.rope_tab) +
-                                (((size_t)min(t, p.T - 1) * p.rope_half + (x >> 1)) >> 1);
+          if (rot) {
 #pragma unroll
             for (int i2 = 0; i2 < 16; ++i2) {
-              const float4 cs = __ldg(cs4 + i2);
+              const float4 cs = csv[i2];
               const float a0 = __uint_as_float(v[4 * i2]), b0 = __uint_as_float(v[4 * i2 + 1]);
               const float a1 = __uint_as_float(v[4 * i2 + 2]), b1 = __uint_as_float(v[4 * i2 + 3]);
               pk[2 * i2] = pack_bf16(a0 * cs.x - b0 * cs.y, a0 * cs.y + b0 * cs.x);
