@@ -366,17 +366,16 @@ attn_status head_view(CUtensorMap* maps, TokView* v, int Bn, int T, int d, int b
   return ATTN_OK;
 }
 
-constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
+constexpr int kGemmBM = 128, kGemmBK = 64;
 // tn products with fewer output tiles than this (the SMs of a GB300) are split over K so
-// that the persistent grid fills the device. A fixed count, not the device's, keeps the
-// result the same on every device.
+// that the persistent grid fills the device; the tile width is chosen against the same
+// count. A fixed count, not the device's, keeps the result the same on every device.
 constexpr int kGemmFillTiles = 152;
 
-// The split count of a tn product (M x N outputs, k_iters K-steps), and the K-steps of
-// each split: at most one split per whole multiple of the output tiles that fits in
-// kGemmFillTiles, at least 8 K-steps per split, at most 16 splits.
-int gemm_splits(int M, int N, int k_iters, int* k_per_split) {
-  const int tiles = ((M + kGemmBM - 1) / kGemmBM) * ((N + kGemmBN - 1) / kGemmBN);
+// The split count of a tn product with `tiles` output tiles and k_iters K-steps, and the
+// K-steps of each split: at most one split per whole multiple of the output tiles that
+// fits in kGemmFillTiles, at least 8 K-steps per split, at most 16 splits.
+int gemm_splits(int tiles, int k_iters, int* k_per_split) {
   int S = std::max(1, kGemmFillTiles / tiles);
   S = std::min(S, std::max(1, k_iters / 8));
   S = std::min(S, 16);
@@ -385,9 +384,35 @@ int gemm_splits(int M, int N, int k_iters, int* k_per_split) {
   return (k_iters + kps - 1) / kps;  // no empty split
 }
 
+// The output tile width of a product: 256 or 192 columns, whichever ends it in less
+// tile-time: (waves of kGemmFillTiles work items) x (K-steps per item) x (the tile's cost:
+// a 192-wide tile was measured at 0.9 of a 256-wide one, not 0.75); 256 on ties. For tn
+// the split count follows the width's tile count.
+int gemm_bn(int layout, int m_tiles, int N, int k_iters) {
+  long long best = -1;
+  int best_bn = 256;
+  for (int bn : {256, 192}) {
+    const long long tiles = (long long)m_tiles * ((N + bn - 1) / bn);
+    long long items = tiles, iters = k_iters;
+    if (layout == kGemmTN) {
+      int kps;
+      items = tiles * gemm_splits((int)std::min<long long>(tiles, INT_MAX), k_iters, &kps);
+      iters = kps;
+    }
+    const long long cost = (items + kGemmFillTiles - 1) / kGemmFillTiles * iters * (bn == 256 ? 10 : 9);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_bn = bn;
+    }
+  }
+  return best_bn;
+}
+
 size_t tn_workspace_bytes(int M, int N, int k_iters) {
+  const int m_tiles = (M + kGemmBM - 1) / kGemmBM;
+  const int bn = gemm_bn(kGemmTN, m_tiles, N, k_iters);
   int kps;
-  const int S = gemm_splits(M, N, k_iters, &kps);
+  const int S = gemm_splits(m_tiles * ((N + bn - 1) / bn), k_iters, &kps);
   return S > 1 ? (size_t)S * M * N * sizeof(float) : 0;
 }
 
@@ -399,18 +424,19 @@ attn_status gemm_params(GemmParams* p, int layout, int M, int N, int K, int T, i
   p->K = K;
   p->T = T;
   p->splits = 1;
-  p->n_tiles = (N + kGemmBN - 1) / kGemmBN;
   if (layout == kGemmTN) {
     p->nT = (T + kGemmBK - 1) / kGemmBK;  // 64-token K-steps per sequence
     p->m_tiles = (M + kGemmBM - 1) / kGemmBM;
     p->k_iters = Bn * p->nT;
-    p->splits = gemm_splits(M, N, p->k_iters, &p->k_per_split);
   } else {
     p->nT = (T + kGemmBM - 1) / kGemmBM;  // 128-token row tiles per sequence
     p->m_tiles = Bn * p->nT;
     p->k_iters = (K + kGemmBK - 1) / kGemmBK;
-    p->k_per_split = p->k_iters;
   }
+  p->bn = gemm_bn(layout, p->m_tiles, N, p->k_iters);
+  p->n_tiles = (N + p->bn - 1) / p->bn;
+  p->k_per_split = p->k_iters;
+  if (layout == kGemmTN) p->splits = gemm_splits(p->m_tiles * p->n_tiles, p->k_iters, &p->k_per_split);
   cudaError_t e;
   p->err = error_word_ptr(&e);
   if (!p->err) return cuda_fail(e, ATTN_ERR_CUDA);
@@ -739,7 +765,7 @@ attn_status attn_gemm(const void* a, const void* b, void* c, int M, int N, int K
   ATTN_TRY(gemm_params(&p, layout, M, N, K, M, 1, &sms));
   ATTN_TRY(plain_view(p.a, &p.va, a, 1, M, K, kGemmBM));
   if (layout == kGemmNT)
-    ATTN_TRY(mat_map(&p.b[0], b, K, N, 128));  // B [N, K]
+    ATTN_TRY(mat_map(&p.b[0], b, K, N, p.bn / 2));  // B [N, K]
   else
     ATTN_TRY(mat_map(&p.b[0], b, N, K, 64));  // B [K, N]
   ATTN_TRY(plain_view(p.c, &p.vc, c, 1, M, N, 32));
@@ -776,7 +802,7 @@ attn_status attn_qkv_proj(const void* x, const void* w_qkv, void* q, void* k, vo
   int sms = 0;
   ATTN_TRY(gemm_params(&p, kGemmNT, B * T, N, C, T, B, &sms));
   ATTN_TRY(plain_view(p.a, &p.va, x, B, T, C, kGemmBM));
-  ATTN_TRY(mat_map(&p.b[0], w_qkv, C, N, 128));
+  ATTN_TRY(mat_map(&p.b[0], w_qkv, C, N, p.bn / 2));
   ATTN_TRY(head_view(p.c, &p.vc, B, T, d, 32, q, H, k, v, H_kv));
   if (rope_tab) {
     p.rope_features = (H + H_kv) * d;  // q and k
@@ -793,7 +819,7 @@ attn_status attn_out_proj(const void* o, const void* w_o, void* y, int B, int T,
   int sms = 0;
   ATTN_TRY(gemm_params(&p, kGemmNT, B * T, C, H * d, T, B, &sms));
   ATTN_TRY(head_view(p.a, &p.va, B, T, d, kGemmBM, o, H));
-  ATTN_TRY(mat_map(&p.b[0], w_o, H * d, C, 128));
+  ATTN_TRY(mat_map(&p.b[0], w_o, H * d, C, p.bn / 2));
   ATTN_TRY(plain_view(p.c, &p.vc, y, B, T, C, 32));
   return launched(launch_gemm(kGemmNT, p, sms, static_cast<cudaStream_t>(stream)));
 }

@@ -10,12 +10,13 @@
 // can rotate q and k (RoPE, Forge RESEARCH.md section 7, model formulas) in fp32 before
 // rounding to bf16.
 //
-// Work item: a 128 x 256 output tile, accumulated over K-steps of 64 (one 128-byte
-// swizzle atom of bf16) through a 4-stage ring of 48 KB stages. Persistent: one CTA per
-// SM loops over the work items.
+// Work item: a 128 x 256 (or 128 x 192) output tile, accumulated over K-steps of 64 (one
+// 128-byte swizzle atom of bf16) through a ring of 48 KB (40 KB) stages; the host picks
+// the width that ends the product in fewer tile-times. Persistent: one CTA per SM loops
+// over the work items.
 //   warp 0      TMA producer
-//   warp 1      TMEM allocator (512 columns = two 256-column fp32 accumulators) and MMA
-//               issuer (M = 128, N = 256, K = 16 per instruction)
+//   warp 1      TMEM allocator (512 columns: two accumulators of up to 256 fp32 columns)
+//               and MMA issuer (M = 128, N = 256 or 192, K = 16 per instruction)
 //   warps 2-5   epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 of the
 //               finished accumulator, converts them, stages 32-row x 128-byte tiles in
 //               shared memory and writes them with TMA stores, while the MMAs of the next
@@ -33,19 +34,30 @@ namespace attn {
 
 namespace {
 
-constexpr int kGM = 128, kGN = 256, kGK = 64, kGST = 4;
+constexpr int kGM = 128, kGK = 64;
 constexpr int kGemmThreads = 192;
 constexpr int kGABytes = kGM * kGK * 2;  // 16 KB
-constexpr int kGBBytes = kGN * kGK * 2;  // 32 KB
-constexpr int kGStageBytes = kGABytes + kGBBytes;
 constexpr int kGChunk = kGK * 128;      // one MN-major chunk: 64 elements x 64 K-rows (8 KB)
 constexpr int kGEpiBytes = 32 * 128;    // one epilogue staging tile: 32 rows x 128 bytes
-constexpr int kGOffEpi = kGST * kGStageBytes;
-constexpr int kGOffBar = kGOffEpi + 4 * 2 * kGEpiBytes;
-constexpr int kGNBar = 2 * kGST + 5;
-constexpr int kGOffMisc = kGOffBar + kGNBar * 8;
-constexpr int kGemmSmem = kGOffMisc + 16 + 1024;  // + alignment slack
-static_assert(kGemmSmem <= 227 * 1024, "shared memory per CTA");
+
+// Shared-memory plan of an output tile width BN (256 or 192): the 256-wide tile has a
+// 4-stage ring of 48 KB stages and two staging tiles per epilogue warp; the 192-wide tile
+// (chosen where it gives fewer or fuller waves) a 5-stage ring of 40 KB stages and one.
+template <int BN>
+struct GemmTile {
+  static_assert(BN == 256 || BN == 192, "tile width");
+  static constexpr int ST = BN == 256 ? 4 : 5;
+  static constexpr int EPIBUF = BN == 256 ? 2 : 1;
+  static constexpr int B_BYTES = BN * kGK * 2;
+  static constexpr int STAGE = kGABytes + B_BYTES;
+  static constexpr int OFF_EPI = ST * STAGE;
+  static constexpr int OFF_BAR = OFF_EPI + 4 * EPIBUF * kGEpiBytes;
+  static constexpr int NBAR = 2 * ST + 5;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment slack
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+  static_assert(STAGE % 1024 == 0 && (B_BYTES / 2) % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+};
 
 // Which map holds feature f of a token view, and its (x, z) coordinates there.
 __device__ __forceinline__ void view_coord(const TokView& v, int f, int& map, int& x, int& z) {
@@ -63,21 +75,23 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return smem_desc<128
 __device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return smem_desc<128>(addr, kGChunk, 1024); }
 constexpr uint64_t kStepK = 32 >> 4, kStepMN = (16 * 128) >> 4;
 
-template <int LAYOUT, bool ROPE>
+template <int LAYOUT, bool ROPE, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool A_MN = LAYOUT == kGemmTN, B_MN = LAYOUT != kGemmNT;
+  using TC = GemmTile<BN>;
+  constexpr int kGN = BN, kGST = TC::ST, kGBBytes = TC::B_BYTES, kGStageBytes = TC::STAGE;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bar0 = base + kGOffBar;
+  const uint32_t bar0 = base + TC::OFF_BAR;
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kGST + s); };
   auto acc_full = [&](int b) { return bar0 + 8u * (2 * kGST + b); };
   auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kGST + 2 + b); };
   const uint32_t drain = bar0 + 8u * (2 * kGST + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kGOffMisc);
-  volatile int* abort = reinterpret_cast<volatile int*>(gbase + kGOffMisc + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + TC::OFF_MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + TC::OFF_MISC + 4);
   const Abort ab{abort, p.err};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -121,8 +135,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         int a_b = 0, a_t = 0, a_f = 0, a_map = 0, a_x = 0, a_z = 0;
         // TN: the token K-step (b, t0) and the MN chunks' coordinates (fixed)
         int k_b = 0, k_t = 0;
-        int am[2] = {0, 0}, ax[2] = {0, 0}, az[2] = {0, 0}, bm[4] = {0, 0, 0, 0}, bx[4] = {0, 0, 0, 0},
-            bz[4] = {0, 0, 0, 0};
+        int am[2] = {0, 0}, ax[2] = {0, 0}, az[2] = {0, 0};
+        int bm[kGN / 64], bx[kGN / 64], bz[kGN / 64];
         if constexpr (!A_MN) {
           a_b = mt / p.nT;
           a_t = (mt % p.nT) * kGM;
@@ -216,17 +230,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // ------------------------------------------------------------ epilogue
     const int eq = warp & 3;  // the TMEM lane quarter this warp may access
     const uint32_t lane_base = (uint32_t)(eq * 32) << 16;
-    const uint32_t stage0 = base + kGOffEpi + (uint32_t)eq * 2u * kGEpiBytes;
+    const uint32_t stage0 = base + TC::OFF_EPI + (uint32_t)eq * (uint32_t)(TC::EPIBUF * kGEpiBytes);
     const uint32_t srow = (uint32_t)lane * 128u;
     int cnt = 0;  // TMA stores this warp has issued (its two staging tiles alternate)
     bool ok = true;
-    // a staging tile may be rewritten once the store issued two stores ago has read it
+    // a staging tile may be rewritten once the store that last used it has read it
     auto take_buffer = [&]() {
-      if (cnt >= 2) {
-        if (lane == 0) bulk_wait_read<1>();
+      if (cnt >= TC::EPIBUF) {
+        if (lane == 0) bulk_wait_read<TC::EPIBUF - 1>();
         __syncwarp();
       }
-      return stage0 + (uint32_t)(cnt & 1) * kGEpiBytes;
+      return stage0 + (uint32_t)(cnt % TC::EPIBUF) * kGEpiBytes;
     };
     int r = 0;
     for (int u = blockIdx.x; ok && u < n_items; u += gridDim.x, ++r) {
@@ -396,15 +410,24 @@ int grid_for(long long work, int per_block, int num_sms) {
   return (int)(blocks < 1 ? 1 : blocks);
 }
 
-template <int LAYOUT, bool ROPE>
-cudaError_t launch_gemm_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
-  auto kern = gemm_kernel<LAYOUT, ROPE>;
+template <int LAYOUT, bool ROPE, int BN>
+cudaError_t launch_gemm_bn(const GemmParams& p, int num_sms, cudaStream_t stream) {
+  auto kern = gemm_kernel<LAYOUT, ROPE, BN>;
   static uint32_t configured = 0;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), kGemmSmem, &configured);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), GemmTile<BN>::SMEM, &configured);
   if (e != cudaSuccess) return e;
   const int n_items = p.m_tiles * p.n_tiles * p.splits;
-  kern<<<min(n_items, num_sms), kGemmThreads, kGemmSmem, stream>>>(p);
+  kern<<<min(n_items, num_sms), kGemmThreads, GemmTile<BN>::SMEM, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int LAYOUT, bool ROPE>
+cudaError_t launch_gemm_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
+  switch (p.bn) {
+    case 256: return launch_gemm_bn<LAYOUT, ROPE, 256>(p, num_sms, stream);
+    case 192: return launch_gemm_bn<LAYOUT, ROPE, 192>(p, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace

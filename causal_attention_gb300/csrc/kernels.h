@@ -83,7 +83,7 @@ struct TokView {
 struct GemmParams {
   CUtensorMap a[3];  // A: token view (NT / NN: K-major boxes of 64 features x 128 tokens;
                      // TN: MN-major boxes of 64 features x 64 tokens)
-  CUtensorMap b[3];  // B: NT a 2-D [N, K] map (64 x 128 boxes); NN a 2-D [K, N] map (64 x 64);
+  CUtensorMap b[3];  // B: NT a 2-D [N, K] map (64 x bn/2 boxes); NN a 2-D [K, N] map (64 x 64);
                      // TN a token view (64 features x 64 tokens)
   CUtensorMap c[3];  // C: NT / NN a token view (bf16 stores of 64 features x 32 tokens);
                      // TN a 3-D fp32 [S, M, N] map (stores of 32 x 32)
@@ -92,6 +92,7 @@ struct GemmParams {
   int T;              // tokens per sequence (the token dimension of the views)
   int nT;             // NT / NN: 128-token row tiles per sequence; TN: 64-token K-steps
   int m_tiles, n_tiles, k_iters, splits, k_per_split;
+  int bn;             // output tile width: 256 or 192 (NT: B boxes of bn / 2 rows)
   int rope_features;  // NT epilogue: features below this are rotated (RoPE), 0 for none
   int rope_half;      // d / 2: entries of one position's row of the rotation table
   const float* rope_tab;  // [T][d/2][2] fp32 (cos, sin), or null
