@@ -662,13 +662,13 @@ def run_block(args, rank, world, local):
     top = max(mean_ms, key=mean_ms.get)
     achieved = flops[top] / (mean_ms[top] * 1e-3) / 1e12
     # kernel launches per step: qkv 1; attention fwd 1; out 1; out bwd 2 (+1 split-K sum);
-    # attention bwd 2 (d <= 64) or 3 (+1 split dK/dV sum); qkv bwd 2 rotations + 2 (+1)
+    # attention bwd 2 (d <= 64) or 3 (+1 split dK/dV sum); qkv bwd 1 rotation (dQ and dK) + 2 (+1)
     # (the projections' tn products take B * ceil(T / 64) K-steps of 64 tokens)
     k_tok = B * ((T + 63) // 64) * 64
     n_red_o = int(ca.attn_gemm_workspace_size(C, H * d, k_tok, "tn") > 0)
     n_red_q = int(ca.attn_gemm_workspace_size(n_qkv, C, k_tok, "tn") > 0)
     split_kv = H_kv != H and ca.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) > ca.attn_bwd_workspace_size(B, H, T, d)
-    launches = 1 + 1 + 1 + 2 + n_red_o + (2 if d <= 64 else 3) + int(split_kv) + 2 + 2 + n_red_q
+    launches = 1 + 1 + 1 + 2 + n_red_o + (2 if d <= 64 else 3) + int(split_kv) + 1 + 2 + n_red_q
     line = {
         "metric": "attention block training step TFLOP/s (bf16): QKV projection + RoPE, causal attention, "
                   "output projection, forward and backward",

@@ -788,8 +788,8 @@ attn_status attn_rope(const void* x, void* y, const float* rope_tab, int B, int 
   cudaError_t e;
   const int sms = num_sms(&e);
   if (sms <= 0) return cuda_fail(e, ATTN_ERR_CUDA);
-  return launched(launch_rope_apply(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), rope_tab,
-                                    (long long)B * H * T, T, d, inverse, sms, static_cast<cudaStream_t>(stream)));
+  return launched(launch_rope_apply(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), H, nullptr,
+                                    nullptr, 0, rope_tab, B, T, d, inverse, sms, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status attn_qkv_proj(const void* x, const void* w_qkv, void* q, void* k, void* v, const float* rope_tab, int B,
@@ -866,8 +866,11 @@ attn_status attn_qkv_proj_bwd(const void* dq, const void* dk, const void* dv, co
     if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
     __nv_bfloat16* wq = static_cast<__nv_bfloat16*>(workspace);
     __nv_bfloat16* wk = wq + rq;
-    ATTN_TRY(attn_rope(dq, wq, rope_tab, B, H, T, d, 1, stream));
-    ATTN_TRY(attn_rope(dk, wk, rope_tab, B, H_kv, T, d, 1, stream));
+    cudaError_t e;
+    const int sms = num_sms(&e);
+    if (sms <= 0) return cuda_fail(e, ATTN_ERR_CUDA);
+    ATTN_TRY(launched(launch_rope_apply(static_cast<const __nv_bfloat16*>(dq), wq, H,
+                                        static_cast<const __nv_bfloat16*>(dk), wk, H_kv, rope_tab, B, T, d, 1, sms, s)));
     dq = wq;
     dk = wk;
   }

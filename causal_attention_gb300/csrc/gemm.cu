@@ -377,29 +377,53 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ ta
   }
 }
 
-// dst = src with each pair (2k, 2k+1) of a row at position t rotated by sgn * t theta_k;
-// one thread takes one 16-byte granule (four pairs)
-__global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                         const float4* __restrict__ tab, long long n_rows, int T,
-                                                         int d, float sgn) {
-  const int gpr = d / 8, half = d / 2;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_rows * gpr;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / gpr;
-    const int gi = (int)(i % gpr), t = (int)(row % T);
-    const uint4 in = src[i];
+// dst = src with each pair (2k, 2k+1) of a row at position t rotated by sgn * t theta_k,
+// for up to two [B, H_i, T, d] bf16 tensors. One thread takes one 16-byte granule (four
+// pairs) of one (b, t) in a group of four heads (of the two tensors' H0 + H1): the (cos,
+// sin) entries, shared by all heads at that position, are loaded once, and the four
+// granules are loaded before any is stored.
+__global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* __restrict__ src0, uint4* __restrict__ dst0,
+                                                         int H0, const uint4* __restrict__ src1,
+                                                         uint4* __restrict__ dst1, int H1,
+                                                         const float4* __restrict__ tab, int B, int T, int d,
+                                                         float sgn) {
+  constexpr int HG = 4;  // heads per thread
+  const int gpr = d / 8, half = d / 2, Ht = H0 + H1, n_hg = (Ht + HG - 1) / HG;
+  const long long n = (long long)B * n_hg * T * gpr;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    // i = ((b * n_hg + hg) * T + t) * gpr + gi: consecutive threads, consecutive granules
+    const int gi = (int)(i % gpr);
+    long long r = i / gpr;
+    const int t = (int)(r % T);
+    r /= T;
+    const int hg = (int)(r % n_hg), b = (int)(r / n_hg);
     const float4* cs4 = tab + (((size_t)t * half + 4 * gi) >> 1);
     const float4 c01 = __ldg(cs4), c23 = __ldg(cs4 + 1);
-    const float cs[8] = {c01.x, c01.y, c01.z, c01.w, c23.x, c23.y, c23.z, c23.w};
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    uint32_t o[4];
+    const float cs[8] = {c01.x, c01.y * sgn, c01.z, c01.w * sgn, c23.x, c23.y * sgn, c23.z, c23.w * sgn};
+    uint4 in[HG];
+    size_t gix[HG];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float a = __uint_as_float(w[q] << 16), b = __uint_as_float(w[q] & 0xFFFF0000u);
-      const float c = cs[2 * q], s = sgn * cs[2 * q + 1];
-      o[q] = pack_bf16(a * c - b * s, a * s + b * c);
+    for (int u = 0; u < HG; ++u) {
+      const int h = hg * HG + u;
+      if (h >= Ht) continue;
+      const bool first = h < H0;
+      gix[u] = (((size_t)b * (first ? H0 : H1) + (first ? h : h - H0)) * T + t) * gpr + gi;
+      in[u] = first ? src0[gix[u]] : src1[gix[u]];
     }
-    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+    for (int u = 0; u < HG; ++u) {
+      const int h = hg * HG + u;
+      if (h >= Ht) continue;
+      const uint32_t w[4] = {in[u].x, in[u].y, in[u].z, in[u].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = __uint_as_float(w[q] << 16), bb = __uint_as_float(w[q] & 0xFFFF0000u);
+        const float c = cs[2 * q], sn = cs[2 * q + 1];
+        o[q] = pack_bf16(a * c - bb * sn, a * sn + bb * c);
+      }
+      (h < H0 ? dst0 : dst1)[gix[u]] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -458,12 +482,13 @@ cudaError_t launch_rope_table(float* tab, int T, int d, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_rope_apply(const __nv_bfloat16* src, __nv_bfloat16* dst, const float* tab, long long n_rows,
-                              int T, int d, int inverse, int num_sms, cudaStream_t stream) {
-  const long long n = n_rows * (d / 8);
+cudaError_t launch_rope_apply(const __nv_bfloat16* src0, __nv_bfloat16* dst0, int H0, const __nv_bfloat16* src1,
+                              __nv_bfloat16* dst1, int H1, const float* tab, int B, int T, int d, int inverse,
+                              int num_sms, cudaStream_t stream) {
+  const long long n = (long long)B * ((H0 + H1 + 3) / 4) * T * (d / 8);
   rope_apply_kernel<<<grid_for(n, 256, num_sms), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), reinterpret_cast<const float4*>(tab), n_rows,
-      T, d, inverse ? -1.f : 1.f);
+      reinterpret_cast<const uint4*>(src0), reinterpret_cast<uint4*>(dst0), H0, reinterpret_cast<const uint4*>(src1),
+      reinterpret_cast<uint4*>(dst1), H1, reinterpret_cast<const float4*>(tab), B, T, d, inverse ? -1.f : 1.f);
   return cudaGetLastError();
 }
 

@@ -106,9 +106,11 @@ cudaError_t launch_splitk_reduce(const float* part, float* out, long long mn, in
                                  cudaStream_t stream);
 // tab[t][k] = (cos, sin)(t * 10000^(-2k/d)), computed in fp64 and rounded to fp32
 cudaError_t launch_rope_table(float* tab, int T, int d, cudaStream_t stream);
-// dst = rope(src) (inverse: the rotation by -t theta_k) over [n_rows / T sequences, T, d] bf16
-cudaError_t launch_rope_apply(const __nv_bfloat16* src, __nv_bfloat16* dst, const float* tab, long long n_rows,
-                              int T, int d, int inverse, int num_sms, cudaStream_t stream);
+// dst_i = rope(src_i) (inverse: the rotation by -t theta_k) for [B, H_i, T, d] bf16 tensors,
+// i = 0, 1 (H1 = 0: one tensor)
+cudaError_t launch_rope_apply(const __nv_bfloat16* src0, __nv_bfloat16* dst0, int H0, const __nv_bfloat16* src1,
+                              __nv_bfloat16* dst1, int H1, const float* tab, int B, int T, int d, int inverse,
+                              int num_sms, cudaStream_t stream);
 
 // Sets the max dynamic shared memory of a kernel once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask);

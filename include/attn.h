@@ -286,7 +286,7 @@ attn_status attn_out_proj_bwd(const void* dy, const void* o, const void* w_o, vo
 /* Backward of the QKV projection given dq [B, H, T, d], dk, dv [B, H_kv, T, d] (the
  * gradients of the tensors attn_qkv_proj wrote): with rope_tab, dq and dk are rotated
  * back first (into the workspace); then dx [B, T, C] = merge(dq, dk, dv) W_qkv (nn) and
- * dw_qkv fp32 [(H + 2 H_kv) d, C] = merge(dq, dk, dv)^T x (tn). Up to five launches. */
+ * dw_qkv fp32 [(H + 2 H_kv) d, C] = merge(dq, dk, dv)^T x (tn). Up to four launches. */
 attn_status attn_qkv_proj_bwd(const void* dq, const void* dk, const void* dv, const void* x, const void* w_qkv,
                               const float* rope_tab, void* dx, float* dw_qkv, void* workspace, size_t workspace_bytes,
                               int B, int T, int C, int H, int H_kv, int d, void* stream);
