@@ -231,6 +231,13 @@ def captured_traffic(workload, kernel):
     return rec["bytes_per_launch"]
 
 
+def spread(values_ms):
+    """min / median / p95 of per-launch durations (ms)."""
+    v = sorted(values_ms)
+    return {"ms_min": round(v[0], 5), "ms_median": round(statistics.median(v), 5),
+            "ms_p95": round(v[min(len(v) - 1, int(round(0.95 * (len(v) - 1))))], 5)}
+
+
 def kernel_flops(w):
     """Algorithmic FLOPs per launch of each kernel (causal half of every T x T GEMM)."""
     g = w.B * w.H * w.T * w.T * w.d * (1.0 if w.causal else 2.0)  # one causal GEMM = B*H*T^2*d
@@ -466,7 +473,7 @@ def run_ours(args, rank, world, local):
                 "peak_kind": f"bf16 dense burst, {peak_kind}"}
     kernels = {}
     for k in KERNELS:
-        e = {"ms": round(mean_ms[k], 5), "share": round(mean_ms[k] / sum(mean_ms.values()), 4)}
+        e = {"ms": round(mean_ms[k], 5), **spread(per_kernel[k]), "share": round(mean_ms[k] / sum(mean_ms.values()), 4)}
         if k in kf:
             tf = kf[k] / (mean_ms[k] * 1e-3) / 1e12
             e.update(tflops=round(tf, 2), frac=round(tf / peak_tf, 4))
@@ -618,7 +625,8 @@ def run_block(args, rank, world, local):
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    mean_ms = {k: statistics.fmean(ev[j].elapsed_time(ev[j + 1]) for ev in evs) for j, k in enumerate(BLOCK_STAGES)}
+    per_stage = {k: [ev[j].elapsed_time(ev[j + 1]) for ev in evs] for j, k in enumerate(BLOCK_STAGES)}
+    mean_ms = {k: statistics.fmean(v) for k, v in per_stage.items()}
     flops = block_flops(B, H, H_kv, T, d, C, causal)
     step_flops = sum(flops.values())
     value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
@@ -657,7 +665,7 @@ def run_block(args, rank, world, local):
         return
 
     peak_tf, _, peak_kind = load_peaks()
-    stages = {k: {"ms": round(mean_ms[k], 5), "share": round(mean_ms[k] / sum(mean_ms.values()), 4),
+    stages = {k: {"ms": round(mean_ms[k], 5), **spread(per_stage[k]), "share": round(mean_ms[k] / sum(mean_ms.values()), 4),
                   "tflops": round(flops[k] / (mean_ms[k] * 1e-3) / 1e12, 2)} for k in BLOCK_STAGES}
     top = max(mean_ms, key=mean_ms.get)
     achieved = flops[top] / (mean_ms[top] * 1e-3) / 1e12
