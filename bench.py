@@ -231,6 +231,30 @@ def captured_traffic(workload, kernel):
     return rec["bytes_per_launch"]
 
 
+def replica(w, rank):
+    """The workload of one rank: its own replica (same shapes, seed offset by 1000 per rank),
+    so that the ranks solve independent problems (no collective on the data path)."""
+    return w.with_(seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(value, device=None):
+    """The largest value over all ranks (the job ends with its slowest rank); the value
+    itself on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step, steps, world, seconds):
+    """Throughput of the whole job: every rank ran `steps` steps of `flops_per_step` within
+    `seconds` (the slowest rank's time)."""
+    return flops_per_step * steps * world / seconds / 1e12
+
+
 def spread(values_ms):
     """min / median / p95 of per-launch durations (ms)."""
     v = sorted(values_ms)
@@ -303,7 +327,7 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = variant(si.WORKLOADS[args.workload], args)
     # each rank: its own replica of the workload (different seed, same shape)
-    wr = w.with_(seed=w.seed + 1000 * rank)
+    wr = replica(w, rank)
     x = si.make_inputs(wr)
     B, H, T, d = wr.shape
     scale, causal = wr.scale, wr.causal
@@ -383,14 +407,10 @@ def run_ours(args, rank, world, local):
             per_kernel[k].append(ev[j].elapsed_time(ev[j + 1]))
     mean_ms = {k: statistics.fmean(v) for k, v in per_kernel.items()}
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     fwd_f, bwd_f = oracle.credited_flops(B, H, T, d)
     step_flops = (fwd_f + bwd_f) * (1.0 if causal else 2.0)
-    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, world, elapsed_ms * 1e-3)
 
     # ------------------------------------------------------------------ e2e
     # The public API with host buffers: every step copies its inputs in from pinned host
@@ -450,13 +470,9 @@ def run_ours(args, rank, world, local):
     for i in range(args.e2e_steps):
         e2e_step(i)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     ca.check_device_error(stream)
-    e2e_value = step_flops * args.e2e_steps * world / e2e_s / 1e12
+    e2e_value = whole_job_tflops(step_flops, args.e2e_steps, world, e2e_s)
 
     if rank != 0:
         dist.destroy_process_group()
@@ -555,7 +571,7 @@ def run_block(args, rank, world, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = variant(si.WORKLOADS[args.workload], args)
-    wr = w.with_(seed=w.seed + 1000 * rank)
+    wr = replica(w, rank)
     B, H, T, d = wr.shape
     H_kv = args.kv_heads or H
     C = H * d
@@ -621,15 +637,12 @@ def run_block(args, rank, world, local):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ca.check_device_error(stream)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     per_stage = {k: [ev[j].elapsed_time(ev[j + 1]) for ev in evs] for j, k in enumerate(BLOCK_STAGES)}
     mean_ms = {k: statistics.fmean(v) for k, v in per_stage.items()}
     flops = block_flops(B, H, H_kv, T, d, C, causal)
     step_flops = sum(flops.values())
-    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, world, elapsed_ms * 1e-3)
 
     # e2e: host buffers through the public API, every step copying x and dy in from pinned
     # memory and y, dx, dW_qkv, dW_o out (one stream: copies, then the step)
@@ -654,11 +667,7 @@ def run_block(args, rank, world, local):
     for i in range(args.e2e_steps):
         e2e_step(i)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     ca.check_device_error(stream)
     if rank != 0:
         dist.destroy_process_group()
@@ -692,7 +701,7 @@ def run_block(args, rank, world, local):
                      "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": None,
                      "peak_kind": f"bf16 dense burst, {peak_kind}"},
         "cpu_baseline": None,
-        "e2e": {"value": round(step_flops * args.e2e_steps * world / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(step_flops, args.e2e_steps, world, e2e_s), 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
