@@ -96,6 +96,8 @@ PROJ = [
     # (B, T, C, H, H_kv, d, rope)
     (2, 300, 256, 4, 4, 64, False), (2, 300, 256, 4, 2, 64, True), (1, 129, 128, 2, 1, 128, True),
     (3, 64, 192, 2, 2, 64, True), (1, 1000, 512, 8, 2, 64, False),
+    # one token per sequence (every token tile and K-step is one row); one head, d = 128
+    (3, 1, 64, 1, 1, 64, True), (2, 77, 136, 1, 1, 128, True),
 ]
 
 
