@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
   constexpr int NG = D / 8;                             // 16-byte granules per row
   constexpr int TPR = (NG & (NG - 1)) == 0 ? NG : 8;    // threads per row (a power of two)
   constexpr int RPW = 32 / TPR;                         // rows per warp step
+  griddep_begin();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_cnt; i += gridDim.x * blockDim.x) dq_cnt[i] = 0;
   const int lane = threadIdx.x & 31;
   const int sub = lane % TPR;
@@ -228,6 +229,7 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_begin();  // the inputs may come from the previous kernel in the stream
   return s;
 }
 
@@ -1171,6 +1173,7 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_finish_kernel(const float* __
                                                                  __nv_bfloat16* __restrict__ dq, int T, int T_pad,
                                                                  int BH, float scale) {
   constexpr int C8 = D / 8;
+  griddep_begin();
   const int n_q = T_pad / kTileRows;
   const long long total = (long long)BH * T_pad * C8;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -1202,6 +1205,7 @@ __global__ void __launch_bounds__(256) attn_bwd_dkdv_reduce_kernel(const float* 
                                                                    __nv_bfloat16* __restrict__ dv, int T, int T_pad,
                                                                    int BHkv, int S, float scale) {
   constexpr int C8 = D / 8;  // 8 columns (two float4) per thread
+  griddep_begin();
   const long long rows = (long long)BHkv * T;
   const size_t plane = (size_t)BHkv * T_pad * D;  // one split's partial sums
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < rows * C8;
@@ -1247,9 +1251,8 @@ cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
   const long long cap = (long long)a.num_sms * 8;  // grid-stride beyond 8 blocks per SM
   if (blocks > cap) blocks = cap;
   const int n_cnt = a.dq_cnt ? a.BH * (a.T_pad / kTileRows) : 0;
-  attn_bwd_preprocess_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.o, a.dO, a.lse, a.ws_nlse2, a.ws_D,
-                                                                      a.dq_cnt, n_cnt, a.T, a.T_pad, a.BH);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_preprocess_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, stream, a.o, a.dO, a.lse,
+                    a.ws_nlse2, a.ws_D, a.dq_cnt, n_cnt, a.T, a.T_pad, a.BH);
 }
 
 template <int D, bool CAUSAL, bool FUSE, bool SPLIT = false>
@@ -1265,11 +1268,9 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
   const int grid = C::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
   if (EPI && (!a.tmdK || !a.tmdV)) return cudaErrorInvalidValue;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, EPI ? *a.tmdK : *a.tmQ,
-                                                     EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk,
-                                                     a.dv, a.dq_acc, a.dq_cnt, a.part, a.T, a.T_pad, a.BH / a.G, a.G,
-                                                     a.S, a.scale, a.scale * kLog2e, a.err);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
+                    EPI ? *a.tmdK : *a.tmQ, EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.dq_acc,
+                    a.dq_cnt, a.part, a.T, a.T_pad, a.BH / a.G, a.G, a.S, a.scale, a.scale * kLog2e, a.err);
 }
 
 template <int D>
@@ -1278,8 +1279,8 @@ cudaError_t launch_dq_finish(const BwdArgs& a, cudaStream_t stream) {
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)a.num_sms * 8;
   if (blocks > cap) blocks = cap;
-  attn_bwd_dq_finish_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.dq_acc, a.dq, a.T, a.T_pad, a.BH, a.scale);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_dq_finish_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, stream, a.dq_acc, a.dq, a.T,
+                    a.T_pad, a.BH, a.scale);
 }
 
 template <int D, bool CAUSAL>
@@ -1293,10 +1294,9 @@ cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (PRE && (!a.tmO || !a.lse)) return cudaErrorInvalidValue;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
-  kern<<<min(n_items, a.num_sms), kBwdThreads, C::SMEM_BYTES, stream>>>(
-      *a.tmQ, *a.tmK, *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH,
-      a.G, a.scale, a.scale * kLog2e, a.err);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(kBwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
+                    *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.G,
+                    a.scale, a.scale * kLog2e, a.err);
 }
 
 }  // namespace
@@ -1317,9 +1317,8 @@ cudaError_t launch_dkdv_reduce(const BwdArgs& a, cudaStream_t stream) {
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)a.num_sms * 8;
   if (blocks > cap) blocks = cap;
-  attn_bwd_dkdv_reduce_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(a.part, a.dk, a.dv, a.T, a.T_pad,
-                                                                       a.BH / a.G, a.S, a.scale);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_dkdv_reduce_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, stream, a.part, a.dk, a.dv,
+                    a.T, a.T_pad, a.BH / a.G, a.S, a.scale);
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t stream) {

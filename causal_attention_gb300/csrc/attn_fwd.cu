@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_begin();  // the inputs may come from the previous kernel in the stream
 
   constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
   constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
@@ -505,9 +506,8 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t stream) {
   const int n_items = n_pairs * a.BH;
   // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
   const int grid = C::SEP_P ? min(n_items, a.num_sms) : n_items;
-  kern<<<grid, kFwdThreads, C::SMEM_BYTES, stream>>>(*a.tmQ, *a.tmK, *a.tmV, a.o, a.lse, a.T, a.BH, a.G, n_pairs,
-                                                      a.scale, a.scale * 1.4426950408889634f, a.err);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kFwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, a.o, a.lse,
+                    a.T, a.BH, a.G, n_pairs, a.scale, a.scale * 1.4426950408889634f, a.err);
 }
 
 }  // namespace

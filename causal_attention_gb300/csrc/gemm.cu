@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_begin();  // the operands may come from the previous kernel in the stream
 
   // work item u: K range u % splits, output tile u / splits (n tiles fastest, so that
   // neighbouring CTAs share the A rows)
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 // out = sum over s of part[s] (fp32, added in split order), 4 values per thread
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __restrict__ part, float4* __restrict__ out,
                                                             long long mn4, int splits) {
+  griddep_begin();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < mn4;
        i += (long long)gridDim.x * blockDim.x) {
     float4 a = part[i];
@@ -366,6 +368,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
 
 // tab[t][k] = (cos, sin) of t * 10000^(-2k/d), in fp64, rounded to fp32
 __global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ tab, int T, int d) {
+  griddep_begin();
   const int half = d / 2;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)T * half;
        i += (long long)gridDim.x * blockDim.x) {
@@ -388,6 +391,7 @@ __global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* __restrict
                                                          const float4* __restrict__ tab, int B, int T, int d,
                                                          float sgn) {
   constexpr int HG = 4;  // heads per thread
+  griddep_begin();
   const int gpr = d / 8, half = d / 2, Ht = H0 + H1, n_hg = (Ht + HG - 1) / HG;
   const long long n = (long long)B * n_hg * T * gpr;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -441,8 +445,7 @@ cudaError_t launch_gemm_bn(const GemmParams& p, int num_sms, cudaStream_t stream
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), GemmTile<BN>::SMEM, &configured);
   if (e != cudaSuccess) return e;
   const int n_items = p.m_tiles * p.n_tiles * p.splits;
-  kern<<<min(n_items, num_sms), kGemmThreads, GemmTile<BN>::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(min(n_items, num_sms)), dim3(kGemmThreads), GemmTile<BN>::SMEM, stream, p);
 }
 
 template <int LAYOUT, bool ROPE>
@@ -471,25 +474,24 @@ cudaError_t launch_gemm(int layout, const GemmParams& p, int num_sms, cudaStream
 cudaError_t launch_splitk_reduce(const float* part, float* out, long long mn, int splits, int num_sms,
                                  cudaStream_t stream) {
   const long long mn4 = mn / 4;
-  splitk_reduce_kernel<<<grid_for(mn4, 256, num_sms), 256, 0, stream>>>(reinterpret_cast<const float4*>(part),
-                                                                       reinterpret_cast<float4*>(out), mn4, splits);
-  return cudaGetLastError();
+  return launch_pdl(splitk_reduce_kernel, dim3(grid_for(mn4, 256, num_sms)), dim3(256), 0, stream,
+                    reinterpret_cast<const float4*>(part), reinterpret_cast<float4*>(out), mn4, splits);
 }
 
 cudaError_t launch_rope_table(float* tab, int T, int d, cudaStream_t stream) {
   const long long n = (long long)T * (d / 2);
-  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(reinterpret_cast<float2*>(tab), T, d);
-  return cudaGetLastError();
+  return launch_pdl(rope_table_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream,
+                    reinterpret_cast<float2*>(tab), T, d);
 }
 
 cudaError_t launch_rope_apply(const __nv_bfloat16* src0, __nv_bfloat16* dst0, int H0, const __nv_bfloat16* src1,
                               __nv_bfloat16* dst1, int H1, const float* tab, int B, int T, int d, int inverse,
                               int num_sms, cudaStream_t stream) {
   const long long n = (long long)B * ((H0 + H1 + 3) / 4) * T * (d / 8);
-  rope_apply_kernel<<<grid_for(n, 256, num_sms), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(src0), reinterpret_cast<uint4*>(dst0), H0, reinterpret_cast<const uint4*>(src1),
-      reinterpret_cast<uint4*>(dst1), H1, reinterpret_cast<const float4*>(tab), B, T, d, inverse ? -1.f : 1.f);
-  return cudaGetLastError();
+  return launch_pdl(rope_apply_kernel, dim3(grid_for(n, 256, num_sms)), dim3(256), 0, stream,
+                    reinterpret_cast<const uint4*>(src0), reinterpret_cast<uint4*>(dst0), H0,
+                    reinterpret_cast<const uint4*>(src1), reinterpret_cast<uint4*>(dst1), H1,
+                    reinterpret_cast<const float4*>(tab), B, T, d, inverse ? -1.f : 1.f);
 }
 
 }  // namespace attn

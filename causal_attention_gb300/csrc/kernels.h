@@ -112,6 +112,25 @@ cudaError_t launch_rope_apply(const __nv_bfloat16* src0, __nv_bfloat16* dst0, in
                               __nv_bfloat16* dst1, int H1, const float* tab, int B, int T, int d, int inverse,
                               int num_sms, cudaStream_t stream);
 
+// Launches a kernel with programmatic stream serialization: its CTAs may be scheduled
+// while the previous kernel in the stream drains; every kernel of the library waits for
+// the previous kernels (griddep_begin) before its first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Sets the max dynamic shared memory of a kernel once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask);
 

@@ -438,6 +438,21 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization
+// may start while the previous kernel in the stream is still running: it waits here,
+// after its prologue (barriers, tensor memory, descriptor prefetch) and before its first
+// global-memory access, until the previous kernels have completed and their writes are
+// visible; and it lets the next kernel be scheduled as soon as SMs free up. Without a
+// programmatic dependency both are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_begin() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
