@@ -191,6 +191,7 @@ def run_reference(args, rank, world):
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": f"{heads_per_step} head of {w.B * w.H} per step, fp64 numpy oracle"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "provenance": provenance(w.seed),
     }
     print(json.dumps(line), flush=True)
 
@@ -229,6 +230,28 @@ def captured_traffic(workload, kernel):
     if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_prefix"]:
         return None
     return rec["bytes_per_launch"]
+
+
+def provenance(seed, device=None):
+    """What produced a line: the sha256 of the library's sources, the GPU, the software
+    versions, the seed of the inputs and the host cores."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    srcs = sorted(glob.glob(os.path.join(ROOT, "causal_attention_gb300", "csrc", "*"))) + [
+        os.path.join(ROOT, "include", "attn.h")]
+    for f in srcs:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    out = {"source_sha256": h.hexdigest()[:16], "seed": seed, "host_cores": os.cpu_count()}
+    try:
+        import torch
+        out.update(torch=torch.__version__, cuda=torch.version.cuda)
+        if device is not None and torch.cuda.is_available():
+            out["gpu"] = torch.cuda.get_device_name(device)
+    except ImportError:
+        pass
+    return out
 
 
 def replica(w, rank):
@@ -525,6 +548,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "provenance": provenance(wr.seed, dev),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -705,6 +729,7 @@ def run_block(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
+        "provenance": provenance(wr.seed, dev),
     }
     print(json.dumps(line), flush=True)
     if world > 1:

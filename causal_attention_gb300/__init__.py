@@ -150,6 +150,12 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=True, stream
                                  _stream_handle(stream)), "attn_bwd_noalloc")
 
 
+def selftest_wait_timeout(stream=None):
+    """Launches the bounded-wait self-test (see attn.h); the next check_device_error on the
+    stream raises AttnError with ATTN_ERR_DEVICE_TIMEOUT."""
+    _check(_dll.attn_selftest_wait_timeout(_stream_handle(stream)), "attn_selftest_wait_timeout")
+
+
 def check_device_error(stream=None):
     """Synchronises the stream and raises AttnError if a kernel's bounded wait expired."""
     _check(_dll.attn_check_device_error(_stream_handle(stream)), "attn_check_device_error")

@@ -47,6 +47,7 @@ SIGNATURES = {
     "attn_bwd_dq_finish": (_I, [_P, _P, _S, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "attn_check_device_error": (_I, [_P]),
+    "attn_selftest_wait_timeout": (_I, [_P]),
     "attn_gemm_workspace_size": (_S, [_I, _I, _I, _I]),
     "attn_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
     "attn_rope_table": (_I, [_P, _I, _I, _P]),

@@ -9,12 +9,29 @@
 
 #include "attn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace attn {
 
 // Written by kernels whose bounded waits expire; read and cleared by
 // attn_check_device_error. Kernels receive its device address as a parameter.
 __device__ uint32_t g_error_word = 0;
+
+// Self-test of the bounded waits: one warp waits, through the same wait the kernels use,
+// on an mbarrier that nothing ever arrives on. The wait runs out after its time limit,
+// records the failure in the error word and returns; nothing faults or hangs.
+__global__ void wait_timeout_selftest_kernel(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const Abort ab{&abort_flag, err};
+  mbar_wait_warp(smem_u32(&bar), 0, ab, kErrTimeoutElem);
+}
 
 namespace {
 
@@ -733,6 +750,14 @@ const char* attn_status_string(attn_status status) {
 }
 
 const char* attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+attn_status attn_selftest_wait_timeout(void* stream) {
+  cudaError_t e;
+  uint32_t* err = error_word_ptr(&e);
+  if (!err) return cuda_fail(e, ATTN_ERR_CUDA);
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err);
+  return launched(cudaGetLastError());
+}
 
 // ---------------------------------------------------------------------------
 // Projections

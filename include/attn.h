@@ -222,6 +222,13 @@ const char* attn_status_string(attn_status status);
 /* Text of the last CUDA error seen by this thread inside the library ("" if none). */
 const char* attn_last_cuda_error(void);
 
+/* Self-test of the failure path: launches one warp that waits, through the kernels' own
+ * bounded wait, on a barrier that nothing arrives on. After the wait's time limit (2 s)
+ * it records the expiry in the device error word and returns, so that the next
+ * attn_check_device_error on the stream reports ATTN_ERR_DEVICE_TIMEOUT (and clears the
+ * word) and the context stays usable. Nothing faults, traps or hangs. One launch. */
+attn_status attn_selftest_wait_timeout(void* stream);
+
 /* ------------------------------------------------------------------------------------
  * Projections around the attention: the training GEMMs of the attention block.
  *

@@ -365,3 +365,53 @@ def test_cuda_graph_capture_matches_eager(name, kv_heads):
     ca.check_device_error()
     for n in bufs:
         assert torch.equal(bufs[n], eager[n]), n
+
+
+def test_bounded_wait_timeout_is_reported_and_the_context_survives():
+    """A wait that runs out (a barrier nothing arrives on, through the kernels' own bounded
+    wait) is reported as ATTN_ERR_DEVICE_TIMEOUT by the next check, the report clears the
+    error word, and the context keeps working: a forward + backward still matches the oracle."""
+    import time
+    import causal_attention_gb300 as ca
+    ca.check_device_error()
+    t0 = time.perf_counter()
+    ca.selftest_wait_timeout()
+    with pytest.raises(ca.AttnError) as info:
+        ca.check_device_error()
+    assert info.value.status == 6, info.value  # ATTN_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 >= 1.5  # it waited for its time limit (2 s) first
+    ca.check_device_error()  # cleared
+    w = si.WORKLOADS["tiny"]
+    x = si.make_inputs(w)
+    gu.assert_within_tolerance(gu.compare(gu.run_gpu(w, x), gu.run_oracle(w, x)), "after timeout")
+
+
+def test_bitwise_determinism_under_concurrent_load():
+    """300 forward + backward launches on one stream while another stream keeps the GPU
+    busy with large matmuls: every launch gives the same bits as a quiet run (the kernels
+    have no cross-CTA ordering, so how many CTAs run at once does not matter)."""
+    import causal_attention_gb300 as ca
+    w = si.WORKLOADS["gpt100m"].with_(B=2, H=4, T=640)
+    x = si.make_inputs(w)
+    q, k, v, do = (gu.to_device(x[n]) for n in ("q", "k", "v", "do"))
+    ref = gu.run_gpu(w, x)
+    ws = ca.new_workspace(*w.shape)
+    out = {"o": torch.empty_like(q), "lse": torch.empty(w.shape[:3], dtype=torch.float32, device="cuda"),
+           "dq": torch.empty_like(q), "dk": torch.empty_like(q), "dv": torch.empty_like(q)}
+    a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    torch.cuda.synchronize()  # inputs and reference ready before the other streams start
+    load, work = torch.cuda.Stream(), torch.cuda.Stream()
+    mismatches = 0
+    for i in range(300):
+        if i % 10 == 0:
+            with torch.cuda.stream(load):
+                for _ in range(4):
+                    a = (a @ a).clamp_(-1, 1)
+        ca.attn_fwd(q, k, v, out["o"], out["lse"], w.scale, True, work)
+        ca.attn_bwd(q, k, v, out["o"], do, out["lse"], out["dq"], out["dk"], out["dv"], ws, w.scale, True, work)
+        if i % 30 == 29:
+            work.synchronize()
+            mismatches += sum(not torch.equal(out[n], ref[n]) for n in out)
+    torch.cuda.synchronize()
+    ca.check_device_error(work)
+    assert mismatches == 0
