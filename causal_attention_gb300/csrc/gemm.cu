@@ -173,11 +173,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             for (int j = 0; j < kGM / 64; ++j) tma_load_4d(sA + j * kGChunk, &p.a[am[j]], ax[j], k_t, az[j], k_b, full(s));
           }
           if constexpr (LAYOUT == kGemmNT) {
-            // rows 256 nt .. 256 nt + 255 of B [N, K] x K-columns 64i .. 64i + 63
+            // rows BN nt .. BN nt + BN - 1 of B [N, K] (two boxes) x K-columns 64i .. 64i + 63
             tma_load_2d(sB, &p.b[0], i * kGK, nt * kGN, full(s));
             tma_load_2d(sB + kGBBytes / 2, &p.b[0], i * kGK, nt * kGN + kGN / 2, full(s));
           } else if constexpr (LAYOUT == kGemmNN) {
-            // K-rows 64i .. 64i + 63 of B [K, N] x four 64-column MN chunks
+            // K-rows 64i .. 64i + 63 of B [K, N] x BN / 64 MN chunks of 64 columns
 #pragma unroll
             for (int j = 0; j < kGN / 64; ++j) tma_load_2d(sB + j * kGChunk, &p.b[0], nt * kGN + 64 * j, i * kGK, full(s));
           } else {
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t lane_base = (uint32_t)(eq * 32) << 16;
     const uint32_t stage0 = base + TC::OFF_EPI + (uint32_t)eq * (uint32_t)(TC::EPIBUF * kGEpiBytes);
     const uint32_t srow = (uint32_t)lane * 128u;
-    int cnt = 0;  // TMA stores this warp has issued (its two staging tiles alternate)
+    int cnt = 0;  // TMA stores this warp has issued (its staging tiles are used in turn)
     bool ok = true;
     // a staging tile may be rewritten once the store that last used it has read it
     auto take_buffer = [&]() {
@@ -249,6 +249,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (!(ok = mbar_wait_warp(acc_full(b), (r >> 1) & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
       const uint32_t tacc = tmem + lane_base + 256u * (uint32_t)b;
+      // after its last accumulator load this warp frees the accumulator, so that the MMAs of
+      // work item r + 2 can start while it still converts and stores the last chunk
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty(b));
+      };
       if constexpr (LAYOUT != kGemmTN) {
         // bf16 tokens x features through the token view of C
         const int bi = mt / p.nT, t0 = (mt % p.nT) * kGM + 32 * eq, t = t0 + lane;
@@ -257,10 +264,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         // 64-column chunk of a head at that offset reuses them (at d = 64, all chunks)
         float4 csv[16];
         int cs_x = -1;
+        const int n_chunks = min(kGN / 64, (p.N - nt * kGN + 63) / 64);  // >= 1: nt < n_tiles
 #pragma unroll 1
-        for (int j = 0; j < kGN / 64; ++j) {
+        for (int j = 0; j < n_chunks; ++j) {
           const int f = nt * kGN + 64 * j;
-          if (f >= p.N) break;
           int map, x, z;
           view_coord(p.vc, f, map, x, z);
           const bool rot = ROPE && f < p.rope_features;
@@ -277,6 +284,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           tmem_ld32(tacc + 64u * j, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           tmem_ld32(tacc + 64u * j + 32u, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_wait_ld();
+          if (j == n_chunks - 1) release();
           if (!rows) continue;
           uint32_t pk[32];
           if (rot) {
@@ -309,13 +317,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         // fp32 [split][M][N] through the 3-D map of C
         const int m0 = mt * kGM + 32 * eq, sp = u % p.splits;
         const bool rows = m0 < p.M;
+        const int n_chunks = min(kGN / 32, (p.N - nt * kGN + 31) / 32);  // >= 1: nt < n_tiles
 #pragma unroll 1
-        for (int j = 0; j < kGN / 32; ++j) {
+        for (int j = 0; j < n_chunks; ++j) {
           const int n = nt * kGN + 32 * j;
-          if (n >= p.N) break;
           uint32_t v[32];
           tmem_ld32(tacc + 32u * j, v);
           tmem_wait_ld();
+          if (j == n_chunks - 1) release();
           if (!rows) continue;
           const uint32_t buf = take_buffer();
 #pragma unroll
@@ -331,10 +340,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           ++cnt;
         }
       }
-      // this warp has read its lanes of the accumulator
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty(b));
     }
     if (lane == 0) bulk_wait_all();  // every store has landed before the CTA exits
     __syncwarp();
