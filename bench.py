@@ -198,8 +198,8 @@ def run_reference(args, rank, world):
 
 def variant(w, args):
     """The workload as the flags change it (no causal mask; another head dimension)."""
-    if args.non_causal:
-        w = w.with_(causal=False)
+    if args.non_causal:  # renamed: its kernels and traffic differ from the causal workload's
+        w = w.with_(name=f"{w.name}_noncausal", causal=False)
     if args.head_dim and args.head_dim != w.d:
         w = w.with_(name=f"{w.name}_d{args.head_dim}", d=args.head_dim)
     return w
