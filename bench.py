@@ -669,24 +669,44 @@ def run_block(args, rank, world, local):
     value = whole_job_tflops(step_flops, args.steps, world, elapsed_ms * 1e-3)
 
     # e2e: host buffers through the public API, every step copying x and dy in from pinned
-    # memory and y, dx, dW_qkv, dW_o out (one stream: copies, then the step)
+    # memory and y, dx, dW_qkv, dW_o out; pipelined as a caller would run it: the two
+    # device buffer sets alternate over three streams (copies in, compute, copies out), so
+    # one step's copies overlap its neighbours' compute
     x_h = torch.from_numpy(x_bits.view("int16")).view(torch.bfloat16).pin_memory()
     dy_h = torch.from_numpy(dy_bits.view("int16")).view(torch.bfloat16).pin_memory()
-    outs = {n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in ("y", "dx", "dw_qkv", "dw_o")}
+    outs_h = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory()
+               for n in ("y", "dx", "dw_qkv", "dw_o")} for _ in range(n_sets)]
     h2d = 2 * x_h.numel() * 2
-    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h[0].values())
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(n_sets)] for _ in range(3))
+    used = [False] * n_sets
 
     def e2e_step(i):
-        s = sets[i % n_sets]
-        with torch.cuda.stream(stream):
+        b = i % n_sets
+        s, oh = sets[b], outs_h[b]
+        if used[b]:
+            s_in.wait_event(ev_cmp[b])  # the compute two steps back has read these inputs
+        with torch.cuda.stream(s_in):
             s["x"].copy_(x_h, non_blocking=True)
             s["dy"].copy_(dy_h, non_blocking=True)
-            step(s)
-            for n, t in outs.items():
+        ev_in[b].record(s_in)
+        s_cmp.wait_event(ev_in[b])
+        if used[b]:
+            s_cmp.wait_event(ev_out[b])  # the outputs two steps back have been copied out
+        step(s, None, s_cmp)
+        ev_cmp[b].record(s_cmp)
+        s_out.wait_event(ev_cmp[b])
+        with torch.cuda.stream(s_out):
+            for n, t in oh.items():
                 t.copy_(s[n], non_blocking=True)
+        ev_out[b].record(s_out)
+        used[b] = True
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
     t0 = time.perf_counter()
     for i in range(args.e2e_steps):
         e2e_step(i)
