@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
 // NFIX: tiles fixed for a whole work item (K_j, V_j for dK/dV; Q_i, dO_i and, when the
 // dQ kernel computes D itself, O_i). NEPI: bf16 output tiles staged in shared memory for
 // a TMA store in the epilogue (dV and dK).
-template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0>
+// KRING, VRING (dQ kernel): separate rings of K and V tiles instead of the stages.
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D > 64) ? 2 : (D == 64 ? 3 : 4);
@@ -120,11 +121,14 @@ struct BwdCfg {
   // way to the workspace
   static constexpr int DS_BYTES = FUSE ? kTileRows * kTileRows * 2 : 0;
   static constexpr int DQS_BYTES = FUSE ? kTileRows * D * 4 : 0;
-  static constexpr int OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int STAGE_AREA = KRING ? (KRING + VRING) * TL::BYTES : STAGES * STAGE_BYTES;
+  static constexpr int OFF_DS = OFF_STAGE + STAGE_AREA;
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_EPI = OFF_DQS + DQS_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + NEPI * TL::BYTES;
-  static constexpr int NBAR = 1 + 2 * STAGES + 22;
+  // barrier rings: st_full / st_empty (the stages, or the K ring) and v_full / v_empty
+  static constexpr int RB = KRING > STAGES ? KRING : STAGES;
+  static constexpr int NBAR = 1 + 2 * RB + 22 + 2 * VRING;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -149,7 +153,7 @@ struct BwdSmem {
   uint32_t base;
   uint8_t* gbase;
   uint32_t bar0;
-  int st;
+  int st, vr;
   __device__ uint32_t fix_full(int b) const { return b ? bar0 + 8u * (20 + 2 * st) : bar0; }
   __device__ uint32_t st_full(int s) const { return bar0 + 8u * (1 + s); }
   __device__ uint32_t st_empty(int s) const { return bar0 + 8u * (1 + st + s); }
@@ -175,22 +179,26 @@ struct BwdSmem {
   __device__ uint32_t drain3() const { return bar0 + 8u * (18 + 2 * st); }
   // epilogue through shared memory: the TMA stores of the previous item read its tiles
   __device__ uint32_t epi_free() const { return bar0 + 8u * (19 + 2 * st); }
+  // dQ kernel: the V ring (its K ring uses st_full / st_empty)
+  __device__ uint32_t v_full(int s) const { return bar0 + 8u * (23 + 2 * st + s); }
+  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (23 + 2 * st + vr + s); }
 };
 
 constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
 // fix_empty_count: arrivals that release an item's fixed tiles (the MMA commit, plus the
 // elementwise threads where they read a fixed tile themselves).
-template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0>
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
                                                   volatile int*& abort, uint32_t fix_empty_count = 1) {
-  using C = BwdCfg<D, FUSE, NFIX, NEPI>;
+  using C = BwdCfg<D, FUSE, NFIX, NEPI, KRING, VRING>;
   BwdSmem s;
   const uint32_t raw = smem_u32(smem_raw);
   s.base = (raw + 1023u) & ~1023u;
   s.gbase = smem_raw + (s.base - raw);
   s.bar0 = s.base + C::OFF_BAR;
-  s.st = C::STAGES;
+  s.st = C::RB;
+  s.vr = VRING;
   tmem_slot = reinterpret_cast<uint32_t*>(s.gbase + C::OFF_MISC);
   abort = reinterpret_cast<volatile int*>(s.gbase + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
@@ -198,9 +206,13 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
       mbar_init(s.fix_full(b), 1);
       mbar_init(s.fix_empty(b), fix_empty_count);
     }
-    for (int i = 0; i < C::STAGES; ++i) {
+    for (int i = 0; i < C::RB; ++i) {
       mbar_init(s.st_full(i), 1);
       mbar_init(s.st_empty(i), 1);
+    }
+    for (int i = 0; i < VRING; ++i) {
+      mbar_init(s.v_full(i), 1);
+      mbar_init(s.v_empty(i), 1);
     }
     mbar_init(s.s_full(), 1);
     mbar_init(s.dp_full(), 1);
@@ -878,6 +890,16 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
 // ---------------------------------------------------------------------------
 // 3. dQ
 // ---------------------------------------------------------------------------
+// K and V rings of the dQ kernel. K_j is read by S_j and, last, by dQ_j; V_j by dP_j
+// alone, so a V slot turns over about one MMA group sooner than a K slot. At d >= 80 the
+// K ring has a third slot: K_{j+3} loads while iteration j + 1 runs (two combined K/V
+// stages left the S MMA waiting for its K tile).
+template <int D>
+struct DqRing {
+  static constexpr int K = D > 64 ? 3 : BwdCfg<D>::STAGES;
+  static constexpr int V = D > 64 ? 2 : BwdCfg<D>::STAGES;
+};
+
 // Work item = one 128-query tile i of one (b, h); its iterations run over the key tiles
 // j (j <= i when causal). Persistent, two MMA issuers:
 //   warp 17: S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
@@ -897,14 +919,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        float* __restrict__ ws_nlse2, float* __restrict__ ws_D, __nv_bfloat16* __restrict__ dq,
                        int T, int T_pad, int BH, int G, float scale, float scale_log2, uint32_t* __restrict__ err) {
   constexpr int NFIX = PRE ? 3 : 2;
-  using C = BwdCfg<D, false, NFIX>;
+  constexpr int KR = DqRing<D>::K, VR = DqRing<D>::V;
+  using C = BwdCfg<D, false, NFIX, 0, KR, VR>;
   using TL = Tile<D>;
-  constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
   // with PRE the elementwise threads read O_i and dO_i themselves: they release them too
-  const BwdSmem sm = bwd_smem_setup<D, false, NFIX>(smem_raw, tmem_slot, abort, PRE ? 1u + kEwThreads : 1u);
+  const BwdSmem sm = bwd_smem_setup<D, false, NFIX, 0, KR, VR>(smem_raw, tmem_slot, abort, PRE ? 1u + kEwThreads : 1u);
   const Abort ab{abort, err};
   const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -924,8 +946,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto acc_col = [&](int b) { return 256u + (b ? (uint32_t)D + 64u : 0u); };
   auto acc_full_b = [&](int b) { return b ? sm.dv_done() : sm.acc_full(); };
   auto acc_free_b = [&](int b) { return b ? sm.p_full() : sm.acc_free(); };
-  auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * C::STAGE_BYTES; };
-  auto sV = [&](int s) { return sK(s) + TL::BYTES; };
+  auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * TL::BYTES; };
+  auto sV = [&](int s) { return sm.base + C::OFF_STAGE + (KR + s) * TL::BYTES; };
+  constexpr uint64_t kSlotOff = TL::bytes_off(TL::BYTES);
 
   if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
@@ -935,7 +958,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
       bool ok = true;
-      int g = 0, r = 0, fix_issued = 0;
+      int g = 0, r = 0, fix_issued = 0, nk = 0, nv = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
         const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
         const int slot = r % NS;
@@ -946,15 +969,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         TL::load(sQf(slot) + TL::BYTES, &tmdO, qt * kTileRows, bh, sm.fix_full(slot));
         if (PRE) TL::load(sQf(slot) + 2 * TL::BYTES, &tmO, qt * kTileRows, bh, sm.fix_full(slot));
         for (int it = 0; it < n_it; ++it, ++g) {
-          const int s = g % ST, n = g / ST;
-          if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
-          mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES);
+          const int sk = g % KR, sv = g % VR;
           // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
-          TL::load(sK(s), &tmK, it * kTileRows, bh / G, sm.st_full(s));
-          TL::load(sV(s), &tmV, it * kTileRows, bh / G, sm.st_full(s));
+          if (g >= KR && !(ok = mbar_wait(sm.st_empty(sk), (g / KR - 1) & 1, ab, kErrTimeoutLoad))) break;
+          mbar_arrive_expect_tx(sm.st_full(sk), TL::BYTES);
+          TL::load(sK(sk), &tmK, it * kTileRows, bh / G, sm.st_full(sk));
+          ++nk;
+          if (g >= VR && !(ok = mbar_wait(sm.v_empty(sv), (g / VR - 1) & 1, ab, kErrTimeoutLoad))) break;
+          mbar_arrive_expect_tx(sm.v_full(sv), TL::BYTES);
+          TL::load(sV(sv), &tmV, it * kTileRows, bh / G, sm.v_full(sv));
+          ++nv;
         }
       }
-      if (!ok) drain_loads(sm, fix_issued, C::NSLOT, g, ST, ab);
+      if (!ok) {
+        drain_loads(sm, fix_issued, C::NSLOT, nk, KR, ab);  // fixed tiles and the K ring
+        for (int x = max(0, nv - VR); x < nv; ++x) mbar_wait_drain(sm.v_full(x % VR), (x / VR) & 1, ab);
+      }
     }
   } else if (warp == kWarpMmaA) {
     // ------------------------------------------------------------ MMA issuer (S, dP)
@@ -962,7 +992,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       const uint32_t tS = tmem, tDP = tmem + 128u;
       const uint64_t dKk0 = TL::desc_kmajor0(sK(0)), dVk0 = TL::desc_kmajor0(sV(0));
-      constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       bool ok = true;
       int g = 0;
       for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
@@ -970,18 +999,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait(sm.fix_full(slot), (r / NS) & 1, ab, kErrTimeoutMma))) break;
         const uint64_t dQk = TL::desc_kmajor0(sQf(slot)), dOk = TL::desc_kmajor0(sQf(slot) + TL::BYTES);
         for (int it = 0; it < n_it; ++it, ++g) {
-          const int s = g % ST;
+          const int sk = g % KR, sv = g % VR;
           if (g > 0 && !(ok = mbar_wait(sm.s_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // S read out
-          if (!(ok = mbar_wait(sm.st_full(s), (g / ST) & 1, ab, kErrTimeoutMma))) break;
+          if (!(ok = mbar_wait(sm.st_full(sk), (g / KR) & 1, ab, kErrTimeoutMma))) break;
           tc_fence_after();
           // S = Q_i K_j^T (M = queries, N = keys, K = d)
-          mma_chain_ss<TL, TL::KSTEPS_D>(tS, dQk, dKk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
+          mma_chain_ss<TL, TL::KSTEPS_D>(tS, dQk, dKk0 + (uint64_t)sk * kSlotOff, idesc_s, 0u);
           mma_commit(sm.s_full());
           if (g > 0 && !(ok = mbar_wait(sm.dp_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // dP read out
+          if (!(ok = mbar_wait(sm.v_full(sv), (g / VR) & 1, ab, kErrTimeoutMma))) break;
           tc_fence_after();
           // dP = dO_i V_j^T
-          mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)s * kStageOff, idesc_s, 0u);
+          mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)sv * kSlotOff, idesc_s, 0u);
           mma_commit(sm.dp_full());
+          mma_commit(sm.v_empty(sv));  // V_j is read by dP_j only
           if (it == n_it - 1) mma_commit(sm.fix_empty(slot));  // Q_i, dO_i are no longer read
         }
       }
@@ -996,23 +1027,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
       const uint32_t tDS = tmem + 256u + (uint32_t)TL::ACC_COLS;
       const uint64_t dKm0 = TL::desc_mnmajor0(sK(0));
-      constexpr uint64_t kStageOff = TL::bytes_off(C::STAGE_BYTES);
       bool ok = true;
       int g = 0;
       for (int r = 0, u; ok && (u = sched.item(r)) >= 0; ++r) {
         const int n_it = n_iters(u), b = r % NACC;
         for (int it = 0; it < n_it; ++it, ++g) {
-          const int s = g % ST;
+          const int sk = g % KR;
           if (!(ok = mbar_wait(sm.ds_full(), g & 1, ab, kErrTimeoutMma))) break;
           // this accumulator buffer still holds item r - NACC until its epilogue read it
           if (it == 0 && r >= NACC && !(ok = mbar_wait(acc_free_b(b), (r / NACC - 1) & 1, ab, kErrTimeoutMma))) break;
           tc_fence_after();
           // dQ += dS K_j (M = queries, N = d, K = keys); dS has its own 64 columns
-          mma_chain_ts<TL, false>(tmem + acc_col(b), tDS, dKm0 + (uint64_t)s * kStageOff, idesc_acc,
+          mma_chain_ts<TL, false>(tmem + acc_col(b), tDS, dKm0 + (uint64_t)sk * kSlotOff, idesc_acc,
                                   it > 0 ? 1u : 0u);
           mma_commit(sm.dk_done());  // "dQ_j done": the dS columns may be rewritten
-          // S_j and dP_j (warp 17) were read out before dS_j was signalled
-          mma_commit(sm.st_empty(s));
+          // K_j: S_j (warp 17) was read out before dS_j was signalled, dQ_j is its last reader
+          mma_commit(sm.st_empty(sk));
         }
         if (ok) mma_commit(acc_full_b(b));
       }
@@ -1287,7 +1317,8 @@ template <int D, bool CAUSAL>
 cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
   // d <= 64: the dQ kernel forms D itself (and runs before dK/dV)
   constexpr bool PRE = D <= 64;
-  using C = BwdCfg<D, false, PRE ? 3 : 2>;
+  using C = BwdCfg<D, false, PRE ? 3 : 2, 0, DqRing<D>::K, DqRing<D>::V>;
+  static_assert(C::SMEM_BYTES <= 227 * 1024, "dQ kernel shared memory");
   auto kern = attn_bwd_dq_kernel<D, CAUSAL, PRE>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
