@@ -66,6 +66,9 @@ def parse():
                     help="launch the timed steps one by one instead of replaying them as one CUDA graph")
     ap.add_argument("--fused-dq", action="store_true",
                     help="time the fused-dQ backward stages (d <= 64) instead of attn_bwd's kernels")
+    ap.add_argument("--order", default="fwd-bwd", choices=["fwd-bwd", "bwd-fwd"],
+                    help="launch order within a step: the backward of a buffer set may run before its "
+                         "forward (its O and LSE then come from that set's previous forward)")
     return ap.parse_args()
 
 
@@ -150,7 +153,7 @@ def oracle_sample(w, n_heads, x=None, budget_s=None):
         if budget_s is not None and time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    fwd, bwd = oracle.credited_flops(1, 1, w.T, w.d)
+    fwd, bwd = credited_flops(1, 1, w.T, w.d)
     return (fwd + bwd) * (1.0 if w.causal else 2.0) * done, dt, done
 
 
@@ -285,6 +288,20 @@ def spread(values_ms):
             "ms_p95": round(v[min(len(v) - 1, int(round(0.95 * (len(v) - 1))))], 5)}
 
 
+def to_device(bits):
+    """A device bf16 tensor from seeded bf16 bit patterns (numpy uint16 / int16)."""
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def credited_flops(B, H, T, d):
+    """The metric's credited causal FLOPs: forward 2*B*H*T^2*d, backward 2.5 times that (the
+    convention that reproduces the Forge RESEARCH.md section 6 table)."""
+    fwd = 2.0 * B * H * T * T * d
+    return fwd, 2.5 * fwd
+
+
 def kernel_flops(w):
     """Algorithmic FLOPs per launch of each kernel (causal half of every T x T GEMM)."""
     g = w.B * w.H * w.T * w.T * w.d * (1.0 if w.causal else 2.0)  # one causal GEMM = B*H*T^2*d
@@ -341,9 +358,7 @@ def run_ours(args, rank, world, local):
     import torch
     import torch.distributed as dist
     import causal_attention_gb300 as ca
-    import oracle
     import seeded_inputs as si
-    from tests.gpu_util import to_device
 
     torch.cuda.set_device(local)
     if world > 1:
@@ -362,6 +377,8 @@ def run_ours(args, rank, world, local):
     gqa = H_kv != H
     KERNELS = ("fwd", "bwd") if gqa else kernels_for(d, args.fused_dq)
     fused = "bwd_dkdv_dq" in KERNELS
+    if args.order == "bwd-fwd":  # the forward last: KERNELS starts with it
+        KERNELS = KERNELS[1:] + KERNELS[:1]
     ws_bytes = (ca.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) if gqa else
                 (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d))
     per_set = 8 * B * H * T * d * 2 + B * H * T * 4 + ws_bytes
@@ -407,6 +424,9 @@ def run_ours(args, rank, world, local):
         if ev is not None:
             ev[len(KERNELS)].record(stream)
 
+    if args.order == "bwd-fwd":  # every set's O and LSE exist before its first backward
+        for s in sets:
+            launch["fwd"](s)
     for i in range(max(3, args.warmup)):
         step(sets[i % n_sets])
     ca.check_device_error(stream)
@@ -431,7 +451,7 @@ def run_ours(args, rank, world, local):
     mean_ms = {k: statistics.fmean(v) for k, v in per_kernel.items()}
 
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
-    fwd_f, bwd_f = oracle.credited_flops(B, H, T, d)
+    fwd_f, bwd_f = credited_flops(B, H, T, d)
     step_flops = (fwd_f + bwd_f) * (1.0 if causal else 2.0)
     value = whole_job_tflops(step_flops, args.steps, world, elapsed_ms * 1e-3)
 
@@ -521,7 +541,7 @@ def run_ours(args, rank, world, local):
             e.update(gbs=round(gbs, 1), frac=round(gbs / peak_gbs, 4))
         kernels[k] = e
     fwd_tf = fwd_f * (1.0 if causal else 2.0) / (mean_ms["fwd"] * 1e-3) / 1e12
-    bwd_ms = sum(mean_ms[k] for k in KERNELS[1:])
+    bwd_ms = sum(mean_ms[k] for k in KERNELS if k != "fwd")
     bwd_tf = bwd_f * (1.0 if causal else 2.0) / (bwd_ms * 1e-3) / 1e12
 
     cpu = None
@@ -538,7 +558,7 @@ def run_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wr.name, "B": B, "H": H, "H_kv": H_kv, "T": T, "d": d, "causal": causal,
                    "parallelism": f"replicas x{world}", "l2": f"inputs rotate over {n_sets} sets ({n_sets * per_set / 2**20:.0f} MiB > L2)",
-                   "launch": launch_mode},
+                   "launch": launch_mode, "order": args.order},
         "frac_of_peak": round(value / peak_tf, 4),
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
         "fwd_frac": round(fwd_tf / peak_tf, 4), "bwd_frac": round(bwd_tf / peak_tf, 4),
@@ -562,6 +582,8 @@ def main():
         run_reference(args, rank, world)
         return
     if args.block:
+        if args.order != "fwd-bwd":
+            raise SystemExit("--order applies to the attention line, not to --block")
         run_block(args, rank, world, local)
         return
     run_ours(args, rank, world, local)
@@ -573,8 +595,7 @@ BLOCK_STAGES = ("qkv_proj", "attn_fwd", "out_proj", "out_proj_bwd", "attn_bwd", 
 def block_flops(B, H, H_kv, T, d, C, causal):
     """Credited FLOPs per stage: the attention's (forward 2 B H T^2 d, backward 2.5x, causal
     halves counted as in the attention line) and 2 M N K per GEMM."""
-    import oracle
-    fwd, bwd = oracle.credited_flops(B, H, T, d)
+    fwd, bwd = credited_flops(B, H, T, d)
     mul = 1.0 if causal else 2.0
     n_qkv, tok = (H + 2 * H_kv) * d, B * T
     return {"qkv_proj": 2.0 * tok * n_qkv * C, "attn_fwd": fwd * mul, "out_proj": 2.0 * tok * C * H * d,
@@ -589,7 +610,6 @@ def run_block(args, rank, world, local):
     import torch.distributed as dist
     import causal_attention_gb300 as ca
     import seeded_inputs as si
-    from tests.gpu_util import to_device
 
     torch.cuda.set_device(local)
     if world > 1:
