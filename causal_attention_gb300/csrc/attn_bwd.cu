@@ -1091,10 +1091,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t* ow = &ov.x;
             const uint32_t* dw = &dv4.x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              a0 = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), a0);
-              a1 = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), a1);
-            }
+            for (int e = 0; e < 4; ++e) fma_bf16x2_f32(ow[e], dw[e], a0, a1);
           }
         mbar_arrive(sm.fix_empty(slot));  // O_i, dO_i read (the MMA commit is the other arrival)
         Dr = a0 + a1;

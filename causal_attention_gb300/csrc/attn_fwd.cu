@@ -394,7 +394,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // values, so that O / lr stays a convex combination of V rows.
         const uint64_t nmc = f2_pack(-m * scale_log2, -m * scale_log2);
         uint32_t pk[64];
-        uint64_t se[4] = {0, 0, 0, 0}, sr[4] = {0, 0, 0, 0};
+        uint64_t se[4] = {0, 0, 0, 0};
+        float sr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           float a, b;
@@ -403,12 +404,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           b = ex2(b);
           pk[i] = pack_bf16(a, b);
           se[i & 3] = f2_add(se[i & 3], f2_pack(a, b));
-          sr[i & 3] = f2_add(sr[i & 3], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
+          add_bf16x2_f32(pk[i], sr[2 * (i & 1)], sr[2 * (i & 1) + 1]);
         }
         {
           float a0, a1, b0, b1;
           f2_unpack(f2_add(f2_add(se[0], se[1]), f2_add(se[2], se[3])), a0, a1);
-          f2_unpack(f2_add(f2_add(sr[0], sr[1]), f2_add(sr[2], sr[3])), b0, b1);
+          b0 = sr[0] + sr[2];
+          b1 = sr[1] + sr[3];
           l = l * corr + (a0 + a1);
           lr = lr * corr + (b0 + b1);
         }

@@ -408,6 +408,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// Mixed-precision accumulation into fp32 from a packed bf16 pair (sm_100+ add / fma with
+// .bf16 sources and an .f32 destination). Widening bf16 to fp32 is exact, so each is the
+// fp32 operation on the widened values with one rounding, without separate unpacking.
+// lo += low half of x; hi += high half of x.
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t x, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 xl, xh;\n\tmov.b32 {xl, xh}, %2;\n\t"
+      "add.rn.f32.bf16 %0, xl, %0;\n\tadd.rn.f32.bf16 %1, xh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi) : "r"(x));
+}
+// lo = x.lo * y.lo + lo; hi = x.hi * y.hi + hi (each a single-rounding fma).
+__device__ __forceinline__ void fma_bf16x2_f32(uint32_t x, uint32_t y, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %2;\n\tmov.b32 {yl, yh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, xl, yl, %0;\n\tfma.rn.f32.bf16 %1, xh, yh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi) : "r"(x), "r"(y));
+}
+
 // Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction for two lanes of math).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
