@@ -58,3 +58,18 @@ def test_bench_line_keys(order):
 def test_order_is_refused_for_the_block():
     r = _bench("--block", "--order", "bwd-fwd", timeout=120)
     assert r.returncode != 0 and "--order applies to the attention line" in r.stderr
+
+
+@pytest.mark.gpu
+def test_bench_block_line_keys():
+    d = _line(_bench("--block", "--workload", "gpt12m", "--steps", "4", "--warmup", "3", "--e2e-steps", "3"))
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "config", "roofline", "e2e",
+              "gpu_launches", "clocks", "stages"):
+        assert k in d, k
+    c = d["config"]
+    assert c["workload"] == "gpt12m_block" and c["C"] == 6 * 64 and c["rope"] is True
+    assert set(d["stages"]) == {"qkv_proj", "attn_fwd", "out_proj", "out_proj_bwd", "attn_bwd", "qkv_proj_bwd"}
+    assert d["value"] > 0 and d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
+    assert d["e2e"]["d2h_bytes_per_step"] > 0 and d["gpu_launches"] > 0
+    rf = d["roofline"]
+    assert rf["peak"] > 0 and abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
