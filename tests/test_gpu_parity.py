@@ -415,3 +415,41 @@ def test_bitwise_determinism_under_concurrent_load():
     torch.cuda.synchronize()
     ca.check_device_error(work)
     assert mismatches == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_running_max_grows_every_block(d):
+    """Logits that rise along every row (q = e_0, k_j = 4j e_0 at scale 1/sqrt(d)) move the
+    running max by far more than the forward's lazy-rescale threshold (2^32) in every
+    128-key block, so O is rescaled at every step; O, LSE and the gradients must still
+    match the oracle on the same bf16-rounded inputs."""
+    T = 512
+    w = si.Workload(f"rising{d}", 1, 1, T, d, seed=91 + d)
+    x = si.make_inputs(w)
+    q = np.zeros((1, 1, T, d), np.float32)
+    q[..., 0] = 1.0
+    k = np.zeros((1, 1, T, d), np.float32)
+    k[0, 0, :, 0] = 4.0 * np.arange(T, dtype=np.float32)
+    x = dict(x, q=si.f32_to_bf16_bits(q), k=si.f32_to_bf16_bits(k))
+    # growth of the row max per 128-key block, in log2 units, against the threshold of 32
+    assert 4.0 * 128 * w.scale / np.log(2.0) > 60
+    gpu, ref = gu.run_gpu(w, x), gu.run_oracle(w, x)
+    err = gu.compare(gpu, ref)
+    assert err["o"][0] <= gu.TOL_O_MAX_ABS and err["o"][1] <= gu.TOL_O_REL_RMS, err["o"]
+    assert err["lse"][0] <= gu.TOL_LSE_MAX_ABS, err["lse"]
+    assert err["dk"][1] <= gu.TOL_GRAD_REL_RMS and err["dv"][1] <= gu.TOL_GRAD_REL_RMS, (err["dk"], err["dv"])
+    # dQ_i = scale sum_j dS_ij k_j sums large, nearly equal k_j against weights that add up
+    # to zero (sum_j dS_ij = 0): an ill-conditioned sum whose error is set by the bf16 inputs
+    # of the backward, not by the kernel: dS enters the MMA as bf16 (relative 2^-9), and D is
+    # formed from the bf16 O that the forward returned (an error dD_i moves dQ_i by
+    # scale dD_i sum_j P_ij k_j). Bound: twice each term's rounding.
+    qf, kf, vf, dof = (si.bf16_bits_to_f64(x[n])[0, 0] for n in ("q", "k", "v", "do"))
+    s_ = w.scale * qf @ kf.T
+    s_[np.triu_indices(T, 1)] = -np.inf
+    p_ = np.exp(s_ - ref["lse"][0, 0][:, None])
+    ds = p_ * (dof @ vf.T - (dof * ref["o"][0, 0]).sum(1, keepdims=True))
+    d_err = 2.0 ** -8 * (np.abs(dof) * np.abs(ref["o"][0, 0])).sum(1, keepdims=True)
+    bound = w.scale * 2.0 ** -8 * (np.abs(ds) @ np.abs(kf)) + w.scale * d_err * (p_ @ np.abs(kf)) \
+        + 4e-3 * np.abs(ref["dq"][0, 0]).max()
+    ratio = np.abs(gu.to_f64(gpu["dq"])[0, 0] - ref["dq"][0, 0]) / bound
+    assert ratio.max() <= 1.0, f"dQ error {ratio.max():.2f} x the rounding bound, row {np.unravel_index(ratio.argmax(), ratio.shape)}"
