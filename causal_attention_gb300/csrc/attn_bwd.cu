@@ -135,7 +135,7 @@ struct BwdCfg {
   static constexpr int SMEM_RAW = OFF_MISC + 16 + 1024;
   static constexpr int SMEM_BYTES = SMEM_RAW > 116 * 1024 ? SMEM_RAW : 116 * 1024;
   // The dK/dV kernel gives P^T and dS^T their own TMEM columns when they fit (d <= 64);
-  // then it also runs persistently with two MMA issuers.
+  // then two threads issue its MMAs.
   static constexpr bool SEP_DKDV = D <= 64;
   static constexpr uint32_t COL_P = 384, COL_DS = 448;
   // fused dQ: dQ_ij (fp32, d columns) takes the columns of dS^T, which lives in shared memory
@@ -395,14 +395,15 @@ __device__ __forceinline__ bool wait_turn(const int* cnt, int want, const Abort&
 // 2. dK / dV (and, fused, dQ)
 // ---------------------------------------------------------------------------
 // Work item = one 128-key tile j of one (b, h); its iterations run over the query tiles
-// i (i >= j when causal). With separate P^T / dS^T columns (d <= 64) the kernel is
-// persistent and two threads issue MMAs:
+// i (i >= j when causal). Persistent. With separate P^T / dS^T columns (d <= 64) two
+// threads issue MMAs:
 //   warp 17: S_i (= S^T, K_j Q_i^T) as soon as S_{i-1} was read out, dP_i likewise;
 //   warp 18: dV += P_i^T dO_i once P_i^T is in TMEM, dK += dS_i^T Q_i once dS_i^T is.
 // The next item's S and dP run while the elementwise warps store this item's dK, dV.
 // At d = 128 (TMEM full, P^T / dS^T written over S^T / dP^T) one thread issues in the
 // order S_0, dP_0 | P_0: dV_0, S_1 | dS_0: dK_0, dP_1 | ..., which relies on same-thread
-// MMAs executing in issue order, and each CTA takes one item.
+// MMAs executing in issue order; persistent too (the next item's K_j, V_j and first S,
+// dP overlap this item's epilogue).
 //
 // FUSE (d <= 64): the dQ contributions are formed here too, so the separate dQ kernel and
 // its two recomputed GEMMs (S and dP) go away. The elementwise warps write dS^T to shared
@@ -1292,8 +1293,8 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * (a.BH / a.G) * a.S;  // key tiles x slices x splits
-  // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
-  const int grid = C::SEP_DKDV ? min(n_items, a.num_sms) : n_items;
+  // persistent: one CTA per SM walks its share of the items
+  const int grid = min(n_items, a.num_sms);
   if (EPI && (!a.tmdK || !a.tmdV)) return cudaErrorInvalidValue;
   return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
                     EPI ? *a.tmdK : *a.tmQ, EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.dq_acc,

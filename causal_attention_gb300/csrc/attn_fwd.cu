@@ -39,9 +39,10 @@ template <int D>
 struct FwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D > 64) ? 2 : (D == 64 ? 3 : 4);
-  // P gets its own TMEM columns when they fit (d <= 64); then the kernel is persistent
-  // and each query tile has its own MMA issuer. At d = 80 and 128, S and O of both tiles
-  // leave no room for P: P is written over S and one thread issues every MMA.
+  // P gets its own TMEM columns when they fit (d <= 64); then each query tile has its own
+  // MMA issuer. At d = 80 and 128, S and O of both tiles leave no room for P: P is written
+  // over S and one thread issues every MMA. Persistent either way: the next item's Q load
+  // and first S MMAs overlap this item's epilogue.
   static constexpr bool SEP_P = D <= 64;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + TL::ACC_COLS;
   static constexpr uint32_t COL_P0 = SEP_P ? 384 : COL_S0, COL_P1 = SEP_P ? 448 : COL_S1;
@@ -507,8 +508,8 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int n_pairs = (a.T + 2 * kTileRows - 1) / (2 * kTileRows);
   const int n_items = n_pairs * a.BH;
-  // persistent (one CTA per SM) where the kernel overlaps items; else one item per CTA
-  const int grid = C::SEP_P ? min(n_items, a.num_sms) : n_items;
+  // persistent: one CTA per SM walks its share of the items
+  const int grid = min(n_items, a.num_sms);
   return launch_pdl(kern, dim3(grid), dim3(kFwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, a.o, a.lse,
                     a.T, a.BH, a.G, n_pairs, a.scale, a.scale * 1.4426950408889634f, a.err);
 }
