@@ -1293,8 +1293,11 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * (a.BH / a.G) * a.S;  // key tiles x slices x splits
-  // persistent: one CTA per SM walks its share of the items
-  const int grid = min(n_items, a.num_sms);
+  // persistent: one CTA per SM walks its share of the items. Split items (few key/value
+  // heads) differ in length by the split's head count as well as by key tile, and there
+  // the hardware's dynamic dealing of one item per CTA, longest first, balances better
+  // than a fixed per-CTA share.
+  const int grid = SPLIT ? n_items : min(n_items, a.num_sms);
   if (EPI && (!a.tmdK || !a.tmdV)) return cudaErrorInvalidValue;
   return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
                     EPI ? *a.tmdK : *a.tmQ, EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.dq_acc,
