@@ -200,7 +200,11 @@ attn_status attn_bwd_dq_finish(void* dq, const void* workspace, size_t workspace
  *   Limit: B*H*T_pad <= 1,048,576 (T_pad = T rounded up to 128); larger shapes return
  *   ATTN_ERR_WORKSPACE without launching anything (use attn_bwd with a workspace).
  *   Set-up: the first call on each device looks up the array's device address (with
- *   that device current) and caches it; make that first call before any stream capture.
+ *   that device current) and caches it. Under lazy module loading (the CUDA runtime's
+ *   default) that lookup may also be what loads the library's device code, and with it
+ *   the array, onto the device: the first call on a device can allocate device memory and
+ *   synchronise. Treat it as a warm-up: make it before any stream capture and outside
+ *   the region that must not allocate; later calls allocate nothing.
  *   Sharing: every call on a device uses the same array, and the array keeps the last
  *   call's contents. Nothing in it has to start at zero (each call overwrites every
  *   entry it reads), but calls whose executions overlap on the GPU (different streams,

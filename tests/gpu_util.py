@@ -50,17 +50,40 @@ def run_oracle(w: si.Workload, x, heads=None):
     return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
 
 
-def compare(gpu, ref, heads=None):
-    """Error metrics over the compared heads (all heads if None)."""
+def run_oracle_all_heads(w: si.Workload, x, workers: int = 8):
+    """The oracle over every head of a workload, spread over a process pool."""
+    from tests import oracle_pool
+    return oracle_pool.all_heads(w.scale, w.causal, x, workers)
+
+
+# Per-tile bar of the gradients: the whole-tensor bar applied to every 128-row tile of every
+# head, with a factor 2 for tiles whose norm is below the tensor's average. A tile with one
+# row wrong by about that row's own size has rel-RMS near sqrt(1/128) = 0.088 and fails it.
+TOL_GRAD_TILE_REL_RMS = 2 * TOL_GRAD_REL_RMS
+
+
+def tile_errors(gpu, ref, tile=128):
+    """The worst 128-row tile of dQ, dK and dV over every head: {name: (rel-RMS of that
+    tile, (b, h, first row), its max-abs error / the tile's max |ref|)}."""
     out = {}
-    for name in ("o", "lse", "dq", "dk", "dv"):
-        g = to_f64(gpu[name])
-        r = ref[name]
-        if heads is not None:
-            g = np.stack([g[b, h] for b, h in heads])
-            r = np.stack([r[b, h] for b, h in heads])
-        out[name] = (max_abs(g, r), rel_rms(g, r))
+    for name in ("dq", "dk", "dv"):
+        g, r = to_f64(gpu[name]), ref[name]
+        B, H, T, _ = r.shape
+        worst = (-1.0, None, 0.0)
+        for b in range(B):
+            for h in range(H):
+                for t0 in range(0, T, tile):
+                    gt, rt = g[b, h, t0:t0 + tile], r[b, h, t0:t0 + tile]
+                    e = rel_rms(gt, rt)
+                    if e > worst[0]:
+                        worst = (e, (b, h, t0), max_abs(gt, rt) / max(float(np.max(np.abs(rt))), 1e-30))
+        out[name] = worst
     return out
+
+
+def assert_tiles_within_tolerance(terr, label=""):
+    for name, (e, where, rel_max) in terr.items():
+        assert e <= TOL_GRAD_TILE_REL_RMS, f"{label} {name} tile {where}: rel-RMS {e:.3e} (max-abs / max {rel_max:.3e})"
 
 
 def assert_within_tolerance(err, label=""):

@@ -16,11 +16,10 @@ from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-# heads compared on the large workloads (first, middle, last and a few between)
+# heads compared by the tests that run a large workload's shapes in another variant
+# (first, middle, last); the five workloads themselves are compared on every head
 SAMPLED_HEADS = {
-    "gpt100m": [(0, 0), (2, 5), (5, 9), (7, 11)],
     "gpt205m": [(0, 0), (1, 7), (3, 15)],
-    "long8k": [(0, 0), (0, 9), (0, 15)],
 }
 
 
@@ -32,17 +31,19 @@ def _need_gpu():
 
 @pytest.mark.parametrize("name", ["tiny", "gpt12m", "gpt100m", "gpt205m", "long8k"])
 def test_workload_parity(name):
+    """Every head of every workload against the oracle: the whole-tensor bars, and the
+    per-tile bar on every 128-row tile of dQ, dK and dV (so that one wrong tile or row of
+    one head cannot hide in the whole tensor's RMS)."""
     w = si.WORKLOADS[name]
     x = si.make_inputs(w)
     gpu = gu.run_gpu(w, x)
-    heads = SAMPLED_HEADS.get(name)
-    ref = gu.run_oracle(w, x, heads=heads)
-    err = gu.compare(gpu, ref, heads)
-    print(name, {k: tuple(f"{e:.2e}" for e in v) for k, v in err.items()})
+    ref = gu.run_oracle(w, x) if w.T <= 256 else gu.run_oracle_all_heads(w, x)
+    err = gu.compare(gpu, ref)
+    terr = gu.tile_errors(gpu, ref)
+    print(name, {k: tuple(f"{e:.2e}" for e in v) for k, v in err.items()},
+          "worst tiles", {k: (f"{e:.2e}", where, f"{m:.2e}") for k, (e, where, m) in terr.items()})
     gu.assert_within_tolerance(err, name)
-    # outputs outside the sampled heads must be finite too
-    for t in gpu.values():
-        assert torch.isfinite(t).all()
+    gu.assert_tiles_within_tolerance(terr, name)
 
 
 EDGE = [
@@ -439,10 +440,16 @@ def test_running_max_grows_every_block(d):
     assert err["lse"][0] <= gu.TOL_LSE_MAX_ABS, err["lse"]
     assert err["dk"][1] <= gu.TOL_GRAD_REL_RMS and err["dv"][1] <= gu.TOL_GRAD_REL_RMS, (err["dk"], err["dv"])
     # dQ_i = scale sum_j dS_ij k_j sums large, nearly equal k_j against weights that add up
-    # to zero (sum_j dS_ij = 0): an ill-conditioned sum whose error is set by the bf16 inputs
-    # of the backward, not by the kernel: dS enters the MMA as bf16 (relative 2^-9), and D is
-    # formed from the bf16 O that the forward returned (an error dD_i moves dQ_i by
-    # scale dD_i sum_j P_ij k_j). Bound: twice each term's rounding.
+    # to zero (sum_j dS_ij = 0): an ill-conditioned sum whose error is set by the bf16
+    # roundings of the backward, not by the kernel's arithmetic. Three of them, each bounded
+    # element by element with a factor 2 of margin:
+    #   dS enters the dQ MMA as bf16 (relative 2^-9 per element): scale 2^-8 (|dS| |K|)_ic;
+    #   D is formed from the bf16 O the forward returned (O's rounding and the forward's own
+    #   error, each about 2^-9 relative): |dD_i| <= 2^-8 sum_c |dO_ic O_ic|, which moves dQ_i
+    #   by scale dD_i sum_j P_ij k_j;
+    #   dQ itself is returned in bf16 (relative 2^-9): 2^-8 |dQ_ic|.
+    # The fp32 accumulation of the MMAs and exp2 of the recomputed P add errors near 2^-24
+    # relative, far below these.
     qf, kf, vf, dof = (si.bf16_bits_to_f64(x[n])[0, 0] for n in ("q", "k", "v", "do"))
     s_ = w.scale * qf @ kf.T
     s_[np.triu_indices(T, 1)] = -np.inf
@@ -450,6 +457,11 @@ def test_running_max_grows_every_block(d):
     ds = p_ * (dof @ vf.T - (dof * ref["o"][0, 0]).sum(1, keepdims=True))
     d_err = 2.0 ** -8 * (np.abs(dof) * np.abs(ref["o"][0, 0])).sum(1, keepdims=True)
     bound = w.scale * 2.0 ** -8 * (np.abs(ds) @ np.abs(kf)) + w.scale * d_err * (p_ @ np.abs(kf)) \
-        + 4e-3 * np.abs(ref["dq"][0, 0]).max()
-    ratio = np.abs(gu.to_f64(gpu["dq"])[0, 0] - ref["dq"][0, 0]) / bound
+        + 2.0 ** -8 * np.abs(ref["dq"][0, 0])
+    got = gu.to_f64(gpu["dq"])[0, 0]
+    e_abs = np.abs(got - ref["dq"][0, 0])
+    # columns c > 0 of K are zero, so there dQ and the bound are exactly 0
+    ratio = np.where(bound > 0, e_abs / np.where(bound > 0, bound, 1.0), np.where(e_abs > 0, np.inf, 0.0))
+    print(f"rising d={d}: dQ rel-RMS {err['dq'][1]:.3e} (whole-tensor bar {gu.TOL_GRAD_REL_RMS:g} not applied), "
+          f"worst error / rounding bound {ratio.max():.3f}")
     assert ratio.max() <= 1.0, f"dQ error {ratio.max():.2f} x the rounding bound, row {np.unravel_index(ratio.argmax(), ratio.shape)}"
