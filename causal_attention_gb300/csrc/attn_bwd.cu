@@ -39,9 +39,10 @@ namespace attn {
 
 namespace {
 
-// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers, 19 (fused dQ) reducer
+// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers, 19 (fused dQ) reducer or
+// (dQ kernel at d >= 80) the D warp
 constexpr int kBwdThreads = 608;
-constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18, kWarpRed = 19;
+constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18, kWarpRed = 19, kWarpD = 19;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -104,7 +105,8 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
 // dQ kernel computes D itself, O_i). NEPI: bf16 output tiles staged in shared memory for
 // a TMA store in the epilogue (dV and dK).
 // KRING, VRING (dQ kernel): separate rings of K and V tiles instead of the stages.
-template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0>
+// DBUF (dQ kernel at d >= 80): bytes of the shared D buffer its D warp fills per item.
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0, int DBUF = 0>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D > 64) ? 2 : (D == 64 ? 3 : 4);
@@ -125,10 +127,12 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_STAGE + STAGE_AREA;
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_EPI = OFF_DQS + DQS_BYTES;
-  static constexpr int OFF_BAR = OFF_EPI + NEPI * TL::BYTES;
-  // barrier rings: st_full / st_empty (the stages, or the K ring) and v_full / v_empty
+  static constexpr int OFF_DBUF = OFF_EPI + NEPI * TL::BYTES;
+  static constexpr int OFF_BAR = OFF_DBUF + DBUF;
+  // barrier rings: st_full / st_empty (the stages, or the K ring) and v_full / v_empty;
+  // then d_full / d_free
   static constexpr int RB = KRING > STAGES ? KRING : STAGES;
-  static constexpr int NBAR = 1 + 2 * RB + 22 + 2 * VRING;
+  static constexpr int NBAR = 1 + 2 * RB + 22 + 2 * VRING + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -140,7 +144,7 @@ struct BwdCfg {
   static constexpr uint32_t COL_P = 384, COL_DS = 448;
   // fused dQ: dQ_ij (fp32, d columns) takes the columns of dS^T, which lives in shared memory
   static constexpr uint32_t COL_DQ = 448;
-  static constexpr int THREADS = FUSE ? kBwdThreads + 32 : kBwdThreads;
+  static constexpr int THREADS = (FUSE || DBUF) ? kBwdThreads + 32 : kBwdThreads;
   static_assert(!FUSE || SEP_DKDV, "the fused dQ needs the separate P^T columns (d <= 64)");
 };
 
@@ -182,16 +186,19 @@ struct BwdSmem {
   // dQ kernel: the V ring (its K ring uses st_full / st_empty)
   __device__ uint32_t v_full(int s) const { return bar0 + 8u * (23 + 2 * st + s); }
   __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (23 + 2 * st + vr + s); }
+  // dQ kernel with a D warp: the item's D values are in the shared buffer / were read
+  __device__ uint32_t d_full() const { return bar0 + 8u * (23 + 2 * st + 2 * vr); }
+  __device__ uint32_t d_free() const { return bar0 + 8u * (24 + 2 * st + 2 * vr); }
 };
 
 constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
 // fix_empty_count: arrivals that release an item's fixed tiles (the MMA commit, plus the
 // elementwise threads where they read a fixed tile themselves).
-template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0>
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0, int DBUF = 0>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
                                                   volatile int*& abort, uint32_t fix_empty_count = 1) {
-  using C = BwdCfg<D, FUSE, NFIX, NEPI, KRING, VRING>;
+  using C = BwdCfg<D, FUSE, NFIX, NEPI, KRING, VRING, DBUF>;
   BwdSmem s;
   const uint32_t raw = smem_u32(smem_raw);
   s.base = (raw + 1023u) & ~1023u;
@@ -227,6 +234,10 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     mbar_init(s.drain(), 1);
     mbar_init(s.drain2(), 1);
     mbar_init(s.epi_free(), 1);
+    if (DBUF) {
+      mbar_init(s.d_full(), 2);  // lanes 0 and 16 of the D warp
+      mbar_init(s.d_free(), kEwThreads);
+    }
     if (FUSE) {
       mbar_init(s.dq_done(), 1);
       mbar_init(s.dq_free(), kEwThreads);
@@ -475,6 +486,8 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
+      // Q_i and dO_i are read by every key tile of their head: keep them in L2; K_j, V_j once
+      const uint64_t keep = l2_evict_last(), once = l2_evict_first();
       bool ok = true;
       int g = 0, r = 0, fix_issued = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
@@ -483,14 +496,14 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         if (r >= NS && !(ok = mbar_wait(sm.fix_empty(slot), (r / NS - 1) & 1, ab, kErrTimeoutLoad))) break;
         ++fix_issued;
         mbar_arrive_expect_tx(sm.fix_full(slot), 2 * TL::BYTES);
-        TL::load(sKf(slot), &tmK, kt * kTileRows, bh, sm.fix_full(slot));
-        TL::load(sKf(slot) + TL::BYTES, &tmV, kt * kTileRows, bh, sm.fix_full(slot));
+        TL::load(sKf(slot), &tmK, kt * kTileRows, bh, sm.fix_full(slot), once);
+        TL::load(sKf(slot) + TL::BYTES, &tmV, kt * kTileRows, bh, sm.fix_full(slot), once);
         for (int it = 0, qi = i0, bq = bh * G + head0(u); it < n_it; ++it, ++g) {
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES + 1024);
-          TL::load(sQ(s), &tmQ, qi * kTileRows, bq, sm.st_full(s));
-          TL::load(sdO(s), &tmdO, qi * kTileRows, bq, sm.st_full(s));
+          TL::load(sQ(s), &tmQ, qi * kTileRows, bq, sm.st_full(s), keep);
+          TL::load(sdO(s), &tmdO, qi * kTileRows, bq, sm.st_full(s), keep);
           const size_t woff = (size_t)bq * T_pad + (size_t)qi * kTileRows;
           bulk_load(sL(s), ws_nlse2 + woff, 512, sm.st_full(s));
           bulk_load(sL(s) + 512, ws_D + woff, 512, sm.st_full(s));
@@ -901,6 +914,11 @@ struct DqRing {
   static constexpr int V = D > 64 ? 2 : BwdCfg<D>::STAGES;
 };
 
+// The dQ kernel's shared-memory plan: at d <= 64 O_i is staged as a third fixed tile; at
+// d >= 80 (no room for it) the D warp's 128-float D buffer instead.
+template <int D>
+using DqCfg = BwdCfg<D, false, D <= 64 ? 3 : 2, 0, DqRing<D>::K, DqRing<D>::V, D <= 64 ? 0 : 512>;
+
 // Work item = one 128-query tile i of one (b, h); its iterations run over the key tiles
 // j (j <= i when causal). Persistent, two MMA issuers:
 //   warp 17: S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
@@ -908,26 +926,35 @@ struct DqRing {
 // At d <= 64 the dQ accumulator has two TMEM buffers (items alternate), and the
 // elementwise warps store an item's dQ during the next item's first iteration, by when
 // its last dQ MMA has finished, instead of waiting for it at the end of the item.
-// PRE (d <= 64): the kernel also does the preprocess for its query tile, so that it runs
-// first and no separate D launch is needed: O_i is staged with Q_i and dO_i, the
-// elementwise threads form D_i = rowsum(dO_i * O_i) and -LSE_i * log2(e) themselves at the
-// start of the item and write both to the workspace for the dK/dV kernel that follows.
-template <int D, bool CAUSAL, bool PRE>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+// The kernel also does the preprocess for its query tile, so that it runs first and no
+// separate D launch is needed: D_i = rowsum(dO_i * O_i) and -LSE_i * log2(e) are formed
+// here and written to the workspace for the dK/dV kernel that follows.
+//   d <= 64: O_i is staged with Q_i and dO_i, and the elementwise threads form D and
+//            -LSE * log2(e) themselves at the start of the item.
+//   d >= 80 (the three fixed tiles and the rings do not fit in shared memory together):
+//            a D warp reads the rows of O_i and dO_i from global memory, one item ahead of
+//            the elementwise threads, and hands D over through a shared buffer; the
+//            elementwise threads read LSE themselves.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const __grid_constant__ CUtensorMap tmO, const float* __restrict__ lse,
+                       const __grid_constant__ CUtensorMap tmO, const __nv_bfloat16* __restrict__ o,
+                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
                        float* __restrict__ ws_nlse2, float* __restrict__ ws_D, __nv_bfloat16* __restrict__ dq,
                        int T, int T_pad, int BH, int G, float scale, float scale_log2, uint32_t* __restrict__ err) {
-  constexpr int NFIX = PRE ? 3 : 2;
+  constexpr bool STAGED = D <= 64;  // O_i staged in shared memory (else the D warp)
+  constexpr int NFIX = STAGED ? 3 : 2;
   constexpr int KR = DqRing<D>::K, VR = DqRing<D>::V;
-  using C = BwdCfg<D, false, NFIX, 0, KR, VR>;
+  constexpr int DBUF = STAGED ? 0 : 512;
+  using C = DqCfg<D>;
   using TL = Tile<D>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
-  // with PRE the elementwise threads read O_i and dO_i themselves: they release them too
-  const BwdSmem sm = bwd_smem_setup<D, false, NFIX, 0, KR, VR>(smem_raw, tmem_slot, abort, PRE ? 1u + kEwThreads : 1u);
+  // with O_i staged the elementwise threads read O_i and dO_i themselves: they release them too
+  const BwdSmem sm =
+      bwd_smem_setup<D, false, NFIX, 0, KR, VR, DBUF>(smem_raw, tmem_slot, abort, STAGED ? 1u + kEwThreads : 1u);
   const Abort ab{abort, err};
   const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -958,6 +985,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
+      // K_j and V_j are read by every query tile of their head: keep them in L2; Q_i, dO_i once
+      const uint64_t keep = l2_evict_last(), once = l2_evict_first();
       bool ok = true;
       int g = 0, r = 0, fix_issued = 0, nk = 0, nv = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
@@ -966,19 +995,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (r >= NS && !(ok = mbar_wait(sm.fix_empty(slot), (r / NS - 1) & 1, ab, kErrTimeoutLoad))) break;
         ++fix_issued;
         mbar_arrive_expect_tx(sm.fix_full(slot), NFIX * TL::BYTES);
-        TL::load(sQf(slot), &tmQ, qt * kTileRows, bh, sm.fix_full(slot));
-        TL::load(sQf(slot) + TL::BYTES, &tmdO, qt * kTileRows, bh, sm.fix_full(slot));
-        if (PRE) TL::load(sQf(slot) + 2 * TL::BYTES, &tmO, qt * kTileRows, bh, sm.fix_full(slot));
+        TL::load(sQf(slot), &tmQ, qt * kTileRows, bh, sm.fix_full(slot), once);
+        TL::load(sQf(slot) + TL::BYTES, &tmdO, qt * kTileRows, bh, sm.fix_full(slot), once);
+        if (STAGED) TL::load(sQf(slot) + 2 * TL::BYTES, &tmO, qt * kTileRows, bh, sm.fix_full(slot), once);
         for (int it = 0; it < n_it; ++it, ++g) {
           const int sk = g % KR, sv = g % VR;
           // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
           if (g >= KR && !(ok = mbar_wait(sm.st_empty(sk), (g / KR - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(sm.st_full(sk), TL::BYTES);
-          TL::load(sK(sk), &tmK, it * kTileRows, bh / G, sm.st_full(sk));
+          TL::load(sK(sk), &tmK, it * kTileRows, bh / G, sm.st_full(sk), keep);
           ++nk;
           if (g >= VR && !(ok = mbar_wait(sm.v_empty(sv), (g / VR - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(sm.v_full(sv), TL::BYTES);
-          TL::load(sV(sv), &tmV, it * kTileRows, bh / G, sm.v_full(sv));
+          TL::load(sV(sv), &tmV, it * kTileRows, bh / G, sm.v_full(sv), keep);
           ++nv;
         }
       }
@@ -1052,6 +1081,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait_drain(sm.drain2(), 0, ab);
       }
     }
+  } else if (!STAGED && warp == kWarpD) {
+    // ------------------------------------------------------------ D warp (d >= 80)
+    // For each item, one ahead of the elementwise threads: D = rowsum(dO * O) of its 128
+    // rows, two rows per step (lanes 0-15 and 16-31, one 16-byte granule each), summed over
+    // a half-warp; D into the shared buffer, D and -LSE * log2(e) into the workspace.
+    constexpr int NG = D / 8;  // 16-byte granules per row: 10 (d = 80) or 16 (d = 128)
+    constexpr int U = 8;       // steps whose loads are in flight together
+    const int half = lane >> 4, gl = lane & 15;
+    float* sD = reinterpret_cast<float*>(sm.gbase + C::OFF_DBUF);
+    bool ok = true;
+    for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
+      const int qt = query_tile(u), bh = u % BH, row0 = qt * kTileRows;
+      // the elementwise threads have read the previous item's D
+      if (ri > 0 && !(ok = mbar_wait(sm.d_free(), (ri - 1) & 1, ab, kErrTimeoutElem))) break;
+      for (int s0 = 0; s0 < kTileRows / 2; s0 += U) {
+        uint4 ov[U], dv[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int row = row0 + 2 * (s0 + k) + half;
+          ov[k] = make_uint4(0u, 0u, 0u, 0u);
+          dv[k] = ov[k];
+          if (row < T && gl < NG) {
+            const size_t off = ((size_t)bh * T + row) * D + gl * 8;
+            ov[k] = __ldg(reinterpret_cast<const uint4*>(o + off));
+            dv[k] = __ldg(reinterpret_cast<const uint4*>(dO + off));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          float a0 = 0.f, a1 = 0.f;
+          fma_bf16x2_f32(ov[k].x, dv[k].x, a0, a1);
+          fma_bf16x2_f32(ov[k].y, dv[k].y, a0, a1);
+          fma_bf16x2_f32(ov[k].z, dv[k].z, a0, a1);
+          fma_bf16x2_f32(ov[k].w, dv[k].w, a0, a1);
+          float acc = a0 + a1;
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+          const int rr = 2 * (s0 + k) + half, row = row0 + rr;
+          if (gl == 0) {
+            const bool valid = row < T;
+            sD[rr] = acc;  // 0 past T
+            ws_D[(size_t)bh * T_pad + row] = acc;
+            ws_nlse2[(size_t)bh * T_pad + row] = valid ? -lse[(size_t)bh * T + row] * kLog2e : -INFINITY;
+          }
+        }
+      }
+      __syncwarp();
+      if (gl == 0) mbar_arrive(sm.d_full());  // lanes 0 and 16: their own rows' writes
+    }
   } else {
     // ------------------------------------------------------------ elementwise
     // thread owns query row qt*128 + r and key columns [32*hc, 32*hc + 32)
@@ -1077,7 +1155,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
       const int row = qt * kTileRows + r;
       float nl, Dr;
-      if constexpr (PRE) {
+      if constexpr (STAGED) {
         // D for this row from the staged O_i and dO_i rows (zero past T, as TMA fills them)
         const int slot = ri % NS;
         if (!(ok = mbar_wait_warp(sm.fix_full(slot), (ri / NS) & 1, ab, kErrTimeoutElem))) break;
@@ -1102,10 +1180,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ws_D[(size_t)bh * T_pad + row] = Dr;
         }
       } else {
-        nl = ws_nlse2[(size_t)bh * T_pad + row];
-        Dr = ws_D[(size_t)bh * T_pad + row];
+        // D comes from the D warp at the item's first dS
+        nl = row < T ? -lse[(size_t)bh * T + row] * kLog2e : -INFINITY;
+        Dr = 0.f;
       }
-      const uint64_t nl2 = f2_pack(nl, nl), D2 = f2_pack(Dr, Dr);
+      const uint64_t nl2 = f2_pack(nl, nl);
+      uint64_t D2 = f2_pack(Dr, Dr);
       for (int it = 0; it < n_it; ++it, ++g) {
         if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
@@ -1135,6 +1215,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (c >= lim) p[c] = 0.f;
+        }
+        if (!STAGED && it == 0) {
+          // this item's D from the D warp's shared buffer
+          if (!(ok = mbar_wait_warp(sm.d_full(), ri & 1, ab, kErrTimeoutElem))) break;
+          Dr = reinterpret_cast<const float*>(sm.gbase + C::OFF_DBUF)[r];
+          mbar_arrive(sm.d_free());
+          D2 = f2_pack(Dr, Dr);
         }
         if (!(ok = mbar_wait_warp(sm.dp_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
@@ -1316,19 +1403,20 @@ cudaError_t launch_dq_finish(const BwdArgs& a, cudaStream_t stream) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
-  // d <= 64: the dQ kernel forms D itself (and runs before dK/dV)
-  constexpr bool PRE = D <= 64;
-  using C = BwdCfg<D, false, PRE ? 3 : 2, 0, DqRing<D>::K, DqRing<D>::V>;
+  // the dQ kernel forms D itself (and runs before dK/dV): from a staged O_i at d <= 64,
+  // in its D warp at d >= 80
+  constexpr bool STAGED = D <= 64;
+  using C = DqCfg<D>;
   static_assert(C::SMEM_BYTES <= 227 * 1024, "dQ kernel shared memory");
-  auto kern = attn_bwd_dq_kernel<D, CAUSAL, PRE>;
+  auto kern = attn_bwd_dq_kernel<D, CAUSAL>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
-  if (PRE && (!a.tmO || !a.lse)) return cudaErrorInvalidValue;
+  if (!a.lse || (STAGED ? !a.tmO : (!a.o || !a.dO))) return cudaErrorInvalidValue;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
-  return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(kBwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
-                    *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.G,
-                    a.scale, a.scale * kLog2e, a.err);
+  return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
+                    *a.tmV, *a.tmdO, STAGED ? *a.tmO : *a.tmQ, a.o, a.dO, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T,
+                    a.T_pad, a.BH, a.G, a.scale, a.scale * kLog2e, a.err);
 }
 
 }  // namespace

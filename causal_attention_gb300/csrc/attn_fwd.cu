@@ -164,25 +164,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      // K and V tiles are read by every item of their head: keep them in L2; Q once
+      const uint64_t keep = l2_evict_last(), once = l2_evict_first();
       bool ok = true;
       int g = 0, r = 0, q_issued = 0, k_issued = 0, v_issued = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
         const int t = pair_of(u), bh = u % BH, nb = n_blocks(u, 1);
         if (r > 0 && !(ok = mbar_wait(q_empty, (r - 1) & 1, ab, kErrTimeoutLoad))) break;
         mbar_arrive_expect_tx(q_full, 2 * TL::BYTES);
-        TL::load(sQ, &tmQ, 2 * t * kTileRows, bh, q_full);
-        TL::load(sQ + TL::BYTES, &tmQ, (2 * t + 1) * kTileRows, bh, q_full);
+        TL::load(sQ, &tmQ, 2 * t * kTileRows, bh, q_full, once);
+        TL::load(sQ + TL::BYTES, &tmQ, (2 * t + 1) * kTileRows, bh, q_full, once);
         ++q_issued;
         for (int j = 0; j < nb; ++j, ++g) {
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(k_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(k_full(s), TL::BYTES);
           // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
-          TL::load(sK + s * TL::BYTES, &tmK, j * kTileRows, bh / G, k_full(s));
+          TL::load(sK + s * TL::BYTES, &tmK, j * kTileRows, bh / G, k_full(s), keep);
           ++k_issued;
           if (g >= ST && !(ok = mbar_wait(v_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
           mbar_arrive_expect_tx(v_full(s), TL::BYTES);
-          TL::load(sV + s * TL::BYTES, &tmV, j * kTileRows, bh / G, v_full(s));
+          TL::load(sV + s * TL::BYTES, &tmV, j * kTileRows, bh / G, v_full(s), keep);
           ++v_issued;
         }
       }

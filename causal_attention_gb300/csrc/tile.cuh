@@ -75,6 +75,13 @@ struct Tile {
 #pragma unroll
     for (int c = 0; c < NCHUNK; ++c) tma_load_3d(dst + c * CHUNK_BYTES, m, c * CHUNK_ELEMS, row0, bh, bar);
   }
+  // The same with an L2 cache policy (l2_evict_last / l2_evict_first).
+  static __device__ __forceinline__ void load(uint32_t dst, const CUtensorMap* m, int row0, int bh,
+                                              uint32_t bar, uint64_t policy) {
+#pragma unroll
+    for (int c = 0; c < NCHUNK; ++c)
+      tma_load_3d_hint(dst + c * CHUNK_BYTES, m, c * CHUNK_ELEMS, row0, bh, bar, policy);
+  }
 };
 
 // D[tmem] (+)= A[smem] B[smem] over NK K-steps of 16, both operands K-major (contraction

@@ -56,6 +56,19 @@ def run_oracle_all_heads(w: si.Workload, x, workers: int = 8):
     return oracle_pool.all_heads(w.scale, w.causal, x, workers)
 
 
+def compare(gpu, ref, heads=None):
+    """Error metrics over the compared heads (all heads if None)."""
+    out = {}
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        g = to_f64(gpu[name])
+        r = ref[name]
+        if heads is not None:
+            g = np.stack([g[b, h] for b, h in heads])
+            r = np.stack([r[b, h] for b, h in heads])
+        out[name] = (max_abs(g, r), rel_rms(g, r))
+    return out
+
+
 # Per-tile bar of the gradients: the whole-tensor bar applied to every 128-row tile of every
 # head, with a factor 2 for tiles whose norm is below the tensor's average. A tile with one
 # row wrong by about that row's own size has rel-RMS near sqrt(1/128) = 0.088 and fails it.
