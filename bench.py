@@ -1,8 +1,9 @@
 """Throughput of the fused causal attention forward + backward on GB300.
 
 One step = attn_fwd followed by attn_bwd over one batch of the workload, through the
-C ABI (the backward is the dQ kernel, which also forms D, then dK/dV; with --fused-dq,
-at d <= 64: D, dK/dV with dQ fused, dQ conversion). Prints ONE JSON line (rank 0).
+C ABI (at d <= 64 the backward is the dQ kernel, which also forms D, then dK/dV; at
+d = 80 and 128 D, dK/dV, dQ; with --fused-dq, at d <= 64: D, dK/dV with dQ fused, dQ
+conversion). Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -209,12 +210,14 @@ def variant(w, args):
 
 
 def kernels_for(d, fused_dq):
-    """The launches of one step, in order: the forward, then attn_bwd's stages (dQ, which
-    also forms D, then dK/dV), or with --fused-dq (d <= 64) the fused-dQ stages (D, dK/dV
-    with dQ formed inside, dQ conversion)."""
+    """The launches of one step, in order: the forward, then attn_bwd's stages (d <= 64:
+    dQ, which also forms D, then dK/dV; d = 80, 128: D, dK/dV, dQ), or with --fused-dq the
+    fused-dQ stages (D, dK/dV with dQ formed inside, dQ conversion)."""
     if fused_dq and d <= 64:
         return ("fwd", "bwd_preprocess", "bwd_dkdv_dq", "bwd_dq_finish")
-    return ("fwd", "bwd_dq", "bwd_dkdv")
+    if d <= 64:
+        return ("fwd", "bwd_dq", "bwd_dkdv")
+    return ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 
 
 def captured_traffic(workload, kernel):
@@ -380,10 +383,10 @@ def run_ours(args, rank, world, local):
     ws_bytes = (ca.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) if gqa else
                 (ca.attn_bwd_fused_workspace_size if fused else ca.attn_bwd_workspace_size)(B, H, T, d))
     per_set = 8 * B * H * T * d * 2 + B * H * T * 4 + ws_bytes
-    # attn_bwd_gqa: 2 launches, plus the sum of the split dK/dV when its workspace holds the
-    # partial sums
+    # attn_bwd_gqa: 2 (d <= 64) or 3 launches, plus the sum of the split dK/dV when its
+    # workspace holds the partial sums
     split = gqa and ws_bytes > ca.attn_bwd_workspace_size(B, H, T, d)
-    launches_per_step = 1 + 2 + int(split) if gqa else len(KERNELS)
+    launches_per_step = 1 + (2 if d <= 64 else 3) + int(split) if gqa else len(KERNELS)
     n_sets = max(2, -(-3 * L2_BYTES // per_set))
     if gqa:  # key/value heads: the seeded bytes of the first H_kv heads
         import numpy as np
@@ -741,13 +744,13 @@ def run_block(args, rank, world, local):
     top = max(mean_ms, key=mean_ms.get)
     achieved = flops[top] / (mean_ms[top] * 1e-3) / 1e12
     # kernel launches per step: qkv 1; attention fwd 1; out 1; out bwd 2 (+1 split-K sum);
-    # attention bwd 2 (+1 split dK/dV sum); qkv bwd 1 rotation (dQ and dK) + 2 (+1)
+    # attention bwd 2 (d <= 64) or 3 (+1 split dK/dV sum); qkv bwd 1 rotation (dQ and dK) + 2 (+1)
     # (the projections' tn products take B * ceil(T / 64) K-steps of 64 tokens)
     k_tok = B * ((T + 63) // 64) * 64
     n_red_o = int(ca.attn_gemm_workspace_size(C, H * d, k_tok, "tn") > 0)
     n_red_q = int(ca.attn_gemm_workspace_size(n_qkv, C, k_tok, "tn") > 0)
     split_kv = H_kv != H and ca.attn_bwd_gqa_workspace_size(B, H, H_kv, T, d) > ca.attn_bwd_workspace_size(B, H, T, d)
-    launches = 1 + 1 + 1 + 2 + n_red_o + 2 + int(split_kv) + 1 + 2 + n_red_q
+    launches = 1 + 1 + 1 + 2 + n_red_o + (2 if d <= 64 else 3) + int(split_kv) + 1 + 2 + n_red_q
     line = {
         "metric": "attention block training step TFLOP/s (bf16): QKV projection + RoPE, causal attention, "
                   "output projection, forward and backward",

@@ -642,8 +642,6 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void*
   CUtensorMap maps[5];
   ATTN_TRY(bwd_args(&a, q, k, v, dO, workspace, B, H, T, d, scale, causal, maps, true));
   ATTN_TRY(bwd_map_o(&a, o, &maps[4]));
-  a.o = static_cast<const __nv_bfloat16*>(o);
-  a.dO = static_cast<const __nv_bfloat16*>(dO);
   a.lse = lse;
   a.dq = static_cast<__nv_bfloat16*>(dq);
   return launched(launch_bwd_dq(a, static_cast<cudaStream_t>(stream)));
@@ -688,9 +686,14 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
   a.dv = static_cast<__nv_bfloat16*>(dv);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   a.dq_cnt = nullptr;  // the fused dQ's counters are not used here
-  // the dQ kernel writes D and -LSE*log2(e) itself, then dK/dV reads them
-  ATTN_TRY(launched(launch_bwd_dq(a, s)));
-  return launched(launch_bwd_dkdv(a, s));
+  if (d <= 64) {
+    // the dQ kernel writes D and -LSE*log2(e) itself, then dK/dV reads them
+    ATTN_TRY(launched(launch_bwd_dq(a, s)));
+    return launched(launch_bwd_dkdv(a, s));
+  }
+  ATTN_TRY(launched(launch_bwd_preprocess(a, s)));
+  ATTN_TRY(launched(launch_bwd_dkdv(a, s)));
+  return launched(launch_bwd_dq(a, s));
 }
 
 attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,

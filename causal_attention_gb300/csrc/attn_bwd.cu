@@ -39,61 +39,75 @@ namespace attn {
 
 namespace {
 
-// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers, 19 (fused dQ) reducer or
-// (dQ kernel at d >= 80) the D warp
+// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers, 19 (fused dQ) reducer
 constexpr int kBwdThreads = 608;
-constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18, kWarpRed = 19, kWarpD = 19;
+constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18, kWarpRed = 19;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
 // 1. preprocess
 // ---------------------------------------------------------------------------
 // With the fused dQ it also zeroes the per-tile ordering counters (dq_cnt, n_cnt entries).
+//
+// HBM-bound. CTA c takes rows t = 64x .. 64x + 63 of slice bh, c = bh * (T_pad / 64) + x
+// (padding rows t >= T included), TPR threads per row reading 16-byte granules. Every load of a thread
+// (its granules of O and dO in PRE_U rows, and LSE) is issued before any of them is used,
+// so one round trip to memory serves the whole CTA.
+constexpr int kPreRows = 64, kPreThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
+__global__ void __launch_bounds__(kPreThreads) attn_bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
     const float* __restrict__ lse, float* __restrict__ ws_nlse2, float* __restrict__ ws_D, int* __restrict__ dq_cnt,
-    int n_cnt, int T, int T_pad, int BH) {
+    int n_cnt, int T, int T_pad) {
   constexpr int NG = D / 8;                             // 16-byte granules per row
   constexpr int TPR = (NG & (NG - 1)) == 0 ? NG : 8;    // threads per row (a power of two)
-  constexpr int RPW = 32 / TPR;                         // rows per warp step
+  constexpr int RPP = kPreThreads / TPR;                // rows per pass
+  constexpr int U = kPreRows / RPP;                     // rows per thread
+  constexpr int GPT = (NG + TPR - 1) / TPR;             // granules per thread and row
   griddep_begin();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_cnt; i += gridDim.x * blockDim.x) dq_cnt[i] = 0;
-  const int lane = threadIdx.x & 31;
-  const int sub = lane % TPR;
-  const long long total = (long long)BH * T_pad;
-  const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long base = warp_id * RPW; base < total; base += n_warps * RPW) {
-    const long long row = base + lane / TPR;
-    float acc = 0.f;
-    int t = 0, bh = 0;
-    const bool in_range = row < total;
-    if (in_range) {
-      bh = (int)(row / T_pad);
-      t = (int)(row % T_pad);
-      // granules sub, sub + TPR, ... of the row (one each unless d = 80)
-      for (int gi = sub; in_range && t < T && gi < NG; gi += TPR) {
-        const size_t off = ((size_t)bh * T + t) * D + gi * 8;
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + off));
-        const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + off));
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_cnt;
+       i += (long long)gridDim.x * blockDim.x)
+    dq_cnt[i] = 0;
+  const int n_ch = T_pad / kPreRows;
+  const int bh = (int)(blockIdx.x / n_ch), sub = threadIdx.x % TPR;
+  const int t0 = (int)(blockIdx.x % n_ch) * kPreRows + threadIdx.x / TPR;
+  const __nv_bfloat16* ob = o + (size_t)bh * T * D;
+  const __nv_bfloat16* db = dO + (size_t)bh * T * D;
+  uint4 a[U][GPT], b[U][GPT];
+  float L[U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 fa = __bfloat1622float2(pa[i]);
-          const float2 fb = __bfloat1622float2(pb[i]);
-          acc = fmaf(fa.x, fb.x, acc);
-          acc = fmaf(fa.y, fb.y, acc);
-        }
+  for (int u = 0; u < U; ++u) {
+    const int t = t0 + u * RPP;
+    L[u] = (sub == 0 && t < T) ? lse[(size_t)bh * T + t] : 0.f;
+#pragma unroll
+    for (int k = 0; k < GPT; ++k) {
+      const int gi = sub + k * TPR;
+      a[u][k] = make_uint4(0u, 0u, 0u, 0u);
+      b[u][k] = a[u][k];
+      if (t < T && gi < NG) {
+        a[u][k] = ldg_stream(ob + (size_t)t * D + gi * 8);
+        b[u][k] = ldg_stream(db + (size_t)t * D + gi * 8);
       }
     }
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < GPT; ++k) {
+      fma_bf16x2_f32(a[u][k].x, b[u][k].x, a0, a1);
+      fma_bf16x2_f32(a[u][k].y, b[u][k].y, a0, a1);
+      fma_bf16x2_f32(a[u][k].z, b[u][k].z, a0, a1);
+      fma_bf16x2_f32(a[u][k].w, b[u][k].w, a0, a1);
+    }
+    float acc = a0 + a1;
 #pragma unroll
     for (int w = TPR / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (in_range && sub == 0) {
-      const bool valid = t < T;
-      ws_D[row] = valid ? acc : 0.f;
-      ws_nlse2[row] = valid ? -lse[(size_t)bh * T + t] * kLog2e : -INFINITY;
+    const int t = t0 + u * RPP;
+    if (sub == 0 && t < T_pad) {
+      ws_D[(size_t)bh * T_pad + t] = acc;  // 0 on padding rows
+      ws_nlse2[(size_t)bh * T_pad + t] = t < T ? -L[u] * kLog2e : -INFINITY;
     }
   }
 }
@@ -105,8 +119,7 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(
 // dQ kernel computes D itself, O_i). NEPI: bf16 output tiles staged in shared memory for
 // a TMA store in the epilogue (dV and dK).
 // KRING, VRING (dQ kernel): separate rings of K and V tiles instead of the stages.
-// DBUF (dQ kernel at d >= 80): bytes of the shared D buffer its D warp fills per item.
-template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0, int DBUF = 0>
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0>
 struct BwdCfg {
   using TL = Tile<D>;
   static constexpr int STAGES = (D > 64) ? 2 : (D == 64 ? 3 : 4);
@@ -127,12 +140,10 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_STAGE + STAGE_AREA;
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_EPI = OFF_DQS + DQS_BYTES;
-  static constexpr int OFF_DBUF = OFF_EPI + NEPI * TL::BYTES;
-  static constexpr int OFF_BAR = OFF_DBUF + DBUF;
-  // barrier rings: st_full / st_empty (the stages, or the K ring) and v_full / v_empty;
-  // then d_full / d_free
+  static constexpr int OFF_BAR = OFF_EPI + NEPI * TL::BYTES;
+  // barrier rings: st_full / st_empty (the stages, or the K ring) and v_full / v_empty
   static constexpr int RB = KRING > STAGES ? KRING : STAGES;
-  static constexpr int NBAR = 1 + 2 * RB + 22 + 2 * VRING + 2;
+  static constexpr int NBAR = 1 + 2 * RB + 22 + 2 * VRING;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // at least 116 KB so that one CTA occupies an SM: each CTA allocates all 512
   // TMEM columns, and a second resident CTA would only wait for them
@@ -144,7 +155,7 @@ struct BwdCfg {
   static constexpr uint32_t COL_P = 384, COL_DS = 448;
   // fused dQ: dQ_ij (fp32, d columns) takes the columns of dS^T, which lives in shared memory
   static constexpr uint32_t COL_DQ = 448;
-  static constexpr int THREADS = (FUSE || DBUF) ? kBwdThreads + 32 : kBwdThreads;
+  static constexpr int THREADS = FUSE ? kBwdThreads + 32 : kBwdThreads;
   static_assert(!FUSE || SEP_DKDV, "the fused dQ needs the separate P^T columns (d <= 64)");
 };
 
@@ -186,19 +197,16 @@ struct BwdSmem {
   // dQ kernel: the V ring (its K ring uses st_full / st_empty)
   __device__ uint32_t v_full(int s) const { return bar0 + 8u * (23 + 2 * st + s); }
   __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (23 + 2 * st + vr + s); }
-  // dQ kernel with a D warp: the item's D values are in the shared buffer / were read
-  __device__ uint32_t d_full() const { return bar0 + 8u * (23 + 2 * st + 2 * vr); }
-  __device__ uint32_t d_free() const { return bar0 + 8u * (24 + 2 * st + 2 * vr); }
 };
 
 constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
 // fix_empty_count: arrivals that release an item's fixed tiles (the MMA commit, plus the
 // elementwise threads where they read a fixed tile themselves).
-template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0, int DBUF = 0>
+template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
                                                   volatile int*& abort, uint32_t fix_empty_count = 1) {
-  using C = BwdCfg<D, FUSE, NFIX, NEPI, KRING, VRING, DBUF>;
+  using C = BwdCfg<D, FUSE, NFIX, NEPI, KRING, VRING>;
   BwdSmem s;
   const uint32_t raw = smem_u32(smem_raw);
   s.base = (raw + 1023u) & ~1023u;
@@ -234,10 +242,6 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     mbar_init(s.drain(), 1);
     mbar_init(s.drain2(), 1);
     mbar_init(s.epi_free(), 1);
-    if (DBUF) {
-      mbar_init(s.d_full(), 2);  // lanes 0 and 16 of the D warp
-      mbar_init(s.d_free(), kEwThreads);
-    }
     if (FUSE) {
       mbar_init(s.dq_done(), 1);
       mbar_init(s.dq_free(), kEwThreads);
@@ -914,11 +918,6 @@ struct DqRing {
   static constexpr int V = D > 64 ? 2 : BwdCfg<D>::STAGES;
 };
 
-// The dQ kernel's shared-memory plan: at d <= 64 O_i is staged as a third fixed tile; at
-// d >= 80 (no room for it) the D warp's 128-float D buffer instead.
-template <int D>
-using DqCfg = BwdCfg<D, false, D <= 64 ? 3 : 2, 0, DqRing<D>::K, DqRing<D>::V, D <= 64 ? 0 : 512>;
-
 // Work item = one 128-query tile i of one (b, h); its iterations run over the key tiles
 // j (j <= i when causal). Persistent, two MMA issuers:
 //   warp 17: S_j = Q_i K_j^T as soon as S_{j-1} was read out, dP_j = dO_i V_j^T likewise;
@@ -926,35 +925,26 @@ using DqCfg = BwdCfg<D, false, D <= 64 ? 3 : 2, 0, DqRing<D>::K, DqRing<D>::V, D
 // At d <= 64 the dQ accumulator has two TMEM buffers (items alternate), and the
 // elementwise warps store an item's dQ during the next item's first iteration, by when
 // its last dQ MMA has finished, instead of waiting for it at the end of the item.
-// The kernel also does the preprocess for its query tile, so that it runs first and no
-// separate D launch is needed: D_i = rowsum(dO_i * O_i) and -LSE_i * log2(e) are formed
-// here and written to the workspace for the dK/dV kernel that follows.
-//   d <= 64: O_i is staged with Q_i and dO_i, and the elementwise threads form D and
-//            -LSE * log2(e) themselves at the start of the item.
-//   d >= 80 (the three fixed tiles and the rings do not fit in shared memory together):
-//            a D warp reads the rows of O_i and dO_i from global memory, one item ahead of
-//            the elementwise threads, and hands D over through a shared buffer; the
-//            elementwise threads read LSE themselves.
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
+// PRE (d <= 64): the kernel also does the preprocess for its query tile, so that it runs
+// first and no separate D launch is needed: O_i is staged with Q_i and dO_i, the
+// elementwise threads form D_i = rowsum(dO_i * O_i) and -LSE_i * log2(e) themselves at the
+// start of the item and write both to the workspace for the dK/dV kernel that follows.
+template <int D, bool CAUSAL, bool PRE>
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const __grid_constant__ CUtensorMap tmO, const __nv_bfloat16* __restrict__ o,
-                       const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
+                       const __grid_constant__ CUtensorMap tmO, const float* __restrict__ lse,
                        float* __restrict__ ws_nlse2, float* __restrict__ ws_D, __nv_bfloat16* __restrict__ dq,
                        int T, int T_pad, int BH, int G, float scale, float scale_log2, uint32_t* __restrict__ err) {
-  constexpr bool STAGED = D <= 64;  // O_i staged in shared memory (else the D warp)
-  constexpr int NFIX = STAGED ? 3 : 2;
+  constexpr int NFIX = PRE ? 3 : 2;
   constexpr int KR = DqRing<D>::K, VR = DqRing<D>::V;
-  constexpr int DBUF = STAGED ? 0 : 512;
-  using C = DqCfg<D>;
+  using C = BwdCfg<D, false, NFIX, 0, KR, VR>;
   using TL = Tile<D>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
-  // with O_i staged the elementwise threads read O_i and dO_i themselves: they release them too
-  const BwdSmem sm =
-      bwd_smem_setup<D, false, NFIX, 0, KR, VR, DBUF>(smem_raw, tmem_slot, abort, STAGED ? 1u + kEwThreads : 1u);
+  // with PRE the elementwise threads read O_i and dO_i themselves: they release them too
+  const BwdSmem sm = bwd_smem_setup<D, false, NFIX, 0, KR, VR>(smem_raw, tmem_slot, abort, PRE ? 1u + kEwThreads : 1u);
   const Abort ab{abort, err};
   const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -997,7 +987,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(sm.fix_full(slot), NFIX * TL::BYTES);
         TL::load(sQf(slot), &tmQ, qt * kTileRows, bh, sm.fix_full(slot), once);
         TL::load(sQf(slot) + TL::BYTES, &tmdO, qt * kTileRows, bh, sm.fix_full(slot), once);
-        if (STAGED) TL::load(sQf(slot) + 2 * TL::BYTES, &tmO, qt * kTileRows, bh, sm.fix_full(slot), once);
+        if (PRE) TL::load(sQf(slot) + 2 * TL::BYTES, &tmO, qt * kTileRows, bh, sm.fix_full(slot), once);
         for (int it = 0; it < n_it; ++it, ++g) {
           const int sk = g % KR, sv = g % VR;
           // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
@@ -1081,55 +1071,6 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mbar_wait_drain(sm.drain2(), 0, ab);
       }
     }
-  } else if (!STAGED && warp == kWarpD) {
-    // ------------------------------------------------------------ D warp (d >= 80)
-    // For each item, one ahead of the elementwise threads: D = rowsum(dO * O) of its 128
-    // rows, two rows per step (lanes 0-15 and 16-31, one 16-byte granule each), summed over
-    // a half-warp; D into the shared buffer, D and -LSE * log2(e) into the workspace.
-    constexpr int NG = D / 8;  // 16-byte granules per row: 10 (d = 80) or 16 (d = 128)
-    constexpr int U = 8;       // steps whose loads are in flight together
-    const int half = lane >> 4, gl = lane & 15;
-    float* sD = reinterpret_cast<float*>(sm.gbase + C::OFF_DBUF);
-    bool ok = true;
-    for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
-      const int qt = query_tile(u), bh = u % BH, row0 = qt * kTileRows;
-      // the elementwise threads have read the previous item's D
-      if (ri > 0 && !(ok = mbar_wait(sm.d_free(), (ri - 1) & 1, ab, kErrTimeoutElem))) break;
-      for (int s0 = 0; s0 < kTileRows / 2; s0 += U) {
-        uint4 ov[U], dv[U];
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-          const int row = row0 + 2 * (s0 + k) + half;
-          ov[k] = make_uint4(0u, 0u, 0u, 0u);
-          dv[k] = ov[k];
-          if (row < T && gl < NG) {
-            const size_t off = ((size_t)bh * T + row) * D + gl * 8;
-            ov[k] = __ldg(reinterpret_cast<const uint4*>(o + off));
-            dv[k] = __ldg(reinterpret_cast<const uint4*>(dO + off));
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-          float a0 = 0.f, a1 = 0.f;
-          fma_bf16x2_f32(ov[k].x, dv[k].x, a0, a1);
-          fma_bf16x2_f32(ov[k].y, dv[k].y, a0, a1);
-          fma_bf16x2_f32(ov[k].z, dv[k].z, a0, a1);
-          fma_bf16x2_f32(ov[k].w, dv[k].w, a0, a1);
-          float acc = a0 + a1;
-#pragma unroll
-          for (int w = 8; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-          const int rr = 2 * (s0 + k) + half, row = row0 + rr;
-          if (gl == 0) {
-            const bool valid = row < T;
-            sD[rr] = acc;  // 0 past T
-            ws_D[(size_t)bh * T_pad + row] = acc;
-            ws_nlse2[(size_t)bh * T_pad + row] = valid ? -lse[(size_t)bh * T + row] * kLog2e : -INFINITY;
-          }
-        }
-      }
-      __syncwarp();
-      if (gl == 0) mbar_arrive(sm.d_full());  // lanes 0 and 16: their own rows' writes
-    }
   } else {
     // ------------------------------------------------------------ elementwise
     // thread owns query row qt*128 + r and key columns [32*hc, 32*hc + 32)
@@ -1155,7 +1096,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
       const int row = qt * kTileRows + r;
       float nl, Dr;
-      if constexpr (STAGED) {
+      if constexpr (PRE) {
         // D for this row from the staged O_i and dO_i rows (zero past T, as TMA fills them)
         const int slot = ri % NS;
         if (!(ok = mbar_wait_warp(sm.fix_full(slot), (ri / NS) & 1, ab, kErrTimeoutElem))) break;
@@ -1180,12 +1121,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           ws_D[(size_t)bh * T_pad + row] = Dr;
         }
       } else {
-        // D comes from the D warp at the item's first dS
-        nl = row < T ? -lse[(size_t)bh * T + row] * kLog2e : -INFINITY;
-        Dr = 0.f;
+        nl = ws_nlse2[(size_t)bh * T_pad + row];
+        Dr = ws_D[(size_t)bh * T_pad + row];
       }
-      const uint64_t nl2 = f2_pack(nl, nl);
-      uint64_t D2 = f2_pack(Dr, Dr);
+      const uint64_t nl2 = f2_pack(nl, nl), D2 = f2_pack(Dr, Dr);
       for (int it = 0; it < n_it; ++it, ++g) {
         if (!(ok = mbar_wait_warp(sm.s_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
@@ -1215,13 +1154,6 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (c >= lim) p[c] = 0.f;
-        }
-        if (!STAGED && it == 0) {
-          // this item's D from the D warp's shared buffer
-          if (!(ok = mbar_wait_warp(sm.d_full(), ri & 1, ab, kErrTimeoutElem))) break;
-          Dr = reinterpret_cast<const float*>(sm.gbase + C::OFF_DBUF)[r];
-          mbar_arrive(sm.d_free());
-          D2 = f2_pack(Dr, Dr);
         }
         if (!(ok = mbar_wait_warp(sm.dp_full(), g & 1, ab, kErrTimeoutElem))) break;
         tc_fence_after();
@@ -1359,15 +1291,11 @@ __global__ void __launch_bounds__(256) attn_bwd_dkdv_reduce_kernel(const float* 
 // ---------------------------------------------------------------------------
 template <int D>
 cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
-  const long long rows = (long long)a.BH * a.T_pad;
-  constexpr int NG = D / 8;
-  constexpr int rows_per_block = 256 / ((NG & (NG - 1)) == 0 ? NG : 8);
-  long long blocks = (rows + rows_per_block - 1) / rows_per_block;
-  const long long cap = (long long)a.num_sms * 8;  // grid-stride beyond 8 blocks per SM
-  if (blocks > cap) blocks = cap;
+  // one CTA per 64 rows of each slice (T_pad is a multiple of 64)
+  const dim3 grid((unsigned)((long long)a.T_pad / kPreRows * a.BH));
   const int n_cnt = a.dq_cnt ? a.BH * (a.T_pad / kTileRows) : 0;
-  return launch_pdl(attn_bwd_preprocess_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, stream, a.o, a.dO, a.lse,
-                    a.ws_nlse2, a.ws_D, a.dq_cnt, n_cnt, a.T, a.T_pad, a.BH);
+  return launch_pdl(attn_bwd_preprocess_kernel<D>, grid, dim3(kPreThreads), 0, stream, a.o, a.dO, a.lse, a.ws_nlse2,
+                    a.ws_D, a.dq_cnt, n_cnt, a.T, a.T_pad);
 }
 
 template <int D, bool CAUSAL, bool FUSE, bool SPLIT = false>
@@ -1403,20 +1331,19 @@ cudaError_t launch_dq_finish(const BwdArgs& a, cudaStream_t stream) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
-  // the dQ kernel forms D itself (and runs before dK/dV): from a staged O_i at d <= 64,
-  // in its D warp at d >= 80
-  constexpr bool STAGED = D <= 64;
-  using C = DqCfg<D>;
+  // d <= 64: the dQ kernel forms D itself (and runs before dK/dV)
+  constexpr bool PRE = D <= 64;
+  using C = BwdCfg<D, false, PRE ? 3 : 2, 0, DqRing<D>::K, DqRing<D>::V>;
   static_assert(C::SMEM_BYTES <= 227 * 1024, "dQ kernel shared memory");
-  auto kern = attn_bwd_dq_kernel<D, CAUSAL>;
+  auto kern = attn_bwd_dq_kernel<D, CAUSAL, PRE>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
-  if (!a.lse || (STAGED ? !a.tmO : (!a.o || !a.dO))) return cudaErrorInvalidValue;
+  if (PRE && (!a.tmO || !a.lse)) return cudaErrorInvalidValue;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
-  return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
-                    *a.tmV, *a.tmdO, STAGED ? *a.tmO : *a.tmQ, a.o, a.dO, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T,
-                    a.T_pad, a.BH, a.G, a.scale, a.scale * kLog2e, a.err);
+  return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(kBwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
+                    *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.G,
+                    a.scale, a.scale * kLog2e, a.err);
 }
 
 }  // namespace

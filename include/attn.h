@@ -95,14 +95,15 @@ size_t attn_bwd_fused_workspace_size(int B, int H, int T, int d);
 /*
  * Backward. Cited definition: Forge RESEARCH.md section 6, "The D term is free"
  * and "Backward (training)"; the three-stage atomic-free structure of the Forge
- * paper's "Ecosystem survey". Equivalent to, on the same stream: attn_bwd_dq (which
- * also forms D, stage 1's work) then attn_bwd_dkdv.
+ * paper's "Ecosystem survey". Equivalent to, on the same stream: at d <= 64
+ * attn_bwd_dq (which also forms D) then attn_bwd_dkdv; at d >= 80 attn_bwd_preprocess,
+ * attn_bwd_dkdv, attn_bwd_dq.
  *   q, k, v, o, dO : bf16 [B, H, T, d] (o and lse as written by attn_fwd)
  *   lse            : fp32 [B, H, T]
  *   dq, dk, dv     : bf16 [B, H, T, d] outputs
  *   workspace      : >= attn_bwd_workspace_size(B, H, T, d) bytes of device memory,
  *                    16-byte aligned; its contents on entry do not matter
- * Two kernel launches.
+ * Two kernel launches at d <= 64, three at d >= 80.
  */
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                      const float* lse, void* dq, void* dk, void* dv, void* workspace,
@@ -133,8 +134,7 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
                          int causal, void* stream);
 
 /* Backward stage 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace
- * (Forge RESEARCH.md section 6, "The D term is free"). Memory-bound. attn_bwd does not
- * call it (attn_bwd_dq does the same work); the fused dQ path does. With d <= 64 and a
+ * (Forge RESEARCH.md section 6, "The D term is free"). Memory-bound. With d <= 64 and a
  * workspace of attn_bwd_fused_workspace_size bytes it also zeroes the fused dQ's
  * counters, so it must run before every attn_bwd_dkdv_dq. */
 attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
@@ -142,17 +142,18 @@ attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse,
 
 /* Backward stage 2: dK and dV, one CTA per 128-key tile looping over query tiles
  * (Forge paper, "Attention kernel design": transposes by operand-role swap).
- * Reads the D / LSE workspace written by stage 1 or by attn_bwd_dq. */
+ * Reads the D / LSE workspace written by stage 1 or, at d <= 64, by attn_bwd_dq. */
 attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
                           void* dv, const void* workspace, size_t workspace_bytes, int B, int H,
                           int T, int d, float scale, int causal, void* stream);
 
 /* Backward stage 3: dQ, one CTA per 128-query tile looping over key tiles
  * (deterministic; Forge RESEARCH.md section 6, "a dQ kernel with grid (NQ, H, B)").
- * It does stage 1's work for its own query tile (D = rowsum(dO * O), -LSE * log2(e)
+ * At d >= 80 it reads the workspace written by stage 1. At d <= 64 it does stage 1's
+ * work for its own query tile (D = rowsum(dO * O) from a staged O tile, -LSE * log2(e)
  * from lse) and writes both into the workspace, so it needs no stage 1 before it and
- * attn_bwd_dkdv may follow it. D is formed from a staged O tile at d <= 64 and by a
- * warp that reads the rows of O and dO from memory at d >= 80. */
+ * attn_bwd_dkdv may follow it; o and lse are read only at d <= 64 but are always
+ * checked. */
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* o, const void* dO,
                         const float* lse, void* dq, void* workspace, size_t workspace_bytes, int B, int H,
                         int T, int d, float scale, int causal, void* stream);

@@ -37,10 +37,10 @@ def test_kernel_flops_add_up_to_the_algorithmic_gemms():
 
 @pytest.mark.parametrize("d,fused,expect", [
     (32, False, ("fwd", "bwd_dq", "bwd_dkdv")), (64, False, ("fwd", "bwd_dq", "bwd_dkdv")),
-    (80, False, ("fwd", "bwd_dq", "bwd_dkdv")),
-    (128, False, ("fwd", "bwd_dq", "bwd_dkdv")),
+    (80, False, ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")),
+    (128, False, ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")),
     (64, True, ("fwd", "bwd_preprocess", "bwd_dkdv_dq", "bwd_dq_finish")),
-    (128, True, ("fwd", "bwd_dq", "bwd_dkdv")),
+    (128, True, ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")),
 ])
 def test_launch_list(d, fused, expect):
     assert bench.kernels_for(d, fused) == expect
