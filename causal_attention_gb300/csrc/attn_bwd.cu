@@ -39,9 +39,10 @@ namespace attn {
 
 namespace {
 
-// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers, 19 (fused dQ) reducer
+// warps 0-15 elementwise, 16 producer, 17 and 18 MMA issuers, 19 (fused dQ) reducer or
+// (dQ kernel at d >= 80) third MMA issuer
 constexpr int kBwdThreads = 608;
-constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18, kWarpRed = 19;
+constexpr int kWarpProd = 16, kWarpMmaA = 17, kWarpMmaB = 18, kWarpRed = 19, kWarpMmaC = 19;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -201,11 +202,13 @@ struct BwdSmem {
 
 constexpr int kEwThreads = 512;  // four elementwise warpgroups
 
-// fix_empty_count: arrivals that release an item's fixed tiles (the MMA commit, plus the
-// elementwise threads where they read a fixed tile themselves).
+// fix_empty_count: arrivals that release an item's fixed tiles (the MMA commits, plus the
+// elementwise threads where they read a fixed tile themselves). issuers: MMA-issuing
+// threads whose commits each release a stage and complete an item's accumulators.
 template <int D, bool FUSE = false, int NFIX = 2, int NEPI = 0, int KRING = 0, int VRING = 0>
 __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& tmem_slot,
-                                                  volatile int*& abort, uint32_t fix_empty_count = 1) {
+                                                  volatile int*& abort, uint32_t fix_empty_count = 1,
+                                                  uint32_t issuers = 1) {
   using C = BwdCfg<D, FUSE, NFIX, NEPI, KRING, VRING>;
   BwdSmem s;
   const uint32_t raw = smem_u32(smem_raw);
@@ -223,7 +226,7 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     }
     for (int i = 0; i < C::RB; ++i) {
       mbar_init(s.st_full(i), 1);
-      mbar_init(s.st_empty(i), 1);
+      mbar_init(s.st_empty(i), issuers);
     }
     for (int i = 0; i < VRING; ++i) {
       mbar_init(s.v_full(i), 1);
@@ -237,7 +240,7 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
     mbar_init(s.dp_free(), kEwThreads);
     mbar_init(s.dv_done(), 1);
     mbar_init(s.dk_done(), 1);
-    mbar_init(s.acc_full(), 1);
+    mbar_init(s.acc_full(), issuers);
     mbar_init(s.acc_free(), kEwThreads);
     mbar_init(s.drain(), 1);
     mbar_init(s.drain2(), 1);
@@ -247,8 +250,8 @@ __device__ __forceinline__ BwdSmem bwd_smem_setup(uint8_t* smem_raw, uint32_t*& 
       mbar_init(s.dq_free(), kEwThreads);
       mbar_init(s.dqs_full(), kEwThreads);
       mbar_init(s.dqs_free(), 1);
-      mbar_init(s.drain3(), 1);
     }
+    mbar_init(s.drain3(), 1);
     *abort = 0;
     fence_barrier_init();
   }
@@ -929,8 +932,14 @@ struct DqRing {
 // first and no separate D launch is needed: O_i is staged with Q_i and dO_i, the
 // elementwise threads form D_i = rowsum(dO_i * O_i) and -LSE_i * log2(e) themselves at the
 // start of the item and write both to the workspace for the dK/dV kernel that follows.
+// At d >= 80 the S and dP MMAs (eight K-steps each) get one thread each (warp 17 and a
+// third issuer, warp 19): a thread issues one tcgen05.mma about every hundred cycles
+// however short the MMA, and one thread issuing both bounded the iteration.
+template <int D>
+constexpr int dq_threads() { return D > 64 ? kBwdThreads + 32 : kBwdThreads; }
+
 template <int D, bool CAUSAL, bool PRE>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(dq_threads<D>(), 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ CUtensorMap tmO, const float* __restrict__ lse,
@@ -943,8 +952,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint32_t* tmem_slot;
   volatile int* abort;
-  // with PRE the elementwise threads read O_i and dO_i themselves: they release them too
-  const BwdSmem sm = bwd_smem_setup<D, false, NFIX, 0, KR, VR>(smem_raw, tmem_slot, abort, PRE ? 1u + kEwThreads : 1u);
+  // with PRE the elementwise threads read O_i and dO_i themselves: they release them too;
+  // with a separate dP issuer (d >= 80) Q_i and dO_i are released by two MMA threads
+  constexpr bool SPLIT_SDP = D > 64;
+  const BwdSmem sm = bwd_smem_setup<D, false, NFIX, 0, KR, VR>(smem_raw, tmem_slot, abort,
+                                                               PRE ? 1u + kEwThreads : (SPLIT_SDP ? 2u : 1u));
   const Abort ab{abort, err};
   const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1006,9 +1018,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int x = max(0, nv - VR); x < nv; ++x) mbar_wait_drain(sm.v_full(x % VR), (x / VR) & 1, ab);
       }
     }
-  } else if (warp == kWarpMmaA) {
-    // ------------------------------------------------------------ MMA issuer (S, dP)
+  } else if (warp == kWarpMmaA || (SPLIT_SDP && warp == kWarpMmaC)) {
+    // ------------------------------------------------------------ MMA issuers (S, dP)
+    // warp 17: S and dP (d <= 64), or S alone (d >= 80, with warp 19 issuing dP)
     if (lane == 0) {
+      const bool do_S = warp == kWarpMmaA, do_dP = !SPLIT_SDP || warp == kWarpMmaC;
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       const uint32_t tS = tmem, tDP = tmem + 128u;
       const uint64_t dKk0 = TL::desc_kmajor0(sK(0)), dVk0 = TL::desc_kmajor0(sV(0));
@@ -1020,25 +1034,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dQk = TL::desc_kmajor0(sQf(slot)), dOk = TL::desc_kmajor0(sQf(slot) + TL::BYTES);
         for (int it = 0; it < n_it; ++it, ++g) {
           const int sk = g % KR, sv = g % VR;
-          if (g > 0 && !(ok = mbar_wait(sm.s_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // S read out
-          if (!(ok = mbar_wait(sm.st_full(sk), (g / KR) & 1, ab, kErrTimeoutMma))) break;
-          tc_fence_after();
-          // S = Q_i K_j^T (M = queries, N = keys, K = d)
-          mma_chain_ss<TL, TL::KSTEPS_D>(tS, dQk, dKk0 + (uint64_t)sk * kSlotOff, idesc_s, 0u);
-          mma_commit(sm.s_full());
-          if (g > 0 && !(ok = mbar_wait(sm.dp_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // dP read out
-          if (!(ok = mbar_wait(sm.v_full(sv), (g / VR) & 1, ab, kErrTimeoutMma))) break;
-          tc_fence_after();
-          // dP = dO_i V_j^T
-          mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)sv * kSlotOff, idesc_s, 0u);
-          mma_commit(sm.dp_full());
-          mma_commit(sm.v_empty(sv));  // V_j is read by dP_j only
-          if (it == n_it - 1) mma_commit(sm.fix_empty(slot));  // Q_i, dO_i are no longer read
+          if (do_S) {
+            if (g > 0 && !(ok = mbar_wait(sm.s_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // S read out
+            if (!(ok = mbar_wait(sm.st_full(sk), (g / KR) & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            // S = Q_i K_j^T (M = queries, N = keys, K = d)
+            mma_chain_ss<TL, TL::KSTEPS_D>(tS, dQk, dKk0 + (uint64_t)sk * kSlotOff, idesc_s, 0u);
+            mma_commit(sm.s_full());
+          }
+          if (do_dP) {
+            if (g > 0 && !(ok = mbar_wait(sm.dp_free(), (g - 1) & 1, ab, kErrTimeoutMma))) break;  // dP read out
+            if (!(ok = mbar_wait(sm.v_full(sv), (g / VR) & 1, ab, kErrTimeoutMma))) break;
+            tc_fence_after();
+            // dP = dO_i V_j^T
+            mma_chain_ss<TL, TL::KSTEPS_D>(tDP, dOk, dVk0 + (uint64_t)sv * kSlotOff, idesc_s, 0u);
+            mma_commit(sm.dp_full());
+            mma_commit(sm.v_empty(sv));  // V_j is read by dP_j only
+          }
+          // Q_i (S) and dO_i (dP) are no longer read by this thread
+          if (it == n_it - 1) mma_commit(sm.fix_empty(slot));
         }
       }
       if (!ok) {
-        mma_commit(sm.drain());
-        mbar_wait_drain(sm.drain(), 0, ab);
+        const uint32_t dr = do_S ? sm.drain() : sm.drain3();
+        mma_commit(dr);
+        mbar_wait_drain(dr, 0, ab);
       }
     }
   } else if (warp == kWarpMmaB) {
@@ -1341,7 +1361,7 @@ cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (PRE && (!a.tmO || !a.lse)) return cudaErrorInvalidValue;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
-  return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(kBwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
+  return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(dq_threads<D>()), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
                     *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.G,
                     a.scale, a.scale * kLog2e, a.err);
 }
