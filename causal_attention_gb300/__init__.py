@@ -12,12 +12,16 @@ from __future__ import annotations
 
 import ctypes
 import math
+import os
 
 import torch
 
-from ._lib import load_library, ATTN_OK, AttnError, STATUS_NAMES  # noqa: F401
+from ._lib import load_library, ATTN_OK, AttnError, STATUS_NAMES, LIB_PATH, DEBUG_LIB_PATH  # noqa: F401
 
-_dll = load_library()
+# ATTN_BOUNDS_CHECK=1 in the environment loads the bounds-checked build of the library
+# (libattn_debug.so: every TMA coordinate, bulk-copy range and global store index checked
+# on the device; a failed check skips the access and is reported by check_device_error).
+_dll = load_library(DEBUG_LIB_PATH if os.environ.get("ATTN_BOUNDS_CHECK") == "1" else LIB_PATH)
 
 
 def _stream_handle(stream):

@@ -6,6 +6,8 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libattn.so")
+# the same library built with device-side bounds checks (see build.py)
+DEBUG_LIB_PATH = os.path.join(_HERE, "lib", "libattn_debug.so")
 
 ATTN_OK = 0
 STATUS_NAMES = {
@@ -17,6 +19,7 @@ STATUS_NAMES = {
     5: "ATTN_ERR_LAUNCH",
     6: "ATTN_ERR_DEVICE_TIMEOUT",
     7: "ATTN_ERR_CUDA",
+    8: "ATTN_ERR_DEVICE_BOUNDS",
 }
 
 

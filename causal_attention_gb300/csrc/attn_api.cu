@@ -729,7 +729,7 @@ attn_status attn_check_device_error(void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, ATTN_ERR_CUDA);
     snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "device error word 0x%x", word);
-    return ATTN_ERR_DEVICE_TIMEOUT;
+    return (word & kErrBounds) ? ATTN_ERR_DEVICE_BOUNDS : ATTN_ERR_DEVICE_TIMEOUT;
   }
   return ATTN_OK;
 }
@@ -745,6 +745,7 @@ const char* attn_status_string(attn_status status) {
     case ATTN_ERR_LAUNCH: return "kernel launch failed";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel wait expired on the device";
     case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case ATTN_ERR_DEVICE_BOUNDS: return "a kernel found an index out of range (bounds-checked build)";
   }
   return "unknown status";
 }

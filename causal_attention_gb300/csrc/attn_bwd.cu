@@ -154,6 +154,10 @@ struct BwdCfg {
   // then two threads issue its MMAs.
   static constexpr bool SEP_DKDV = D <= 64;
   static constexpr uint32_t COL_P = 384, COL_DS = 448;
+  // tensor-memory plan of the dK/dV kernel: S^T [0, 128), dP^T [128, 256), dV and dK from
+  // 256, and (d <= 64) P^T, dS^T in 64 columns each after them
+  static_assert(256 + 2 * TL::ACC_COLS <= (SEP_DKDV ? COL_P : 512u), "dV, dK columns");
+  static_assert(COL_DS + 64 <= 512, "P^T, dS^T columns");
   // fused dQ: dQ_ij (fp32, d columns) takes the columns of dS^T, which lives in shared memory
   static constexpr uint32_t COL_DQ = 448;
   static constexpr int THREADS = FUSE ? kBwdThreads + 32 : kBwdThreads;
@@ -501,6 +505,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         const int kt = key_tile(u), bh = kv_slice(u), i0 = CAUSAL ? kt : 0, n_it = n_iters(u);
         const int slot = r % NS;
         if (r >= NS && !(ok = mbar_wait(sm.fix_empty(slot), (r / NS - 1) & 1, ab, kErrTimeoutLoad))) break;
+        if (!(ok = in_bounds(kt * kTileRows < T && bh < BH, ab))) break;
         ++fix_issued;
         mbar_arrive_expect_tx(sm.fix_full(slot), 2 * TL::BYTES);
         TL::load(sKf(slot), &tmK, kt * kTileRows, bh, sm.fix_full(slot), once);
@@ -508,10 +513,12 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         for (int it = 0, qi = i0, bq = bh * G + head0(u); it < n_it; ++it, ++g) {
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(sm.st_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
+          const size_t woff = (size_t)bq * T_pad + (size_t)qi * kTileRows;
+          if (!(ok = in_bounds(qi * kTileRows < T && bq < BH * G && woff + kTileRows <= (size_t)BH * G * T_pad, ab)))
+            break;
           mbar_arrive_expect_tx(sm.st_full(s), 2 * TL::BYTES + 1024);
           TL::load(sQ(s), &tmQ, qi * kTileRows, bq, sm.st_full(s), keep);
           TL::load(sdO(s), &tmdO, qi * kTileRows, bq, sm.st_full(s), keep);
-          const size_t woff = (size_t)bq * T_pad + (size_t)qi * kTileRows;
           bulk_load(sL(s), ws_nlse2 + woff, 512, sm.st_full(s));
           bulk_load(sL(s) + 512, ws_D + woff, 512, sm.st_full(s));
           if (++qi == n_q) {  // the next query head of the group
@@ -615,6 +622,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < TL::NCHUNK; ++c) {
           const int row0 = key_tile(u_prev) * kTileRows, bh_prev = kv_slice(u_prev);
+          if (!in_bounds(row0 >= 0 && row0 < T && bh_prev < BH, ab)) continue;
           tma_store_3d(&tmdV, sEPI + c * TL::CHUNK_BYTES, c * TL::CHUNK_ELEMS, row0, bh_prev);
           tma_store_3d(&tmdK, sEPI + TL::BYTES + c * TL::CHUNK_BYTES, c * TL::CHUNK_ELEMS, row0, bh_prev);
         }
@@ -761,13 +769,16 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
       if (!(ok = mbar_wait_warp(sm.acc_full(), ri_e & 1, ab, kErrTimeoutElem))) return;
       tc_fence_after();
       const int bh_e = kv_slice(u_e), key = key_tile(u_e) * kTileRows + r;
+      const bool key_ok = key < T && in_bounds(bh_e < BH && key >= 0, ab);
       const uint32_t tDV = tmem + lo + 256u, tDK = tmem + lo + 256u + (uint32_t)TL::ACC_COLS;
       if constexpr (SPLIT) {
         // fp32 partial sums of this split (unscaled), [S][key/value slice][T_pad][d] for dK
         // then the same for dV; rows past T are written too and never read
         const size_t off = (((size_t)(u_e % S) * BH + bh_e) * T_pad + key) * D;
-        store_acc_quarter_f32<D>(tDK, part + off, hc);
-        store_acc_quarter_f32<D>(tDV, part + (size_t)S * BH * T_pad * D + off, hc);
+        if (in_bounds(off + D <= (size_t)S * BH * T_pad * D, ab)) {
+          store_acc_quarter_f32<D>(tDK, part + off, hc);
+          store_acc_quarter_f32<D>(tDV, part + (size_t)S * BH * T_pad * D + off, hc);
+        }
       } else if constexpr (EPI) {
         // into the staging tiles (free once the previous item's TMA stores have read them);
         // warp 18 stores them once acc_free says every thread has written its part
@@ -776,8 +787,8 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
         stage_acc_quarter<D>(tDK, sEPI + TL::BYTES, r, hc, scale);
         fence_proxy_async_smem();
       } else {
-        store_acc_quarter<D>(tDV, dv + ((size_t)bh_e * T + key) * D, hc, 1.f, key < T);
-        store_acc_quarter<D>(tDK, dk + ((size_t)bh_e * T + key) * D, hc, scale, key < T);
+        store_acc_quarter<D>(tDV, dv + ((size_t)bh_e * T + key) * D, hc, 1.f, key_ok);
+        store_acc_quarter<D>(tDK, dk + ((size_t)bh_e * T + key) * D, hc, scale, key_ok);
       }
       tc_fence_before();
       mbar_arrive(sm.acc_free());
@@ -974,6 +985,8 @@ __global__ void __launch_bounds__(dq_threads<D>(), 1)
   // buffer 1's full / free barriers are the ones the dK/dV kernel uses for dv_done / p_full
   constexpr int NACC = D <= 64 ? 2 : 1;
   auto acc_col = [&](int b) { return 256u + (b ? (uint32_t)D + 64u : 0u); };
+  // tensor-memory plan: S [0, 128), dP [128, 256), dQ buffer 0, dS (64 columns), dQ buffer 1
+  static_assert(256 + TL::ACC_COLS + 64 + (NACC == 2 ? D : 0) <= 512, "dQ kernel columns");
   auto acc_full_b = [&](int b) { return b ? sm.dv_done() : sm.acc_full(); };
   auto acc_free_b = [&](int b) { return b ? sm.p_full() : sm.acc_free(); };
   auto sK = [&](int s) { return sm.base + C::OFF_STAGE + s * TL::BYTES; };
@@ -995,6 +1008,7 @@ __global__ void __launch_bounds__(dq_threads<D>(), 1)
         const int qt = query_tile(u), bh = u % BH, n_it = n_iters(u);
         const int slot = r % NS;
         if (r >= NS && !(ok = mbar_wait(sm.fix_empty(slot), (r / NS - 1) & 1, ab, kErrTimeoutLoad))) break;
+        if (!(ok = in_bounds(qt >= 0 && qt * kTileRows < T && bh < BH, ab))) break;
         ++fix_issued;
         mbar_arrive_expect_tx(sm.fix_full(slot), NFIX * TL::BYTES);
         TL::load(sQf(slot), &tmQ, qt * kTileRows, bh, sm.fix_full(slot), once);
@@ -1004,6 +1018,7 @@ __global__ void __launch_bounds__(dq_threads<D>(), 1)
           const int sk = g % KR, sv = g % VR;
           // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
           if (g >= KR && !(ok = mbar_wait(sm.st_empty(sk), (g / KR - 1) & 1, ab, kErrTimeoutLoad))) break;
+          if (!(ok = in_bounds(it * kTileRows < T && bh / G < BH / G, ab))) break;
           mbar_arrive_expect_tx(sm.st_full(sk), TL::BYTES);
           TL::load(sK(sk), &tmK, it * kTileRows, bh / G, sm.st_full(sk), keep);
           ++nk;
@@ -1107,7 +1122,8 @@ __global__ void __launch_bounds__(dq_threads<D>(), 1)
       const int b = ri_e % NACC;
       if (!(ok = mbar_wait_warp(acc_full_b(b), (ri_e / NACC) & 1, ab, kErrTimeoutElem))) return;
       tc_fence_after();
-      store_acc_quarter<D>(tmem + lo + acc_col(b), dq + ((size_t)bh_e * T + row_e) * D, hc, scale, row_e < T);
+      store_acc_quarter<D>(tmem + lo + acc_col(b), dq + ((size_t)bh_e * T + row_e) * D, hc, scale,
+                           row_e < T && in_bounds(bh_e < BH, ab));
       tc_fence_before();
       mbar_arrive(acc_free_b(b));
     };
@@ -1136,13 +1152,14 @@ __global__ void __launch_bounds__(dq_threads<D>(), 1)
         mbar_arrive(sm.fix_empty(slot));  // O_i, dO_i read (the MMA commit is the other arrival)
         Dr = a0 + a1;
         nl = row < T ? -lse[(size_t)bh * T + row] * kLog2e : -INFINITY;
-        if (hc == 0) {
+        if (hc == 0 && in_bounds(bh < BH && row < T_pad, ab)) {
           ws_nlse2[(size_t)bh * T_pad + row] = nl;
           ws_D[(size_t)bh * T_pad + row] = Dr;
         }
       } else {
-        nl = ws_nlse2[(size_t)bh * T_pad + row];
-        Dr = ws_D[(size_t)bh * T_pad + row];
+        const bool in = in_bounds(bh < BH && row < T_pad, ab);
+        nl = in ? ws_nlse2[(size_t)bh * T_pad + row] : -INFINITY;
+        Dr = in ? ws_D[(size_t)bh * T_pad + row] : 0.f;
       }
       const uint64_t nl2 = f2_pack(nl, nl), D2 = f2_pack(Dr, Dr);
       for (int it = 0; it < n_it; ++it, ++g) {

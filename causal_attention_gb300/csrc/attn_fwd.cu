@@ -55,6 +55,9 @@ struct FwdCfg {
   static constexpr int NBAR = 2 + 4 * STAGES + 12 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  // tensor-memory plan: S0, S1, O0, O1 (and P0, P1 at d <= 64) inside the 512 columns
+  static_assert(COL_O1 + TL::ACC_COLS <= (SEP_P ? COL_P0 : 512u), "O columns");
+  static_assert(!SEP_P || COL_P1 + 64 <= 512, "P columns");
 };
 
 // Row max of 128 values: eight independent chains of 3-input max, then a short tree.
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
         const int t = pair_of(u), bh = u % BH, nb = n_blocks(u, 1);
         if (r > 0 && !(ok = mbar_wait(q_empty, (r - 1) & 1, ab, kErrTimeoutLoad))) break;
+        if (!(ok = in_bounds(t >= 0 && t < n_pairs && bh >= 0 && bh < BH, ab))) break;
         mbar_arrive_expect_tx(q_full, 2 * TL::BYTES);
         TL::load(sQ, &tmQ, 2 * t * kTileRows, bh, q_full, once);
         TL::load(sQ + TL::BYTES, &tmQ, (2 * t + 1) * kTileRows, bh, q_full, once);
@@ -178,6 +182,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int j = 0; j < nb; ++j, ++g) {
           const int s = g % ST, n = g / ST;
           if (g >= ST && !(ok = mbar_wait(k_empty(s), (n - 1) & 1, ab, kErrTimeoutLoad))) break;
+          if (!(ok = in_bounds(j * kTileRows < T && bh / G < BH / G, ab))) break;
           mbar_arrive_expect_tx(k_full(s), TL::BYTES);
           // query head bh reads key/value slice bh / G (grouped key/value heads; G = 1 without)
           TL::load(sK + s * TL::BYTES, &tmK, j * kTileRows, bh / G, k_full(s), keep);
@@ -454,6 +459,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok || !(ok = mbar_wait_warp(o_final(q), ri & 1, ab, kErrTimeoutElem))) break;
       tc_fence_after();
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const bool row_ok = row < T && in_bounds(bh < BH && row >= 0, ab);
       __nv_bfloat16* orow = out + ((size_t)bh * T + row) * D;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
@@ -465,7 +471,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pw[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-        if (row < T) {
+        if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cb);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
@@ -480,13 +486,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           pw[i] = pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-        if (row < T) {
+        if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + (D - 16));
           dst[0] = pkd[0];
           dst[1] = pkd[1];
         }
       }
-      if (row < T) lse_out[(size_t)bh * T + row] = (m * scale_log2 + __log2f(l)) * 0.69314718055994531f;
+      if (row_ok) lse_out[(size_t)bh * T + row] = (m * scale_log2 + __log2f(l)) * 0.69314718055994531f;
       tc_fence_before();
       mbar_arrive(o_free(q));
       gq += nb;

@@ -22,6 +22,7 @@ enum : uint32_t {
   kErrTimeoutElem = 1u << 2,   // softmax / elementwise warps waited too long
   kErrTimeoutDrain = 1u << 3,  // drain after an abort did not complete
   kErrTimeoutOrder = 1u << 4,  // fused dQ: waited too long for an earlier key tile's turn
+  kErrBounds = 1u << 5,        // debug build: an index failed its bounds check (access skipped)
 };
 
 // Where a CTA reports a failed wait, and how its roles tell one another to stop.
@@ -104,6 +105,29 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
                                                uint32_t err_bit) {
   const bool ok = mbar_wait(bar, parity, ab, err_bit);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Debug build (compiled with -DATTN_DEBUG_BOUNDS=1): every TMA coordinate, bulk-copy
+// range and global store index of the attention kernels is checked against its extent
+// before the access. A failed check records kErrBounds in the error word, raises the CTA's
+// abort flag (the other roles then stop waiting, and the CTA leaves through its abort
+// path) and returns false, and the caller skips the access; nothing traps. In the normal
+// build every check is the constant true and compiles to nothing.
+#ifndef ATTN_DEBUG_BOUNDS
+#define ATTN_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool in_bounds(bool ok, const Abort& ab) {
+#if ATTN_DEBUG_BOUNDS
+  if (!ok) {
+    atomicOr(ab.err, kErrBounds);
+    *ab.flag = 1;
+  }
+  return ok;
+#else
+  (void)ok;
+  (void)ab;
+  return true;
+#endif
 }
 
 // Bounded wait used while draining after an abort: no abort check, shorter limit.

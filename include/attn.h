@@ -52,7 +52,9 @@ typedef enum attn_status {
   ATTN_ERR_WORKSPACE = 4,       /* workspace missing or smaller than attn_bwd_workspace_size() */
   ATTN_ERR_LAUNCH = 5,          /* the CUDA runtime rejected a launch (see attn_last_cuda_error) */
   ATTN_ERR_DEVICE_TIMEOUT = 6,  /* a kernel's bounded wait expired (attn_check_device_error) */
-  ATTN_ERR_CUDA = 7             /* another CUDA runtime or driver call failed */
+  ATTN_ERR_CUDA = 7,            /* another CUDA runtime or driver call failed */
+  ATTN_ERR_DEVICE_BOUNDS = 8    /* bounds-checked build only: a kernel found an index out of its
+                                   range and skipped the access (attn_check_device_error) */
 } attn_status;
 
 /* ABI version of the loaded library (ATTN_ABI_VERSION at build time). */
@@ -216,8 +218,10 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
                              int H, int T, int d, float scale, int causal, void* stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
- * current device. Returns ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait
- * expired since the last check, ATTN_ERR_CUDA if the synchronisation failed. */
+ * current device. Returns ATTN_ERR_DEVICE_BOUNDS if (in the bounds-checked build,
+ * libattn_debug.so) a kernel found an index outside its range since the last check,
+ * else ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait expired, ATTN_ERR_CUDA if
+ * the synchronisation failed. */
 attn_status attn_check_device_error(void* stream);
 
 /* Static description of a status code. */

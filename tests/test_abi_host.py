@@ -41,12 +41,24 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_bounds_checked_build_loads_and_exports_the_same_symbols(lib):
+    """libattn_debug.so (device-side bounds checks) is the same C ABI."""
+    if not os.path.exists(_lib.DEBUG_LIB_PATH):
+        import causal_attention_gb300.build as b
+        b.build()
+    dbg = _lib.load_library(_lib.DEBUG_LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    assert dbg.attn_abi_version() == lib.attn_abi_version()
+    assert b"bounds" in dbg.attn_status_string(8)
+
+
 def test_abi_version(lib):
     assert lib.attn_abi_version() == 3
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert lib.attn_status_string(code)
     assert b"unknown" in lib.attn_status_string(99)
 
