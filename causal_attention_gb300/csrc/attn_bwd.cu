@@ -1351,9 +1351,18 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   // than a fixed per-CTA share.
   const int grid = SPLIT ? n_items : min(n_items, a.num_sms);
   if (EPI && (!a.tmdK || !a.tmdV)) return cudaErrorInvalidValue;
-  return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
+  // the fused dQ's CTAs wait on one another's contributions (per-tile counters): it is
+  // launched cooperatively, so that it starts only when its whole grid (one CTA per SM,
+  // at most the SM count) can be resident and every wait is on a running CTA
+  auto go = [&](auto launcher) {
+    return launcher(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
                     EPI ? *a.tmdK : *a.tmQ, EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.dq_acc,
                     a.dq_cnt, a.part, a.T, a.T_pad, a.BH / a.G, a.G, a.S, a.scale, a.scale * kLog2e, a.err);
+  };
+  if constexpr (FUSE)
+    return go([](auto&&... x) { return launch_coop(static_cast<decltype(x)&&>(x)...); });
+  else
+    return go([](auto&&... x) { return launch_pdl(static_cast<decltype(x)&&>(x)...); });
 }
 
 template <int D>

@@ -131,6 +131,26 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// Launches a kernel cooperatively: the runtime starts it only when every CTA of its grid
+// can be resident at once (the launch fails if the grid is larger than that), which a
+// kernel whose CTAs wait on one another needs to make progress. No programmatic
+// dependency: it starts after the previous kernel in the stream has completed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                        Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Sets the max dynamic shared memory of a kernel once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes, uint32_t* done_mask);
 

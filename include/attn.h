@@ -170,10 +170,12 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void*
  * counter, bounded waits), never with atomics, so the result is the same on every run
  * (Iron "Kernel Engineering Guide", section 3.4 "Determinism": partial sums combined in a
  * fixed order; Forge RESEARCH.md section 8, pitfall 20: no atomic gradient
- * accumulation in deterministic mode). The ordering assumes the launch's CTAs (one per
- * SM, at most the SM count) are resident together, as on an otherwise idle device; if
- * they cannot be, a wait runs out and attn_check_device_error reports
- * ATTN_ERR_DEVICE_TIMEOUT instead of hanging.
+ * accumulation in deterministic mode). The ordering needs the launch's CTAs (one per SM,
+ * at most the SM count) to be resident together, so the kernel is launched cooperatively:
+ * the runtime starts it only once the whole grid fits on the device (kernels already
+ * running on other streams finish first), and every counter wait is on a running CTA.
+ * A wait that still ran out would be reported by attn_check_device_error as
+ * ATTN_ERR_DEVICE_TIMEOUT; nothing hangs.
  *   workspace : attn_bwd_fused_workspace_size(B, H, T, d) bytes (ATTN_ERR_WORKSPACE if
  *               smaller), written by attn_bwd_preprocess just before
  *   dk, dv    : bf16 [B, H, T, d] outputs; dQ is left in the workspace for

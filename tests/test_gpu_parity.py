@@ -465,3 +465,35 @@ def test_running_max_grows_every_block(d):
     print(f"rising d={d}: dQ rel-RMS {err['dq'][1]:.3e} (whole-tensor bar {gu.TOL_GRAD_REL_RMS:g} not applied), "
           f"worst error / rounding bound {ratio.max():.3f}")
     assert ratio.max() <= 1.0, f"dQ error {ratio.max():.2f} x the rounding bound, row {np.unravel_index(ratio.argmax(), ratio.shape)}"
+
+
+def test_fused_dq_progresses_under_concurrent_load():
+    """The fused dQ's CTAs wait on one another (per-tile counters); it is launched
+    cooperatively, so it starts only when its whole grid can be resident. With large
+    matmuls on another stream holding SMs, repeated fused backward passes complete without
+    a timeout and give the bits of a quiet run."""
+    import causal_attention_gb300 as ca
+    w = si.Workload("fusedload", 2, 8, 1024, 64, seed=123)
+    x = si.make_inputs(w)
+    q, k, v, do = (gu.to_device(x[n]) for n in ("q", "k", "v", "do"))
+    o, lse = ca.forward(q, k, v, w.scale, True)
+    ws = ca.new_workspace(*w.shape, fused_dq=True)
+    outs = [torch.empty_like(q) for _ in range(3)]
+    ca.attn_bwd_preprocess(o, do, lse, ws)
+    ca.attn_bwd_dkdv_dq(q, k, v, do, outs[1], outs[2], ws, w.scale, True)
+    ca.attn_bwd_dq_finish(outs[0], ws, w.scale)
+    ca.check_device_error()
+    quiet = [t.clone() for t in outs]
+    a = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    load, work = torch.cuda.Stream(), torch.cuda.Stream()
+    for i in range(20):
+        with torch.cuda.stream(load):
+            for _ in range(3):
+                a = (a @ a).clamp_(-1, 1)
+        ca.attn_bwd_preprocess(o, do, lse, ws, work)
+        ca.attn_bwd_dkdv_dq(q, k, v, do, outs[1], outs[2], ws, w.scale, True, work)
+        ca.attn_bwd_dq_finish(outs[0], ws, w.scale, work)
+        ca.check_device_error(work)
+        assert all(torch.equal(t, r) for t, r in zip(outs, quiet)), i
+    torch.cuda.synchronize()
