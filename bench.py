@@ -136,6 +136,69 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class NvmlClockSampler:
+    """The SM clock and the clock-event reasons of the benchmark's GPU, read through NVML
+    (the driver's library, by ctypes) about every millisecond from a thread while the timed
+    region runs: nvidia-smi's 200 ms loop sees at most a sample or two of a region this
+    short. The GPU is found by its UUID, so the right one is read whatever
+    CUDA_VISIBLE_DEVICES maps. Reads only; changes no setting."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+        self.ok = False
+        self.samples, self.mask = [], 0
+        self.stop_flag = threading.Event()
+        self.thread = None
+        try:
+            import torch
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            self.lib, self.h = lib, ctypes.c_void_p()
+            uuid = str(getattr(torch.cuda.get_device_properties(device), "uuid", ""))
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                return
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 else None
+            self.ok = True
+        except (OSError, AttributeError, ImportError):
+            self.ok = False
+
+    def _run(self):
+        import ctypes
+        mhz, mask = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:  # 1: the SM clock
+                self.samples.append(float(mhz.value))
+            if self.reasons_fn(self.h, ctypes.byref(mask)) == 0:
+                self.mask |= int(mask.value)
+            time.sleep(0.001)
+
+    def start(self):
+        if self.ok:
+            import threading
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        if not self.ok or self.thread is None:
+            return None
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.mask & b),
+                "samples": len(self.samples), "source": "NVML, every ~1 ms during the timed region"}
+
+
 def oracle_sample(w, n_heads, x=None, budget_s=None):
     """Runs the CPU oracle fwd + bwd on up to n_heads heads (stopping once budget_s seconds
     have passed, after at least one head); returns (credited FLOPs, seconds, heads run)."""
@@ -432,17 +495,22 @@ def run_ours(args, rank, world, local):
         step(sets[i % n_sets])
     ca.check_device_error(stream)
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    nvml = NvmlClockSampler(dev) if rank == 0 else None
+    sampler = ClockSampler(local) if rank == 0 and not (nvml and nvml.ok) else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    if nvml:
+        nvml.start()
     elapsed_ms, evs, launch_mode = timed_steps(args, step, sets, len(KERNELS) + 1, stream)
+    clocks = nvml.stop() if nvml else None
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop() if sampler else None
+    if sampler:
+        clocks = sampler.stop()
     ca.check_device_error(stream)
 
     per_kernel = {k: [] for k in KERNELS}
@@ -670,17 +738,22 @@ def run_block(args, rank, world, local):
     for i in range(max(3, args.warmup)):
         step(sets[i % n_sets])
     ca.check_device_error(stream)
-    sampler = ClockSampler(local) if rank == 0 else None
+    nvml = NvmlClockSampler(dev) if rank == 0 else None
+    sampler = ClockSampler(local) if rank == 0 and not (nvml and nvml.ok) else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    if nvml:
+        nvml.start()
     elapsed_ms, evs, launch_mode = timed_steps(args, step, sets, len(BLOCK_STAGES) + 1, stream)
+    clocks = nvml.stop() if nvml else None
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop() if sampler else None
+    if sampler:
+        clocks = sampler.stop()
     ca.check_device_error(stream)
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     per_stage = {k: [ev[j].elapsed_time(ev[j + 1]) for ev in evs] for j, k in enumerate(BLOCK_STAGES)}
