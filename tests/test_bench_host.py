@@ -58,3 +58,16 @@ def test_variants_are_renamed():
 def test_spread():
     s = bench.spread([5.0, 1.0, 3.0, 2.0, 4.0])
     assert s == {"ms_min": 1.0, "ms_median": 3.0, "ms_p95": 5.0}
+
+
+def test_default_line_is_the_largest_configuration(monkeypatch):
+    """Without flags the bench runs long8k (B1 H16 T8192 d128), the largest single-GPU
+    configuration, at N = 1."""
+    import sys
+    import bench
+    import seeded_inputs as si
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    args = bench.parse()
+    assert args.workload == "long8k" and args.gpus == 1 and args.impl == "ours"
+    big = max(si.WORKLOADS.values(), key=lambda w: sum(bench.credited_flops(*w.shape)))
+    assert big.name == args.workload
