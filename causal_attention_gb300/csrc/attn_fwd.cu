@@ -72,22 +72,11 @@ __device__ __forceinline__ float rowmax128(const float (&x)[128]) {
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
 }
 
-// Work items (a pair of query tiles of one (b, h)), longest first, dealt to the CTAs in a
-// snake order (round r left to right when r is even, right to left when odd).
-struct FwdSched {
-  int n_items;
-  __device__ __forceinline__ int item(int r) const {
-    const int G = (int)gridDim.x, c = (int)blockIdx.x;
-    const int u = r * G + ((r & 1) ? (G - 1 - c) : c);
-    return u < n_items ? u : -1;
-  }
-};
-
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse_out, int T, int BH, int G, int n_pairs, float scale,
+                    float* __restrict__ lse_out, int T, int BH, int G, int n_pairs, int HG, float scale,
                     float scale_log2, uint32_t* __restrict__ err) {
   using C = FwdCfg<D>;
   using TL = Tile<D>;
@@ -123,9 +112,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int lane = threadIdx.x & 31;
 
   const int nkv = (T + kTileRows - 1) / kTileRows;
-  const FwdSched sched{n_pairs * BH};
-  // item u: query tiles 2t, 2t+1 with t = n_pairs - 1 - u / BH (longest first), slice u % BH
-  auto pair_of = [&](int u) { return n_pairs - 1 - u / BH; };
+  // work items: a pair of query tiles of one (b, h)
+  const ItemSched sched{n_pairs * BH, n_pairs * HG};
+  // item u, in groups of HG slices (slices_per_group): within group u / (n_pairs HG), query
+  // tiles 2t, 2t+1 with t = n_pairs - 1 - v / HG (longest first), slice of the group v % HG,
+  // v = u % (n_pairs HG)
+  auto pair_of = [&](int u) { return n_pairs - 1 - (u % (n_pairs * HG)) / HG; };
+  auto slice_of = [&](int u) { return u / (n_pairs * HG) * HG + (u % (n_pairs * HG)) % HG; };
   auto n_blocks = [&](int u, int q) { return CAUSAL ? min(2 * pair_of(u) + q + 1, nkv) : nkv; };
   constexpr uint32_t kRelease = SEP ? 2u : 1u;  // arrivals that free a K/V stage or the Q tiles
 
@@ -172,7 +165,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       int g = 0, r = 0, q_issued = 0, k_issued = 0, v_issued = 0;
       for (int u; ok && (u = sched.item(r)) >= 0; ++r) {
-        const int t = pair_of(u), bh = u % BH, nb = n_blocks(u, 1);
+        const int t = pair_of(u), bh = slice_of(u), nb = n_blocks(u, 1);
         if (r > 0 && !(ok = mbar_wait(q_empty, (r - 1) & 1, ab, kErrTimeoutLoad))) break;
         if (!(ok = in_bounds(t >= 0 && t < n_pairs && bh >= 0 && bh < BH, ab))) break;
         mbar_arrive_expect_tx(q_full, 2 * TL::BYTES);
@@ -354,7 +347,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = true;
     int gq = 0;
     for (int ri = 0, u; ok && (u = sched.item(ri)) >= 0; ++ri) {
-      const int qt = 2 * pair_of(u) + q, bh = u % BH, nb = n_blocks(u, q);
+      const int qt = 2 * pair_of(u) + q, bh = slice_of(u), nb = n_blocks(u, q);
       const int row = qt * kTileRows + r;
       float m = -INFINITY, l = 0.f, lr = 0.f;
       for (int j = 0; j < nb; ++j) {
@@ -518,8 +511,11 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t stream) {
   const int n_items = n_pairs * a.BH;
   // persistent: one CTA per SM walks its share of the items
   const int grid = min(n_items, a.num_sms);
+  // K and V of a slice are read by all its items: group the slices (grouped key/value heads:
+  // one group, the key/value slices being shared across query slices)
+  const int hg = a.G == 1 ? slices_per_group(a.BH, 2ll * n_pairs * 2 * kTileRows * D * 2) : a.BH;
   return launch_pdl(kern, dim3(grid), dim3(kFwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, a.o, a.lse,
-                    a.T, a.BH, a.G, n_pairs, a.scale, a.scale * 1.4426950408889634f, a.err);
+                    a.T, a.BH, a.G, n_pairs, hg, a.scale, a.scale * 1.4426950408889634f, a.err);
 }
 
 }  // namespace

@@ -21,6 +21,41 @@ struct FwdArgs {
   int num_sms;    // streaming multiprocessors of the device (persistent grids)
 };
 
+// Work items of the persistent attention kernels come in groups of slices (b, h): all items
+// of the first group's slices, longest first, then the next group's. The tiles that every
+// item of a slice reads again (K, V in the forward and the dQ kernel; Q, dO in dK/dV) then
+// stay in L2 while their group runs instead of being evicted by the other slices' tiles.
+// Returns the slices per group: half the slices when all of them re-read more than the
+// budget, else all. Two groups, dealt as below, balance the CTAs' work as well as one; with
+// four or more, the per-group rounds leave the CTAs up to a few per cent apart.
+inline int slices_per_group(int n_slices, long long bytes_per_slice) {
+  const long long budget = 40ll << 20;
+  return (n_slices % 2 == 0 && (long long)n_slices * bytes_per_slice > budget) ? n_slices / 2 : n_slices;
+}
+
+#ifdef __CUDACC__
+// The persistent CTAs' share of the work items: each group of n_group items (longest first)
+// is dealt in a snake order, round r left to right when r is even and right to left when
+// odd, and every second group with the CTAs in reverse order, so that the CTAs left short
+// by one group's last round are the ones that the next group's serves first. Returns the
+// r-th item of this CTA, or -1 past its last.
+struct ItemSched {
+  int n_items;  // all items, a multiple of n_group
+  int n_group;  // items per group
+  __device__ __forceinline__ int item(int r) const {
+    const int G = (int)gridDim.x;
+    const int full = n_group / G, rem = n_group % G;
+    for (int base = 0, g = 0; base < n_items; base += n_group, ++g) {
+      const int c = (g & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x;
+      const int n_mine = full + (((full & 1) ? G - 1 - c : c) < rem ? 1 : 0);
+      if (r < n_mine) return base + r * G + ((r & 1) ? G - 1 - c : c);
+      r -= n_mine;
+    }
+    return -1;
+  }
+};
+#endif
+
 // Workspace of the backward: two fp32 arrays of [B*H, T_pad], T_pad = T rounded
 // up to 128. ws_nlse2 = -LSE * log2(e) (-inf on padding rows), ws_D = rowsum(dO*O)
 // (0 on padding rows). The fused dQ (d <= 64) adds dq_acc, one fp32 128 x d tile per
