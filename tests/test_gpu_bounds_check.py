@@ -3,8 +3,8 @@
 the attention kernels is checked on the device before the access, and a failed check
 skips the access, records itself in the device error word and makes check_device_error
 raise ATTN_ERR_DEVICE_BOUNDS. This runs the edge shapes (T = 1, tile boundaries, ragged
-tails, d = 32 / 64 / 80 / 128, causal and not), grouped key/value heads and a persistent
-multi-item launch through it, in a process of its own: the outputs must match the oracle
+tails, d = 32 / 64 / 80 / 128, causal and not), grouped key/value heads, persistent
+multi-item launches and work items dealt in two groups of slices through it, in a process of its own: the outputs must match the oracle
 and no check may fire. It stands in for compute-sanitizer, which this GPU pool does not
 offer."""
 import os
@@ -44,7 +44,14 @@ for B, H, Hkv, T, d in ((1, 8, 1, 257, 64), (1, 4, 2, 385, 128), (2, 4, 1, 300, 
     ca.check_device_error()
     for t in (o, lse, dq, dk, dv):
         assert bool(t.isfinite().all())
-print("bounds-checked build: no check fired on", len(cases) + 3, "cases")
+# slices dealt in two groups of three (their K and V exceed the kernels' L2 budget)
+q, k, v, do = (gu.to_device(si.normal_bf16_bits(4300, i, (1, 6, 16384, 128))) for i in range(4))
+o, lse = ca.forward(q, k, v, 1.0 / np.sqrt(128), True)
+dq, dk, dv = ca.backward(q, k, v, o, do, lse, 1.0 / np.sqrt(128), True)
+ca.check_device_error()
+for t in (o, lse, dq, dk, dv):
+    assert bool(t.isfinite().all())
+print("bounds-checked build: no check fired on", len(cases) + 4, "cases")
 """
 
 
