@@ -367,20 +367,10 @@ __device__ __forceinline__ void stage_acc_quarter(uint32_t tacc, uint32_t tile, 
            pack_bf16(__uint_as_float(u[8 * k + 6]) * mul, __uint_as_float(u[8 * k + 7]) * mul));
 }
 
-// Work items of the dK/dV kernel, sorted longest first, dealt to the CTAs in a snake order
-// (round r goes left to right when r is even, right to left when odd) so that every CTA
-// gets about the same total work. This is ItemSched with one group; the dK/dV kernel keeps
-// this plain form, which measured 1-5 % faster there than ItemSched's code dealing the
-// same order, and does not group its slices (two groups of key/value slices cut its Q and
-// dO re-reads from 1.20x to 1.01x of one pass at 8192 tokens, but no time).
-struct Sched {
-  int n_items;
-  __device__ __forceinline__ int item(int r) const {
-    const int G = (int)gridDim.x, c = (int)blockIdx.x;
-    const int u = r * G + ((r & 1) ? (G - 1 - c) : c);
-    return u < n_items ? u : -1;
-  }
-};
+// The dK/dV kernel deals its items in one group (SnakeSched): two groups of key/value
+// slices cut its Q and dO re-reads from 1.20x to 1.01x of one pass at 8192 tokens but
+// saved no time.
+using Sched = SnakeSched;
 
 // Number of items the schedule gives this CTA.
 __device__ __forceinline__ int sched_count(const Sched& s) {
@@ -952,7 +942,7 @@ struct DqRing {
 template <int D>
 constexpr int dq_threads() { return D > 64 ? kBwdThreads + 32 : kBwdThreads; }
 
-template <int D, bool CAUSAL, bool PRE>
+template <int D, bool CAUSAL, bool PRE, bool GROUPED>
 __global__ void __launch_bounds__(dq_threads<D>(), 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -977,11 +967,19 @@ __global__ void __launch_bounds__(dq_threads<D>(), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_k = (T + kTileRows - 1) / kTileRows;
-  const ItemSched sched{n_k * BH, n_k * HG};
-  // item u, in groups of HG slices (slices_per_group): query tile n_k - 1 - v / HG (largest,
-  // i.e. most work, first), slice u / (n_k HG) HG + v % HG, v = u % (n_k HG)
-  auto query_tile = [&](int u) { return n_k - 1 - (u % (n_k * HG)) / HG; };
-  auto slice_of = [&](int u) { return u / (n_k * HG) * HG + (u % (n_k * HG)) % HG; };
+  // item u: query tile n_k - 1 - u / BH (largest, i.e. most work, first), slice u % BH;
+  // GROUPED (two groups of HG = BH / 2 slices, slices_per_group): group g = u >= n_k HG,
+  // v = u - g n_k HG, query tile n_k - 1 - v / HG, slice g HG + v % HG
+  const int n_group = n_k * HG;
+  const auto sched = make_sched<GROUPED>(n_k * BH, n_group);
+  auto query_tile = [&](int u) {
+    if constexpr (GROUPED) return n_k - 1 - (u >= n_group ? u - n_group : u) / HG;
+    else return n_k - 1 - u / BH;
+  };
+  auto slice_of = [&](int u) {
+    if constexpr (GROUPED) return u >= n_group ? HG + (u - n_group) % HG : u % HG;
+    else return u % BH;
+  };
   auto n_iters = [&](int u) { return CAUSAL ? query_tile(u) + 1 : n_k; };
 
   constexpr int NS = C::NSLOT;
@@ -1381,23 +1379,32 @@ cudaError_t launch_dq_finish(const BwdArgs& a, cudaStream_t stream) {
                     a.T_pad, a.BH, a.scale);
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
+template <int D, bool CAUSAL, bool GROUPED>
+cudaError_t launch_dq_as(const BwdArgs& a, cudaStream_t stream, int hg) {
   // d <= 64: the dQ kernel forms D itself (and runs before dK/dV)
   constexpr bool PRE = D <= 64;
   using C = BwdCfg<D, false, PRE ? 3 : 2, 0, DqRing<D>::K, DqRing<D>::V>;
   static_assert(C::SMEM_BYTES <= 227 * 1024, "dQ kernel shared memory");
-  auto kern = attn_bwd_dq_kernel<D, CAUSAL, PRE>;
+  auto kern = attn_bwd_dq_kernel<D, CAUSAL, PRE, GROUPED>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
   if (PRE && (!a.tmO || !a.lse)) return cudaErrorInvalidValue;
   const int n_items = (a.T + kTileRows - 1) / kTileRows * a.BH;
-  // K and V of a slice are read by all its items (grouped key/value heads: one group)
-  const int hg = a.G == 1 ? slices_per_group(a.BH, 2ll * a.T_pad * D * 2) : a.BH;
   return launch_pdl(kern, dim3(min(n_items, a.num_sms)), dim3(dq_threads<D>()), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK,
                     *a.tmV, *a.tmdO, PRE ? *a.tmO : *a.tmQ, a.lse, a.ws_nlse2, a.ws_D, a.dq, a.T, a.T_pad, a.BH, a.G,
                     hg, a.scale, a.scale * kLog2e, a.err);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dq(const BwdArgs& a, cudaStream_t stream) {
+  // K and V of a slice are read by all its items: at d >= 80, when all slices' K and V
+  // exceed the L2 budget, two groups of slices (grouped key/value heads: one group)
+  if constexpr (D > 64) {
+    const int hg = a.G == 1 ? slices_per_group(a.BH, 2ll * a.T_pad * D * 2) : a.BH;
+    if (hg != a.BH) return launch_dq_as<D, CAUSAL, true>(a, stream, hg);
+  }
+  return launch_dq_as<D, CAUSAL, false>(a, stream, a.BH);
 }
 
 }  // namespace

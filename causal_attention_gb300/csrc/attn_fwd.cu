@@ -72,7 +72,7 @@ __device__ __forceinline__ float rowmax128(const float (&x)[128]) {
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool GROUPED>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out,
@@ -112,13 +112,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int lane = threadIdx.x & 31;
 
   const int nkv = (T + kTileRows - 1) / kTileRows;
-  // work items: a pair of query tiles of one (b, h)
-  const ItemSched sched{n_pairs * BH, n_pairs * HG};
-  // item u, in groups of HG slices (slices_per_group): within group u / (n_pairs HG), query
-  // tiles 2t, 2t+1 with t = n_pairs - 1 - v / HG (longest first), slice of the group v % HG,
-  // v = u % (n_pairs HG)
-  auto pair_of = [&](int u) { return n_pairs - 1 - (u % (n_pairs * HG)) / HG; };
-  auto slice_of = [&](int u) { return u / (n_pairs * HG) * HG + (u % (n_pairs * HG)) % HG; };
+  // work items: a pair of query tiles of one (b, h). Item u: query tiles 2t, 2t+1 with
+  // t = n_pairs - 1 - u / BH (longest first), slice u % BH; GROUPED (two groups of HG =
+  // BH / 2 slices, slices_per_group): group g = u >= n_pairs HG, v = u - g n_pairs HG,
+  // t = n_pairs - 1 - v / HG, slice g HG + v % HG
+  const int n_group = n_pairs * HG;
+  const auto sched = make_sched<GROUPED>(n_pairs * BH, n_group);
+  auto pair_of = [&](int u) {
+    if constexpr (GROUPED) return n_pairs - 1 - (u >= n_group ? u - n_group : u) / HG;
+    else return n_pairs - 1 - u / BH;
+  };
+  auto slice_of = [&](int u) {
+    if constexpr (GROUPED) return u >= n_group ? HG + (u - n_group) % HG : u % HG;
+    else return u % BH;
+  };
   auto n_blocks = [&](int u, int q) { return CAUSAL ? min(2 * pair_of(u) + q + 1, nkv) : nkv; };
   constexpr uint32_t kRelease = SEP ? 2u : 1u;  // arrivals that free a K/V stage or the Q tiles
 
@@ -500,22 +507,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch(const FwdArgs& a, cudaStream_t stream) {
+template <int D, bool CAUSAL, bool GROUPED>
+cudaError_t launch_as(const FwdArgs& a, cudaStream_t stream, int n_pairs, int hg) {
   using C = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, GROUPED>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
-  const int n_pairs = (a.T + 2 * kTileRows - 1) / (2 * kTileRows);
-  const int n_items = n_pairs * a.BH;
   // persistent: one CTA per SM walks its share of the items
-  const int grid = min(n_items, a.num_sms);
-  // K and V of a slice are read by all its items: group the slices (grouped key/value heads:
-  // one group, the key/value slices being shared across query slices)
-  const int hg = a.G == 1 ? slices_per_group(a.BH, 2ll * n_pairs * 2 * kTileRows * D * 2) : a.BH;
+  const int grid = min(n_pairs * a.BH, a.num_sms);
   return launch_pdl(kern, dim3(grid), dim3(kFwdThreads), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, a.o, a.lse,
                     a.T, a.BH, a.G, n_pairs, hg, a.scale, a.scale * 1.4426950408889634f, a.err);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch(const FwdArgs& a, cudaStream_t stream) {
+  const int n_pairs = (a.T + 2 * kTileRows - 1) / (2 * kTileRows);
+  // K and V of a slice are read by all its items: at d >= 80, when all slices' K and V
+  // exceed the L2 budget, two groups of slices (grouped key/value heads: one group, their
+  // key/value slices being shared across query slices)
+  if constexpr (D > 64) {
+    const int hg = a.G == 1 ? slices_per_group(a.BH, 2ll * n_pairs * 2 * kTileRows * D * 2) : a.BH;
+    if (hg != a.BH) return launch_as<D, CAUSAL, true>(a, stream, n_pairs, hg);
+  }
+  return launch_as<D, CAUSAL, false>(a, stream, n_pairs, a.BH);
 }
 
 }  // namespace

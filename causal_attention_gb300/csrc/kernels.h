@@ -21,39 +21,61 @@ struct FwdArgs {
   int num_sms;    // streaming multiprocessors of the device (persistent grids)
 };
 
-// Work items of the persistent attention kernels come in groups of slices (b, h): all items
-// of the first group's slices, longest first, then the next group's. The tiles that every
-// item of a slice reads again (K, V in the forward and the dQ kernel; Q, dO in dK/dV) then
-// stay in L2 while their group runs instead of being evicted by the other slices' tiles.
-// Returns the slices per group: half the slices when all of them re-read more than the
-// budget, else all. Two groups, dealt as below, balance the CTAs' work as well as one; with
-// four or more, the per-group rounds leave the CTAs up to a few per cent apart.
+// Work items of the persistent attention kernels are sorted longest first and dealt to the
+// CTAs in a snake order (round r left to right when r is even, right to left when odd), so
+// that every CTA gets about the same total work. Items of every slice (b, h) run side by
+// side, so the L2 holds the tiles that all items of a slice read again (K, V in the
+// forward and the dQ kernel) for all slices at once. When those exceed the budget below
+// (d >= 80 only), the forward and the dQ kernel deal their items in two groups of half the
+// slices each instead, one group after the other, and each group's tiles stay in L2 while
+// it runs. Returns the slices per group: half the slices when all of them re-read more
+// than the budget, else all (one group). Two groups dealt as HeadGroupSched does balance
+// the CTAs' work as well as one; with four or more, the per-group rounds leave the CTAs up
+// to a few per cent apart.
 inline int slices_per_group(int n_slices, long long bytes_per_slice) {
   const long long budget = 40ll << 20;
   return (n_slices % 2 == 0 && (long long)n_slices * bytes_per_slice > budget) ? n_slices / 2 : n_slices;
 }
 
 #ifdef __CUDACC__
-// The persistent CTAs' share of the work items: each group of n_group items (longest first)
-// is dealt in a snake order, round r left to right when r is even and right to left when
-// odd, and every second group with the CTAs in reverse order, so that the CTAs left short
-// by one group's last round are the ones that the next group's serves first. Returns the
-// r-th item of this CTA, or -1 past its last.
-struct ItemSched {
-  int n_items;  // all items, a multiple of n_group
-  int n_group;  // items per group
+// One group: returns the r-th item of this CTA in the snake order, or -1 past its last.
+struct SnakeSched {
+  int n_items;
   __device__ __forceinline__ int item(int r) const {
-    const int G = (int)gridDim.x;
-    const int full = n_group / G, rem = n_group % G;
-    for (int base = 0, g = 0; base < n_items; base += n_group, ++g) {
-      const int c = (g & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x;
-      const int n_mine = full + (((full & 1) ? G - 1 - c : c) < rem ? 1 : 0);
-      if (r < n_mine) return base + r * G + ((r & 1) ? G - 1 - c : c);
-      r -= n_mine;
-    }
-    return -1;
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int u = r * G + ((r & 1) ? (G - 1 - c) : c);
+    return u < n_items ? u : -1;
   }
 };
+
+// Two groups of n_group items each (items [0, n_group) of the first group's slices, then
+// the second's): each group is dealt in the snake order, the second with the CTAs in
+// reverse order, so that the CTAs left short by the first group's last round are the ones
+// that the second group serves first. Returns the r-th item of this CTA, or -1.
+struct HeadGroupSched {
+  int n_items;  // 2 n_group
+  int n_group;
+  __device__ __forceinline__ int item(int r) const {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int full = n_group / G, rem = n_group % G;
+    const int n0 = full + (((full & 1) ? G - 1 - c : c) < rem ? 1 : 0);
+    if (r < n0) return r * G + ((r & 1) ? G - 1 - c : c);
+    r -= n0;
+    const int c1 = G - 1 - c;
+    const int n1 = full + (((full & 1) ? G - 1 - c1 : c1) < rem ? 1 : 0);
+    return r < n1 ? n_group + r * G + ((r & 1) ? G - 1 - c1 : c1) : -1;
+  }
+};
+
+// The scheduler of a kernel compiled with or without the grouped item order: the grouped
+// form is a separate instantiation, so that one-group launches run the plain snake's code.
+template <bool GROUPED>
+__device__ __forceinline__ auto make_sched(int n_items, int n_group) {
+  if constexpr (GROUPED)
+    return HeadGroupSched{n_items, n_group};
+  else
+    return SnakeSched{n_items};
+}
 #endif
 
 // Workspace of the backward: two fp32 arrays of [B*H, T_pad], T_pad = T rounded
