@@ -367,13 +367,9 @@ __device__ __forceinline__ void stage_acc_quarter(uint32_t tacc, uint32_t tile, 
            pack_bf16(__uint_as_float(u[8 * k + 6]) * mul, __uint_as_float(u[8 * k + 7]) * mul));
 }
 
-// The dK/dV kernel deals its items in one group (SnakeSched): two groups of key/value
-// slices cut its Q and dO re-reads from 1.20x to 1.01x of one pass at 8192 tokens but
-// saved no time.
-using Sched = SnakeSched;
-
 // Number of items the schedule gives this CTA.
-__device__ __forceinline__ int sched_count(const Sched& s) {
+template <class SchedT>
+__device__ __forceinline__ int sched_count(const SchedT& s) {
   int n = 0;
   while (s.item(n) >= 0) ++n;
   return n;
@@ -432,7 +428,7 @@ __device__ __forceinline__ bool wait_turn(const int* cnt, int want, const Abort&
 // and the result is the same on every run. Items run longest (smallest j) first, so a
 // wait is only ever on an item that started no later; all CTAs of the persistent grid
 // are resident together (one per SM).
-template <int D, bool CAUSAL, bool FUSE, bool SPLIT>
+template <int D, bool CAUSAL, bool FUSE, bool SPLIT, bool GROUPED>
 __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -440,7 +436,7 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
                          const float* __restrict__ ws_nlse2, const float* __restrict__ ws_D,
                          __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dq_acc,
                          int* __restrict__ dq_cnt, float* __restrict__ part, int T, int T_pad, int BH, int G,
-                         int S_, float scale, float scale_log2, uint32_t* __restrict__ err) {
+                         int S_, int HG, float scale, float scale_log2, uint32_t* __restrict__ err) {
   // persistent d <= 64: dV and dK leave through shared memory and TMA stores (not when
   // SPLIT: then each work item writes fp32 partial sums)
   constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE && !SPLIT;
@@ -464,12 +460,22 @@ __global__ void __launch_bounds__(BwdCfg<D, FUSE>::THREADS, 1)
   // G = 1 without), whose query tiles all feed its dK and dV. With S > 1 (few key/value
   // heads) the G query heads are split over S work items, each writing fp32 partial sums
   // that a second launch adds in split order.
-  const Sched sched{n_q * BH * S};
   // item u: key tile u / (BH S) (small j = most work first), key/value slice
   // (u % (BH S)) / S, split u % S over query heads [sp G / S, (sp + 1) G / S);
-  // iteration it: query head kv * G + h0 + it / n_per, query tile i0 + it % n_per
-  auto key_tile = [&](int u) { return u / (BH * S); };
-  auto kv_slice = [&](int u) { return (u % (BH * S)) / S; };
+  // iteration it: query head kv * G + h0 + it / n_per, query tile i0 + it % n_per.
+  // GROUPED (S = 1; two groups of HG = BH / 2 key/value slices, slices_per_group): group
+  // g = u >= n_q HG, v = u - g n_q HG, key tile v / HG, key/value slice g HG + v % HG
+  static_assert(!(GROUPED && (SPLIT || FUSE)), "grouped order: unsplit, unfused items");
+  const int n_group = n_q * HG;
+  const auto sched = make_sched<GROUPED>(n_q * BH * S, n_group);
+  auto key_tile = [&](int u) {
+    if constexpr (GROUPED) return (u >= n_group ? u - n_group : u) / HG;
+    else return u / (BH * S);
+  };
+  auto kv_slice = [&](int u) {
+    if constexpr (GROUPED) return u >= n_group ? HG + (u - n_group) % HG : u % HG;
+    else return (u % (BH * S)) / S;
+  };
   auto head0 = [&](int u) { return (u % S) * G / S; };
   auto n_iters = [&](int u) {
     return ((u % S + 1) * G / S - head0(u)) * (n_q - (CAUSAL ? key_tile(u) : 0));
@@ -1339,12 +1345,21 @@ cudaError_t launch_pre(const BwdArgs& a, cudaStream_t stream) {
                     a.ws_D, a.dq_cnt, n_cnt, a.T, a.T_pad);
 }
 
-template <int D, bool CAUSAL, bool FUSE, bool SPLIT = false>
+template <int D, bool CAUSAL, bool FUSE, bool SPLIT = false, bool GROUPED = false>
 cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   if (!SPLIT && a.S > 1) return launch_dkdv<D, CAUSAL, FUSE, true>(a, stream);
+  // Q and dO of a key/value slice's G query heads are read by all its items: at d >= 80,
+  // when all key/value slices' Q and dO exceed the L2 budget, two groups of slices
+  int hg = a.BH / a.G;
+  if constexpr (D > 64 && !FUSE && !SPLIT && !GROUPED) {
+    hg = slices_per_group(a.BH / a.G, 2ll * a.G * a.T_pad * D * 2);
+    if (hg != a.BH / a.G) return launch_dkdv<D, CAUSAL, FUSE, false, true>(a, stream);
+  } else if constexpr (GROUPED) {
+    hg = a.BH / a.G / 2;
+  }
   constexpr bool EPI = BwdCfg<D>::SEP_DKDV && !FUSE && !SPLIT;
   using C = BwdCfg<D, FUSE, 2, EPI ? 2 : 0>;
-  auto kern = attn_bwd_dkdv_kernel<D, CAUSAL, FUSE, SPLIT>;
+  auto kern = attn_bwd_dkdv_kernel<D, CAUSAL, FUSE, SPLIT, GROUPED>;
   static uint32_t configured = 0;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, &configured);
   if (e != cudaSuccess) return e;
@@ -1361,7 +1376,7 @@ cudaError_t launch_dkdv(const BwdArgs& a, cudaStream_t stream) {
   auto go = [&](auto launcher) {
     return launcher(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, *a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
                     EPI ? *a.tmdK : *a.tmQ, EPI ? *a.tmdV : *a.tmQ, a.ws_nlse2, a.ws_D, a.dk, a.dv, a.dq_acc,
-                    a.dq_cnt, a.part, a.T, a.T_pad, a.BH / a.G, a.G, a.S, a.scale, a.scale * kLog2e, a.err);
+                    a.dq_cnt, a.part, a.T, a.T_pad, a.BH / a.G, a.G, a.S, hg, a.scale, a.scale * kLog2e, a.err);
   };
   if constexpr (FUSE)
     return go([](auto&&... x) { return launch_coop(static_cast<decltype(x)&&>(x)...); });

@@ -25,8 +25,8 @@ struct FwdArgs {
 // CTAs in a snake order (round r left to right when r is even, right to left when odd), so
 // that every CTA gets about the same total work. Items of every slice (b, h) run side by
 // side, so the L2 holds the tiles that all items of a slice read again (K, V in the
-// forward and the dQ kernel) for all slices at once. When those exceed the budget below
-// (d >= 80 only), the forward and the dQ kernel deal their items in two groups of half the
+// forward and the dQ kernel, Q and dO in dK/dV) for all slices at once. When those exceed
+// the budget below (d >= 80 only), the kernels deal their items in two groups of half the
 // slices each instead, one group after the other, and each group's tiles stay in L2 while
 // it runs. Returns the slices per group: half the slices when all of them re-read more
 // than the budget, else all (one group). Two groups dealt as HeadGroupSched does balance
