@@ -274,9 +274,9 @@ def test_persistent_stress_many_items_per_cta(d):
 
 @pytest.mark.parametrize("H,T,d", [(6, 16384, 128), (10, 16384, 80)])
 def test_head_grouped_item_order_matches_single_head_calls(H, T, d):
-    """At d >= 80, when the slices' K and V (2 T d bf16 each) exceed the kernels' L2 budget
-    of 40 MB, the forward and the dQ kernel deal their items in two groups of H / 2 slices,
-    the second group to the CTAs in reverse order. Here the groups hold an odd number of
+    """At d >= 80, when the slices' K and V (2 T d bf16 each; Q and dO for dK/dV) exceed
+    the kernels' L2 budget of 40 MB, the forward, dK/dV and dQ kernels deal their items in
+    two groups of H / 2 slices, the second group to the CTAs in reverse order. Here the groups hold an odd number of
     slices and end in partial rounds of the 152 CTAs. Each item computes the same values
     whatever the order, so every output must equal, bit for bit, that of H single-head
     calls (one group each, 8 or 5 MB of K and V)."""
