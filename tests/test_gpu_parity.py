@@ -342,6 +342,41 @@ def test_gqa_parity(B, H, H_kv, T, d, causal):
         assert gu.rel_rms(gu.to_f64(a), gu.to_f64(b)) <= 2e-3
 
 
+def test_grouped_kv_heads_in_head_grouped_order():
+    """Grouped key/value heads in the head-grouped item order of the dK/dV kernel: at
+    B16 H16 H_kv 4 T2048 d128 the 64 key/value slices' Q and dO (4 MiB each, over their 4
+    query heads) exceed the L2 budget, so the dK/dV items (128-key tiles sweeping 4 query
+    heads) are dealt in two groups of 32 key/value slices. Checked against the oracle on
+    the first and last key/value slice of each group, and bitwise over repeated runs."""
+    import oracle
+    import causal_attention_gb300 as ca
+    B, H, H_kv, T, d = 16, 16, 4, 2048, 128
+    G = H // H_kv
+    seed = 4400
+    bits = {"q": si.normal_bf16_bits(seed, 0, (B, H, T, d)), "k": si.normal_bf16_bits(seed, 1, (B, H_kv, T, d)),
+            "v": si.normal_bf16_bits(seed, 2, (B, H_kv, T, d)), "do": si.normal_bf16_bits(seed, 3, (B, H, T, d))}
+    scale = 1.0 / np.sqrt(d)
+    q, k, v, do = (gu.to_device(bits[n]) for n in ("q", "k", "v", "do"))
+    o, lse = ca.forward(q, k, v, scale, True)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, True)
+    ca.check_device_error()
+    for b, kh in ((0, 0), (7, 3), (8, 0), (15, 3)):
+        qs = slice(kh * G, (kh + 1) * G)
+        qf = si.bf16_bits_to_f64(bits["q"][b:b + 1, qs])
+        dof = si.bf16_bits_to_f64(bits["do"][b:b + 1, qs])
+        kf = si.bf16_bits_to_f64(bits["k"][b:b + 1, kh:kh + 1])
+        vf = si.bf16_bits_to_f64(bits["v"][b:b + 1, kh:kh + 1])
+        ro, rlse = oracle.forward(qf, kf, vf, scale, True)
+        rdq, rdk, rdv, _ = oracle.backward(qf, kf, vf, dof, scale, True)
+        gpu = dict(o=o[b:b + 1, qs], lse=lse[b:b + 1, qs], dq=dq[b:b + 1, qs], dk=dk[b:b + 1, kh:kh + 1],
+                   dv=dv[b:b + 1, kh:kh + 1])
+        err = gu.compare(gpu, dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv))
+        print((b, kh), {k_: tuple(f"{e:.2e}" for e in v_) for k_, v_ in err.items()})
+        gu.assert_within_tolerance(err, f"grouped gqa b{b} kv{kh}")
+    dq2, dk2, dv2 = ca.backward(q, k, v, o, do, lse, scale, True)
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
 def test_head_dim_80_at_gpt205m_shape():
     """d = 80 at the B4 H16 T2048 shape (the same seeded distributions as that workload),
     compared with the oracle on sampled heads."""
