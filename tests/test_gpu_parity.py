@@ -272,7 +272,7 @@ def test_persistent_stress_many_items_per_cta(d):
             assert torch.equal(t, first[name]), name
 
 
-@pytest.mark.parametrize("H,T,d", [(6, 16384, 128), (10, 16384, 80)])
+@pytest.mark.parametrize("H,T,d", [(6, 16384, 128), (10, 16384, 80), (6, 16000, 128)])
 def test_head_grouped_item_order_matches_single_head_calls(H, T, d):
     """At d >= 80, when the slices' K and V (2 T d bf16 each; Q and dO for dK/dV) exceed
     the kernels' L2 budget of 40 MB, the forward, dK/dV and dQ kernels deal their items in
