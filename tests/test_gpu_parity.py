@@ -272,26 +272,27 @@ def test_persistent_stress_many_items_per_cta(d):
             assert torch.equal(t, first[name]), name
 
 
-@pytest.mark.parametrize("H,T,d", [(6, 16384, 128), (10, 16384, 80), (6, 16000, 128)])
-def test_head_grouped_item_order_matches_single_head_calls(H, T, d):
+@pytest.mark.parametrize("H,T,d,causal", [(6, 16384, 128, True), (10, 16384, 80, True), (6, 16000, 128, True),
+                                           (12, 8192, 128, False)])
+def test_head_grouped_item_order_matches_single_head_calls(H, T, d, causal):
     """At d >= 80, when the slices' K and V (2 T d bf16 each; Q and dO for dK/dV) exceed
     the kernels' L2 budget of 40 MB, the forward, dK/dV and dQ kernels deal their items in
     two groups of H / 2 slices, the second group to the CTAs in reverse order. Here the groups hold an odd number of
     slices and end in partial rounds of the 152 CTAs. Each item computes the same values
     whatever the order, so every output must equal, bit for bit, that of H single-head
-    calls (one group each, 8 or 5 MB of K and V)."""
+    calls (one group each, 8 or 5 MB of K and V), causal or not."""
     import causal_attention_gb300 as ca
     assert H * 2 * T * d * 2 > 40 << 20 and T * 2 * d * 2 <= 40 << 20
     seed = 4200 + H + d
     q, k, v, do = (gu.to_device(si.normal_bf16_bits(seed, i, (1, H, T, d))) for i in range(4))
     scale = 1.0 / np.sqrt(d)
-    o, lse = ca.forward(q, k, v, scale, True)
-    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, True)
+    o, lse = ca.forward(q, k, v, scale, causal)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, causal)
     ca.check_device_error()
     for h in range(H):
         one = lambda t: t[:, h:h + 1].contiguous()
-        oh, lseh = ca.forward(one(q), one(k), one(v), scale, True)
-        dqh, dkh, dvh = ca.backward(one(q), one(k), one(v), one(o), one(do), one(lse), scale, True)
+        oh, lseh = ca.forward(one(q), one(k), one(v), scale, causal)
+        dqh, dkh, dvh = ca.backward(one(q), one(k), one(v), one(o), one(do), one(lse), scale, causal)
         ca.check_device_error()
         for name, a, b in (("o", oh, o), ("lse", lseh, lse), ("dq", dqh, dq), ("dk", dkh, dk), ("dv", dvh, dv)):
             assert torch.equal(a, one(b)), (name, h)
