@@ -74,7 +74,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 
 /*
  * Forward with grouped key/value heads (GQA; MQA when H_kv = 1). Cited mapping: Forge
- * RESEARCH.md section 6, "kv_head = q_head / (n_heads / n_kv_heads)": query head h reads
+ * RESEARCH.md section 6, its GQA index mapping: query head h reads
  * key/value head h / (H / H_kv), with no repeated copies of K and V.
  *   q, o : bf16 [B, H, T, d];  k, v : bf16 [B, H_kv, T, d];  lse : fp32 [B, H, T]
  *   H_kv : 1 <= H_kv <= H, dividing H (ATTN_ERR_INVALID_ARG otherwise)
@@ -95,7 +95,7 @@ size_t attn_bwd_workspace_size(int B, int H, int T, int d);
 size_t attn_bwd_fused_workspace_size(int B, int H, int T, int d);
 
 /*
- * Backward. Cited definition: Forge RESEARCH.md section 6, "The D term is free"
+ * Backward. Cited definition: Forge RESEARCH.md section 6, the bullet on the D term
  * and "Backward (training)"; the three-stage atomic-free structure of the Forge
  * paper's "Ecosystem survey". Equivalent to, on the same stream: at d <= 64
  * attn_bwd_dq (which also forms D) then attn_bwd_dkdv; at d >= 80 attn_bwd_preprocess,
@@ -136,7 +136,7 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
                          int causal, void* stream);
 
 /* Backward stage 1: D = rowsum(dO * O) and LSE * log2(e) into the workspace
- * (Forge RESEARCH.md section 6, "The D term is free"). Memory-bound. With d <= 64 and a
+ * (Forge RESEARCH.md section 6, the bullet on the D term). Memory-bound. With d <= 64 and a
  * workspace of attn_bwd_fused_workspace_size bytes it also zeroes the fused dQ's
  * counters, so it must run before every attn_bwd_dkdv_dq. */
 attn_status attn_bwd_preprocess(const void* o, const void* dO, const float* lse, void* workspace,
@@ -150,7 +150,8 @@ attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const voi
                           int T, int d, float scale, int causal, void* stream);
 
 /* Backward stage 3: dQ, one CTA per 128-query tile looping over key tiles
- * (deterministic; Forge RESEARCH.md section 6, "a dQ kernel with grid (NQ, H, B)").
+ * (deterministic; Forge RESEARCH.md section 6, the production structure it surveys: a
+ * separate dQ launch over query tiles, heads and batches).
  * At d >= 80 it reads the workspace written by stage 1. At d <= 64 it does stage 1's
  * work for its own query tile (D = rowsum(dO * O) from a staged O tile, -LSE * log2(e)
  * from lse) and writes both into the workspace, so it needs no stage 1 before it and

@@ -19,7 +19,7 @@ Definitions followed (page, section):
 * Causal convention: a key column later than the query row is masked (the mask
   test "column > row" of the cooperative-tensors guide, section 5.3 / the assembled
   kernel's causal mask), i.e. key j is visible to query i iff j <= i.
-* Backward: D = rowsum(dO * O) (Forge RESEARCH.md section 6, "The D term is free";
+* Backward: D = rowsum(dO * O) (Forge RESEARCH.md section 6, the bullet on the D term;
   Forge paper, section "Ecosystem survey"); P recomputed from L as P = exp(S - L)
   (RESEARCH.md section 6, "Backward (training)"); dV = P^T dO, dP = dO V^T,
   dS = P * (dP - D), dQ = dS K * scale, dK = dS^T Q * scale.
@@ -32,8 +32,8 @@ Readings where the pages leave a step open:
   at least its own key, so no row is fully masked.
 * Grouped key/value heads (GQA / MQA): K and V may have H_kv heads with H_kv dividing
   H; query head h attends with key/value head h // (H / H_kv), the index mapping of
-  Forge RESEARCH.md section 6 ("kv_head = q_head / (n_heads / n_kv_heads)", no repeated
-  copies). A key/value head's dK and dV are the sums of the contributions of the
+  Forge RESEARCH.md section 6 (integer division of the query head by the group size, no
+  repeated copies). A key/value head's dK and dV are the sums of the contributions of the
   query heads that use it (each contribution is the single-head backward above).
 """
 from __future__ import annotations

@@ -378,6 +378,43 @@ def test_grouped_kv_heads_in_head_grouped_order():
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        d = int(rng.choice([32, 64, 80, 128]))
+        H_kv = int(rng.choice([1, 2, 3]))
+        G = int(rng.choice([1, 2, 4]))
+        B = int(rng.integers(1, 3))
+        T = int(rng.choice([int(rng.integers(1, 130)), int(rng.integers(130, 400)), int(rng.integers(400, 700))]))
+        cases.append((B, H_kv * G, H_kv, T, d, bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("B,H,H_kv,T,d,causal", _random_cases(24, 2026))
+def test_random_shapes_against_oracle(B, H, H_kv, T, d, causal):
+    """Seeded random shapes (any T up to 700, every head dimension, grouped key/value heads
+    with 1, 2 or 4 query heads each, causal or not) against the oracle, element by element,
+    and bitwise over a repeated backward."""
+    import oracle
+    import causal_attention_gb300 as ca
+    seed = 7000 + B * 1000 + H * 100 + T + d
+    bits = {"q": si.normal_bf16_bits(seed, 0, (B, H, T, d)), "k": si.normal_bf16_bits(seed, 1, (B, H_kv, T, d)),
+            "v": si.normal_bf16_bits(seed, 2, (B, H_kv, T, d)), "do": si.normal_bf16_bits(seed, 3, (B, H, T, d))}
+    scale = 1.0 / np.sqrt(d)
+    q, k, v, do = (gu.to_device(bits[n]) for n in ("q", "k", "v", "do"))
+    o, lse = ca.forward(q, k, v, scale, causal)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, causal)
+    ca.check_device_error()
+    qf, kf, vf, dof = (si.bf16_bits_to_f64(bits[n]) for n in ("q", "k", "v", "do"))
+    ro, rlse = oracle.forward(qf, kf, vf, scale, causal)
+    rdq, rdk, rdv, _ = oracle.backward(qf, kf, vf, dof, scale, causal)
+    err = gu.compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv))
+    gu.assert_within_tolerance(err, f"random B{B} H{H} Hkv{H_kv} T{T} d{d} causal={causal}")
+    dq2, dk2, dv2 = ca.backward(q, k, v, o, do, lse, scale, causal)
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
 def test_head_dim_80_at_gpt205m_shape():
     """d = 80 at the B4 H16 T2048 shape (the same seeded distributions as that workload),
     compared with the oracle on sampled heads."""
