@@ -71,3 +71,16 @@ def test_default_line_is_the_largest_configuration(monkeypatch):
     assert args.workload == "long8k" and args.gpus == 1 and args.impl == "ours"
     big = max(si.WORKLOADS.values(), key=lambda w: sum(bench.credited_flops(*w.shape)))
     assert big.name == args.workload
+
+
+def test_every_traffic_record_matches_its_kernel_source():
+    """Each DRAM-traffic record under profiles/ was captured from the kernel source as it
+    stands: a record whose source hash no longer matches would make the bench line's
+    roofline.traffic null for that workload."""
+    import json
+    import os
+    recs = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    stale = [k for k in recs if bench.captured_traffic(*k.split(":", 1)) is None]
+    assert not stale, f"records captured from other kernel sources: {stale}"
+    for k in ("long8k:bwd_dkdv", "long8k:fwd", "gpt205m:bwd_dkdv"):
+        assert k in recs
