@@ -415,6 +415,46 @@ def test_random_shapes_against_oracle(B, H, H_kv, T, d, causal):
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
+@pytest.mark.parametrize("d,H", [(128, 516), (64, 1028)])
+def test_element_offsets_beyond_2_pow_31(d, H):
+    """Tensors of more than 2^31 elements (B128 T256, H = 516 at d = 128 and 1028 at
+    d = 64: B*H*T*d just above 2^31, 4.3 GB per tensor), so that the last heads' rows,
+    output tiles and workspace entries sit past every 32-bit element offset. The inputs
+    repeat four seeded heads over all heads: every head's O, LSE, dQ, dK and dV must equal
+    those of the first four bit for bit (each head's arithmetic is independent of where it
+    sits and of which CTA takes it), and the last four heads are compared with the
+    oracle. At d = 128 the slices exceed the L2 budget, so the head-grouped item order runs
+    too."""
+    import oracle
+    import causal_attention_gb300 as ca
+    B, T, n_base = 128, 256, 4
+    assert H % n_base == 0 and B * H * T * d > 2**31
+    seed = 9100 + d
+    names = ("q", "k", "v", "do")
+    bits = {n: si.normal_bf16_bits(seed, i, (1, n_base, T, d)) for i, n in enumerate(names)}
+    q, k, v, do = (gu.to_device(bits[n]).repeat(B, H // n_base, 1, 1) for n in names)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = ca.forward(q, k, v, scale, True)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, True)
+    ca.check_device_error()
+    del q, k, v, do
+    out = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+    for name, t in out.items():
+        per = t.reshape(B * H // n_base, n_base, *t.shape[2:])
+        for c in range(0, per.shape[0], 4096):  # in chunks: the comparison's mask stays small
+            part = per[c:c + 4096]
+            assert torch.equal(part, per[:1].expand_as(part)), f"{name}: heads from group {c} differ"
+    qf, kf, vf, dof = (si.bf16_bits_to_f64(bits[n]) for n in names)
+    ro, rlse = oracle.forward(qf, kf, vf, scale, True)
+    rdq, rdk, rdv, _ = oracle.backward(qf, kf, vf, dof, scale, True)
+    last = {n: t[B - 1:B, H - n_base:H] for n, t in out.items()}
+    err = gu.compare(last, dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv))
+    print({k_: tuple(f"{e:.2e}" for e in v_) for k_, v_ in err.items()})
+    gu.assert_within_tolerance(err, f"offsets past 2^31, d{d}")
+    del o, lse, dq, dk, dv, out, last
+    torch.cuda.empty_cache()
+
+
 def test_head_dim_80_at_gpt205m_shape():
     """d = 80 at the B4 H16 T2048 shape (the same seeded distributions as that workload),
     compared with the oracle on sampled heads."""
