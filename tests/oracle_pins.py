@@ -188,6 +188,26 @@ def check_gradient_sums(orc, T=48, d=16, seed=81, causal=True):
     assert np.max(np.abs(D - (p * dp).sum(axis=1))) <= 1e-12 * T, "D != sum_j P dP"
 
 
+def check_prefix_locality(orc, T=40, n=12, d=8, seed=131, tol=1e-12):
+    """Causal attention is local to prefixes: rows i < n of O and LSE equal those of the
+    problem cut to its first n rows; with dO zero past row n the whole backward equals the
+    backward of that prefix (a later query has dP = 0 and D = 0, so dS = 0), zero on every
+    later row; and row i alone is non-causal attention of query i over keys 0..i."""
+    q, k, v, do = (_rand(seed + i, (T, d)) for i in range(4))
+    do[n:] = 0.0
+    o, lse, _ = orc.head_forward(q, k, v, 0.3, True)
+    po, plse, _ = orc.head_forward(q[:n], k[:n], v[:n], 0.3, True)
+    assert np.max(np.abs(o[:n] - po)) <= tol and np.max(np.abs(lse[:n] - plse)) <= tol, "prefix forward"
+    dq, dk, dv, _ = orc.head_backward(q, k, v, do, 0.3, True)
+    pdq, pdk, pdv, _ = orc.head_backward(q[:n], k[:n], v[:n], do[:n], 0.3, True)
+    for name, full, pre in (("dQ", dq, pdq), ("dK", dk, pdk), ("dV", dv, pdv)):
+        assert np.max(np.abs(full[:n] - pre)) <= tol, f"prefix {name}"
+        assert not np.any(full[n:]), f"{name} nonzero past the prefix"
+    for i in (0, n, T - 1):
+        oi, li, _ = orc.head_forward(q[i:i + 1], k[:i + 1], v[:i + 1], 0.3, False)
+        assert np.max(np.abs(oi[0] - o[i])) <= tol and abs(li[0] - lse[i]) <= tol, f"row {i} alone"
+
+
 def check_accumulator_cell(orc):
     g = json.load(open(os.path.join(GOLDEN, "accumulator_cell.json")))
     d = g["d"]
@@ -293,6 +313,7 @@ ALL_FAST_CHECKS = (
     check_q_zero,
     check_first_row,
     check_gradient_sums,
+    check_prefix_locality,
     check_accumulator_cell,
     check_gqa_finite_differences,
     check_gqa_against_torch_sdpa,

@@ -90,6 +90,10 @@ def test_gradient_sums(causal):
     pins.check_gradient_sums(oracle, causal=causal)
 
 
+def test_prefix_locality():
+    pins.check_prefix_locality(oracle)
+
+
 def test_accumulator_cell():
     pins.check_accumulator_cell(oracle)
 
