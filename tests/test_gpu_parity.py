@@ -455,6 +455,54 @@ def test_element_offsets_beyond_2_pow_31(d, H):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("d,sigma", [(128, 3.0), (64, 1.0)])
+def test_long_sequence_prefix_and_sampled_rows(d, sigma):
+    """T = 131072 on one head (1024 key tiles, eight times the longest other case; at
+    d = 128 with long8k's peaked Q, K ~ N(0, 3^2)) against the oracle. dO is zero past the
+    first n = 1024 rows, so the whole backward equals that of the n-row prefix: a query
+    past it has dP = dO V^T = 0 and D = 0, hence dS = P (dP - D) = 0 and P dO = 0. Every
+    row of dQ, dK and dV is therefore checked: the prefix against the oracle on the prefix,
+    the rest against exact zeros (a wrong LSE, D or tile index in the long tail shows as a
+    NaN or a nonzero). O and LSE: the prefix rows against the same oracle call (a causal
+    row depends only on earlier keys), and sampled rows up to T - 1 one by one, each as
+    the attention of its query over keys 0..i."""
+    import oracle
+    import causal_attention_gb300 as ca
+    B, H, T, n = 1, 1, 131072, 1024
+    seed = 9300 + d
+    qb = si.normal_bf16_bits(seed, 0, (B, H, T, d), sigma)
+    kb = si.normal_bf16_bits(seed, 1, (B, H, T, d), sigma)
+    vb = si.normal_bf16_bits(seed, 2, (B, H, T, d))
+    dob = np.zeros_like(qb)
+    dob[:, :, :n] = si.normal_bf16_bits(seed, 3, (B, H, n, d))
+    scale = 1.0 / np.sqrt(d)
+    q, k, v, do = (gu.to_device(b) for b in (qb, kb, vb, dob))
+    o, lse = ca.forward(q, k, v, scale, True)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, True)
+    ca.check_device_error()
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.count_nonzero(t[:, :, n:]).item() == 0, f"{name}: nonzero rows past the prefix"
+    pf = {nm: si.bf16_bits_to_f64(b[:, :, :n]) for nm, b in (("q", qb), ("k", kb), ("v", vb), ("do", dob))}
+    ro, rlse = oracle.forward(pf["q"], pf["k"], pf["v"], scale, True)
+    rdq, rdk, rdv, _ = oracle.backward(pf["q"], pf["k"], pf["v"], pf["do"], scale, True)
+    pre = {nm: t[:, :, :n] for nm, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    err = gu.compare(pre, dict(o=ro, lse=rlse, dq=rdq, dk=rdk, dv=rdv))
+    print({k_: tuple(f"{e:.2e}" for e in v_) for k_, v_ in err.items()})
+    gu.assert_within_tolerance(err, f"T{T} d{d} prefix")
+    rows = [n, 4095, 65536, 100001, T - 129, T - 1]
+    go, gl = gu.to_f64(o[0, 0]), gu.to_f64(lse[0, 0])
+    got, want = [], []
+    for i in rows:
+        oi, li, _ = oracle.head_forward(si.bf16_bits_to_f64(qb[0, 0, i:i + 1]), si.bf16_bits_to_f64(kb[0, 0, :i + 1]),
+                                        si.bf16_bits_to_f64(vb[0, 0, :i + 1]), scale, causal=False)
+        assert abs(gl[i] - li[0]) <= gu.TOL_LSE_MAX_ABS, f"row {i}: LSE {gl[i]} against {li[0]}"
+        got.append(go[i])
+        want.append(oi[0])
+    got, want = np.stack(got), np.stack(want)
+    print("sampled rows: O max-abs %.2e rel-RMS %.2e" % (gu.max_abs(got, want), gu.rel_rms(got, want)))
+    assert gu.max_abs(got, want) <= gu.TOL_O_MAX_ABS and gu.rel_rms(got, want) <= gu.TOL_O_REL_RMS
+
+
 def test_head_dim_80_at_gpt205m_shape():
     """d = 80 at the B4 H16 T2048 shape (the same seeded distributions as that workload),
     compared with the oracle on sampled heads."""
