@@ -28,7 +28,7 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def cuda_lib():
-    """The built C-ABI library on a GPU machine (fails loudly if it is missing)."""
+    """The built C-ABI library on a machine with a GPU (fails loudly if it is missing)."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")

@@ -4,9 +4,10 @@ the attention kernels is checked on the device before the access, and a failed c
 skips the access, records itself in the device error word and makes check_device_error
 raise ATTN_ERR_DEVICE_BOUNDS. This runs the edge shapes (T = 1, tile boundaries, ragged
 tails, d = 32 / 64 / 80 / 128, causal and not), grouped key/value heads, persistent
-multi-item launches and work items dealt in two groups of slices through it, in a process of its own: the outputs must match the oracle
-and no check may fire. It stands in for compute-sanitizer, which this GPU pool does not
-offer."""
+multi-item launches, work items dealt in two groups of slices, tensors of more than 2^31
+elements and a 131072-token sequence through it, in a process of its own: the outputs
+must match the oracle (or, for the largest cases, be finite and repeat across identical
+heads) and no check may fire. It stands in for a run under compute-sanitizer."""
 import os
 import subprocess
 import sys
@@ -51,7 +52,27 @@ dq, dk, dv = ca.backward(q, k, v, o, do, lse, 1.0 / np.sqrt(128), True)
 ca.check_device_error()
 for t in (o, lse, dq, dk, dv):
     assert bool(t.isfinite().all())
-print("bounds-checked build: no check fired on", len(cases) + 4, "cases")
+del q, k, v, do, o, lse, dq, dk, dv
+# tensors of more than 2^31 elements: the last heads' offsets pass every 32-bit index;
+# four seeded heads repeated, so the last heads' outputs equal the first heads'
+import torch
+base = [gu.to_device(si.normal_bf16_bits(4400, i, (1, 4, 256, 128))) for i in range(4)]
+q, k, v, do = (t.repeat(128, 129, 1, 1) for t in base)
+o, lse = ca.forward(q, k, v, 1.0 / np.sqrt(128), True)
+dq, dk, dv = ca.backward(q, k, v, o, do, lse, 1.0 / np.sqrt(128), True)
+ca.check_device_error()
+for t in (o, lse, dq, dk, dv):
+    assert torch.equal(t[-1, -4:], t[0, :4])
+del q, k, v, do, o, lse, dq, dk, dv
+torch.cuda.empty_cache()
+# one long sequence, T = 131072 (1024 key tiles)
+q, k, v, do = (gu.to_device(si.normal_bf16_bits(4500, i, (1, 1, 131072, 64))) for i in range(4))
+o, lse = ca.forward(q, k, v, 1.0 / np.sqrt(64), True)
+dq, dk, dv = ca.backward(q, k, v, o, do, lse, 1.0 / np.sqrt(64), True)
+ca.check_device_error()
+for t in (o, lse, dq, dk, dv):
+    assert bool(t.isfinite().all())
+print("bounds-checked build: no check fired on", len(cases) + 6, "cases")
 """
 
 
