@@ -91,6 +91,17 @@ def load_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def sustained_peak():
+    """The bf16 matmul rate held for seconds under the power cap (a second denominator,
+    beside the burst peak the fractions use), or the fallback figure."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        v = json.load(open(p)).get("bf16_tflops_sustained")
+        if v:
+            return float(v), "measured"
+    return 1700.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
 
@@ -616,6 +627,7 @@ def run_ours(args, rank, world, local):
     bwd_ms = sum(mean_ms[k] for k in KERNELS if k != "fwd")
     bwd_tf = bwd_f * (1.0 if causal else 2.0) / (bwd_ms * 1e-3) / 1e12
 
+    sust_tf, sust_kind = sustained_peak()
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         # a bounded sample: whole heads until about 10 s of CPU work
@@ -634,6 +646,9 @@ def run_ours(args, rank, world, local):
         "frac_of_peak": round(value / peak_tf, 4),
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
         "fwd_frac": round(fwd_tf / peak_tf, 4), "bwd_frac": round(bwd_tf / peak_tf, 4),
+        "vs_sustained_peak": {"peak": sust_tf, "peak_kind": f"bf16 dense sustained, {sust_kind}",
+                              "frac": round(value / sust_tf, 4), "fwd_frac": round(fwd_tf / sust_tf, 4),
+                              "bwd_frac": round(bwd_tf / sust_tf, 4)},
         "kernels": kernels,
         "roofline": roofline,
         "cpu_baseline": cpu,

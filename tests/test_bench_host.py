@@ -84,3 +84,13 @@ def test_every_traffic_record_matches_its_kernel_source():
     assert not stale, f"records captured from other kernel sources: {stale}"
     for k in ("long8k:bwd_dkdv", "long8k:fwd", "gpt205m:bwd_dkdv"):
         assert k in recs
+
+
+def test_sustained_peak_is_the_measured_one():
+    """The second denominator is the measured seconds-long bf16 rate, below the burst peak."""
+    import json
+    import os
+    peaks = json.load(open(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")))
+    sust, kind = bench.sustained_peak()
+    assert kind == "measured" and sust == peaks["bf16_tflops_sustained"]
+    assert sust < bench.load_peaks()[0]

@@ -40,6 +40,9 @@ def test_bench_line_keys(order):
     rf = d["roofline"]
     assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
+    sp = d["vs_sustained_peak"]  # the same rates against the seconds-long (power-capped) bf16 rate
+    assert 0 < sp["peak"] <= rf["peak"] and abs(sp["frac"] - d["value"] / sp["peak"]) < 1e-3
+    assert abs(sp["fwd_frac"] - d["fwd_tflops"] / sp["peak"]) < 1e-3
     e = d["e2e"]
     n = 8 * 6 * 256 * 64 * 2
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * n and e["d2h_bytes_per_step"] == 4 * n + 8 * 6 * 256 * 4
