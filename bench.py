@@ -21,6 +21,10 @@ conversion). Prints ONE JSON line (rank 0).
   per launch over its mean CUDA-event duration, against the measured bf16 peak.
 * cpu_baseline: the CPU oracle timed on this host on a bounded sample (whole heads of
   the same workload until about 10 s of work), as it stands.
+* parity_receipt: before anything is timed, one step of the same shape on the GPU is
+  compared with that oracle run on the sampled heads (the tests' bars); a failed receipt
+  ends the run without a line. Warm-up, timed steps and the end-to-end measurement run
+  under an exclusive file lock per GPU, so that two runs never time one device at once.
 * --impl reference: the CPU oracle as the reference arm (the pages publish no code
   that runs here), each step a bounded sample of the workload.
 
@@ -213,26 +217,89 @@ class NvmlClockSampler:
                 "samples": len(self.samples), "source": "NVML, every ~1 ms during the timed region"}
 
 
-def oracle_sample(w, n_heads, x=None, budget_s=None):
-    """Runs the CPU oracle fwd + bwd on up to n_heads heads (stopping once budget_s seconds
-    have passed, after at least one head); returns (credited FLOPs, seconds, heads run)."""
+def oracle_sample(w, n_heads, x=None, budget_s=None, H_kv=None):
+    """Runs the CPU oracle fwd + bwd on up to n_heads query heads (stopping once budget_s
+    seconds have passed, after at least one head); with H_kv key/value heads in x, query
+    head h uses key/value head h // (H / H_kv). Returns (credited FLOPs, seconds, heads
+    run, {(b, h): (O, LSE, dQ, dK, dV) of that head}), dK and dV being that query head's
+    contribution to its key/value head."""
     import numpy as np  # noqa: F401
     import oracle
     import seeded_inputs as si
     x = x or si.make_inputs(w)
+    G = w.H // (H_kv or w.H)
     heads = [(i // w.H % w.B, i % w.H) for i in range(n_heads)]
     q, k, v, do = (si.bf16_bits_to_f64(x[n]) for n in ("q", "k", "v", "do"))
     t0 = time.perf_counter()
-    done = 0
+    outs = {}
     for b, h in heads:
-        oracle.head_forward(q[b, h], k[b, h], v[b, h], w.scale, w.causal)
-        oracle.head_backward(q[b, h], k[b, h], v[b, h], do[b, h], w.scale, w.causal)
-        done += 1
+        g = h // G
+        o, lse, _ = oracle.head_forward(q[b, h], k[b, g], v[b, g], w.scale, w.causal)
+        dq, dk, dv, _ = oracle.head_backward(q[b, h], k[b, g], v[b, g], do[b, h], w.scale, w.causal)
+        outs[(b, h)] = (o, lse, dq, dk, dv)
         if budget_s is not None and time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     fwd, bwd = credited_flops(1, 1, w.T, w.d)
-    return (fwd + bwd) * (1.0 if w.causal else 2.0) * done, dt, done
+    return (fwd + bwd) * (1.0 if w.causal else 2.0) * len(outs), dt, len(outs), outs
+
+
+# The bars a timed line must pass first (the tests' tolerances): O max-abs and rel-RMS,
+# LSE max-abs, and rel-RMS of each gradient, over the heads the oracle sampled.
+RECEIPT_BARS = {"o_max_abs": 2e-2, "o_rel_rms": 5e-3, "lse_max_abs": 1e-3, "grad_rel_rms": 1e-2}
+
+
+def parity_receipt(gpu, ref, G=1):
+    """Compares GPU outputs with the oracle's on the sampled heads. gpu and ref map (b, h)
+    to (O, LSE, dQ, dK, dV) (fp64 arrays; dK and dV of the GPU are those of the head's
+    key/value head). A key/value head's dK and dV are compared only when all G query heads
+    that use it were sampled (their contributions summed). Returns the receipt dict."""
+    import numpy as np
+
+    def rel(a, b):
+        return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+    keys = sorted(ref)
+    cat = lambda src, i: np.concatenate([np.ravel(src[key][i]) for key in keys])
+    o_g, o_r = cat(gpu, 0), cat(ref, 0)
+    l_g, l_r = cat(gpu, 1), cat(ref, 1)
+    r = {"heads": len(keys), "o_max_abs": float(np.max(np.abs(o_g - o_r))), "o_rel_rms": rel(o_g, o_r),
+         "lse_max_abs": float(np.max(np.abs(l_g - l_r))), "dq_rel_rms": rel(cat(gpu, 2), cat(ref, 2))}
+    groups = {}
+    for b, h in keys:
+        groups.setdefault((b, h // G), []).append((b, h))
+    full = [kv for kv, hs in groups.items() if len(hs) == G]
+    if full:
+        for i, name in ((3, "dk_rel_rms"), (4, "dv_rel_rms")):
+            g_ = np.concatenate([np.ravel(gpu[groups[kv][0]][i]) for kv in full])
+            r_ = np.concatenate([np.ravel(sum(ref[hk][i] for hk in groups[kv])) for kv in full])
+            r[name] = rel(g_, r_)
+    bars = RECEIPT_BARS
+    r["pass"] = bool(r["o_max_abs"] <= bars["o_max_abs"] and r["o_rel_rms"] <= bars["o_rel_rms"]
+                     and r["lse_max_abs"] <= bars["lse_max_abs"]
+                     and all(r[k] <= bars["grad_rel_rms"] for k in ("dq_rel_rms", "dk_rel_rms", "dv_rel_rms") if k in r))
+    return r
+
+
+class GpuLock:
+    """An exclusive file lock per GPU around the timed work, so that two runs of this
+    bench never time the same device at once (released when the process exits)."""
+
+    def __init__(self, index):
+        self.path = os.path.join(tempfile.gettempdir(), f"causal_attention_gb300.gpu{index}.lock")
+        self.fd = None
+
+    def __enter__(self):
+        import fcntl
+        self.fd = open(self.path, "w")
+        fcntl.flock(self.fd, fcntl.LOCK_EX)
+        return self
+
+    def __exit__(self, *exc):
+        import fcntl
+        fcntl.flock(self.fd, fcntl.LOCK_UN)
+        self.fd.close()
+        return False
 
 
 def blas_threads():
@@ -258,7 +325,7 @@ def run_reference(args, rank, world):
         oracle_sample(w, heads_per_step, x)
     flops = secs = 0.0
     for _ in range(args.steps):
-        f, s, _ = oracle_sample(w, heads_per_step, x)
+        f, s, _, _ = oracle_sample(w, heads_per_step, x)
         flops += f
         secs += s
     value = flops / secs / 1e12
@@ -502,6 +569,31 @@ def run_ours(args, rank, world, local):
         if ev is not None:
             ev[len(KERNELS)].record(stream)
 
+    lock = GpuLock(local).__enter__()  # held until the end-to-end measurement is done
+    cpu = receipt = None
+    if world == 1 and not args.no_cpu_baseline:
+        # A parity receipt at this exact shape before anything is timed: one step on the
+        # first buffer set against the CPU oracle on the heads its bounded sample reaches
+        # (whole heads until about 10 s of CPU work; that run is also the cpu_baseline).
+        import numpy as np
+        s0 = sets[0]
+        if args.order == "bwd-fwd":
+            launch["fwd"](s0)
+        step(s0)
+        torch.cuda.synchronize()
+        ca.check_device_error(stream)
+        f, sec, n_heads, ref = oracle_sample(wr, B * H, x, budget_s=10.0, H_kv=H_kv)
+        G = H // H_kv
+        host = lambda t: t.float().cpu().numpy().astype(np.float64)
+        gpu = {(b, h): tuple(host(s0[n][b, h]) for n in ("o", "lse", "dq")) +
+               tuple(host(s0[n][b, h // G]) for n in ("dk", "dv")) for b, h in ref}
+        receipt = parity_receipt(gpu, ref, G)
+        if not receipt["pass"]:
+            print(json.dumps({"error": "parity receipt failed: nothing was timed", "parity_receipt": receipt}),
+                  file=sys.stderr, flush=True)
+            raise SystemExit(1)
+        cpu = {"value": f / sec / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n_heads} of {B * H} heads, fwd+bwd, fp64 numpy oracle, {sec:.1f} s"}
     if args.order == "bwd-fwd":  # every set's O and LSE exist before its first backward
         for s in sets:
             launch["fwd"](s)
@@ -599,6 +691,7 @@ def run_ours(args, rank, world, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     ca.check_device_error(stream)
     e2e_value = whole_job_tflops(step_flops, args.e2e_steps, world, e2e_s)
+    lock.__exit__(None, None, None)
 
     if rank != 0:
         dist.destroy_process_group()
@@ -628,12 +721,6 @@ def run_ours(args, rank, world, local):
     bwd_tf = bwd_f * (1.0 if causal else 2.0) / (bwd_ms * 1e-3) / 1e12
 
     sust_tf, sust_kind = sustained_peak()
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        # a bounded sample: whole heads until about 10 s of CPU work
-        f, s, n_heads = oracle_sample(wr, B * H, x, budget_s=10.0)
-        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{n_heads} of {B * H} heads, fwd+bwd, fp64 numpy oracle, {s:.1f} s"}
 
     line = {
         "metric": "causal attention fwd+bwd TFLOP/s (bf16) and % of GB300 dense BF16 peak",
@@ -652,6 +739,7 @@ def run_ours(args, rank, world, local):
         "kernels": kernels,
         "roofline": roofline,
         "cpu_baseline": cpu,
+        "parity_receipt": receipt,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps},
         "gpu_launches": launches_per_step * args.steps,

@@ -94,3 +94,69 @@ def test_sustained_peak_is_the_measured_one():
     sust, kind = bench.sustained_peak()
     assert kind == "measured" and sust == peaks["bf16_tflops_sustained"]
     assert sust < bench.load_peaks()[0]
+
+
+def _heads(seed, H, H_kv, T=40, d=8, bad=None):
+    """Oracle outputs of every head of a tiny problem, as oracle_sample returns them, and
+    the same as 'GPU' outputs (key/value-head dK, dV), optionally with one value wrong."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    q, do = rng.standard_normal((2, H, T, d))
+    k, v = rng.standard_normal((2, H_kv, T, d))
+    G = H // H_kv
+    ref, dk, dv = {}, np.zeros_like(k), np.zeros_like(v)
+    for h in range(H):
+        o, lse, _ = oracle.head_forward(q[h], k[h // G], v[h // G], 0.3, True)
+        dq, dkh, dvh, _ = oracle.head_backward(q[h], k[h // G], v[h // G], do[h], 0.3, True)
+        ref[(0, h)] = (o, lse, dq, dkh, dvh)
+        dk[h // G] += dkh
+        dv[h // G] += dvh
+    gpu = {(0, h): (r[0].copy(), r[1].copy(), r[2].copy(), dk[h // G].copy(), dv[h // G].copy())
+           for (_, h), r in ref.items()}
+    if bad is not None:
+        i, delta = bad
+        gpu[(0, 1)][i][5] += delta
+    return gpu, ref
+
+
+def test_parity_receipt_passes_exact_outputs_and_fails_planted_errors():
+    gpu, ref = _heads(1, 4, 4)
+    r = bench.parity_receipt(gpu, ref)
+    assert r["pass"] and r["heads"] == 4 and r["o_max_abs"] == 0.0 and r["dk_rel_rms"] == 0.0
+    for i, delta in ((0, 0.05), (1, 0.01), (2, 5.0), (3, 5.0), (4, 5.0)):  # O, LSE, dQ, dK, dV
+        g, rf = _heads(1, 4, 4, bad=(i, delta))
+        assert not bench.parity_receipt(g, rf)["pass"], i
+
+
+def test_parity_receipt_sums_grouped_heads():
+    """With 2 query heads per key/value head, dK and dV are compared as the group's sum,
+    and only for groups whose query heads were all sampled."""
+    gpu, ref = _heads(2, 4, 2)
+    r = bench.parity_receipt(gpu, ref, G=2)
+    assert r["pass"] and r["dk_rel_rms"] < 1e-12 and r["dv_rel_rms"] < 1e-12
+    part = {key: ref[key] for key in [(0, 0)]}  # group 0 incomplete: no dK / dV comparison
+    r = bench.parity_receipt({key: gpu[key] for key in part}, part, G=2)
+    assert r["pass"] and "dk_rel_rms" not in r
+
+
+def test_oracle_sample_maps_grouped_heads():
+    """Under grouped key/value heads the CPU sample reads key/value head h // (H / H_kv)."""
+    import numpy as np
+    import seeded_inputs as si
+    w = si.Workload("gqa_sample", 1, 4, 32, 8, seed=5)
+    x = si.make_inputs(w)
+    x = dict(x, k=np.ascontiguousarray(x["k"][:, :2]), v=np.ascontiguousarray(x["v"][:, :2]))
+    f, s, n, outs = bench.oracle_sample(w, 4, x, H_kv=2)
+    assert n == 4 and sorted(outs) == [(0, 0), (0, 1), (0, 2), (0, 3)] and f > 0
+
+
+def test_gpu_lock_is_exclusive(tmp_path, monkeypatch):
+    import fcntl
+    monkeypatch.setattr(bench.tempfile, "gettempdir", lambda: str(tmp_path))
+    with bench.GpuLock(7) as lk:
+        with open(lk.path, "w") as other:
+            with pytest.raises(BlockingIOError):
+                fcntl.flock(other, fcntl.LOCK_EX | fcntl.LOCK_NB)
+    with open(lk.path, "w") as other:  # released on exit
+        fcntl.flock(other, fcntl.LOCK_EX | fcntl.LOCK_NB)

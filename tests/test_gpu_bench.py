@@ -76,3 +76,18 @@ def test_bench_block_line_keys():
     assert d["e2e"]["d2h_bytes_per_step"] > 0 and d["gpu_launches"] > 0
     rf = d["roofline"]
     assert rf["peak"] > 0 and abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("extra", [(), ("--kv-heads", "2")])
+def test_bench_line_carries_a_passing_parity_receipt(extra):
+    """With the CPU leg on, the line carries the receipt of a step at the same shape checked
+    against the oracle before timing (every head of gpt12m fits the sample), and the
+    cpu_baseline from that oracle run; with grouped key/value heads too."""
+    d = _line(_bench("--workload", "gpt12m", "--steps", "5", "--warmup", "3", "--e2e-steps", "3", *extra))
+    r = d["parity_receipt"]
+    assert r["pass"] and r["heads"] == 8 * 6, r
+    assert all(k in r for k in ("o_max_abs", "o_rel_rms", "lse_max_abs", "dq_rel_rms", "dk_rel_rms", "dv_rel_rms"))
+    assert r["o_rel_rms"] <= 5e-3 and r["dk_rel_rms"] <= 1e-2
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and "48 of 48 heads" in cb["sample"]
