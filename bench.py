@@ -320,12 +320,15 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     x = si.make_inputs(w)
+    H_kv = args.kv_heads or w.H  # the same key/value heads as our arm: the first H_kv slices
+    if H_kv != w.H:
+        x = dict(x, k=x["k"][:, :H_kv].copy(), v=x["v"][:, :H_kv].copy())
     heads_per_step = 1
     for _ in range(args.warmup if w.T <= 2048 else 0):
-        oracle_sample(w, heads_per_step, x)
+        oracle_sample(w, heads_per_step, x, H_kv=H_kv)
     flops = secs = 0.0
     for _ in range(args.steps):
-        f, s, _, _ = oracle_sample(w, heads_per_step, x)
+        f, s, _, _ = oracle_sample(w, heads_per_step, x, H_kv=H_kv)
         flops += f
         secs += s
     value = flops / secs / 1e12
@@ -334,7 +337,7 @@ def run_reference(args, rank, world):
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "causal": w.causal,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": H_kv, "T": w.T, "d": w.d, "causal": w.causal,
                    "parallelism": "replicas", "sample": f"{heads_per_step} head(s) per step"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": f"{heads_per_step} head of {w.B * w.H} per step, fp64 numpy oracle"},
@@ -345,11 +348,15 @@ def run_reference(args, rank, world):
 
 
 def variant(w, args):
-    """The workload as the flags change it (no causal mask; another head dimension)."""
+    """The workload as the flags change it (no causal mask; another head dimension; fewer
+    key/value heads), renamed so that its traffic records are its own."""
     if args.non_causal:  # renamed: its kernels and traffic differ from the causal workload's
         w = w.with_(name=f"{w.name}_noncausal", causal=False)
     if args.head_dim and args.head_dim != w.d:
         w = w.with_(name=f"{w.name}_d{args.head_dim}", d=args.head_dim)
+    kv = getattr(args, "kv_heads", None)
+    if kv and kv != w.H:
+        w = w.with_(name=f"{w.name}_kv{kv}")
     return w
 
 

@@ -53,6 +53,9 @@ def test_variants_are_renamed():
     assert v.name == "long8k_noncausal_d80" and not v.causal and v.d == 80 and v.T == w.T
     same = bench.variant(w, argparse.Namespace(non_causal=False, head_dim=128))
     assert same.name == "long8k" and same.d == 128
+    kv = bench.variant(w, argparse.Namespace(non_causal=False, head_dim=None, kv_heads=1))
+    assert kv.name == "long8k_kv1" and kv.H == w.H and kv.seed == w.seed
+    assert bench.variant(w, argparse.Namespace(non_causal=False, head_dim=None, kv_heads=16)).name == "long8k"
 
 
 def test_spread():
