@@ -503,6 +503,53 @@ def test_long_sequence_prefix_and_sampled_rows(d, sigma):
     assert gu.max_abs(got, want) <= gu.TOL_O_MAX_ABS and gu.rel_rms(got, want) <= gu.TOL_O_REL_RMS
 
 
+@pytest.mark.parametrize("d,T,causal", [(128, 131072, True), (64, 131072, True), (128, 8000, False), (64, 8000, False)])
+def test_uniform_attention_closed_form(d, T, causal):
+    """Q = 0 makes every visible weight equal, so the results have closed forms on every
+    row: O_i is the mean of the visible V rows, LSE_i the log of their count n_i (i + 1
+    causal, T without the mask), dV_j the sum of dO_i / n_i over the queries that see key
+    j, and dK = scale dS^T Q is exactly zero. Every row at T = 131072 causal (1024 key
+    tiles of uniform accumulation) and at a ragged T = 8000 without the mask (the 64 padded
+    keys of the last tile must not count: LSE would read ln 8064). dQ on sampled rows from
+    its definition, dQ_i = scale sum_j P_ij (dO_i . v_j - D_i) k_j."""
+    import causal_attention_gb300 as ca
+    B, H = 1, 2
+    seed = 9500 + d + int(causal)
+    kb, vb, dob = (si.normal_bf16_bits(seed, i, (B, H, T, d)) for i in (1, 2, 3))
+    qb = np.zeros_like(kb)
+    scale = 1.0 / np.sqrt(d)
+    q, k, v, do = (gu.to_device(b) for b in (qb, kb, vb, dob))
+    o, lse = ca.forward(q, k, v, scale, causal)
+    dq, dk, dv = ca.backward(q, k, v, o, do, lse, scale, causal)
+    ca.check_device_error()
+    assert torch.count_nonzero(dk).item() == 0, "dK must be exactly zero when Q = 0"
+    kf, vf, dof = (si.bf16_bits_to_f64(b)[0] for b in (kb, vb, dob))  # [H, T, d]
+    n = np.arange(1, T + 1, dtype=np.float64) if causal else np.full(T, float(T))
+    if causal:
+        ro = np.cumsum(vf, axis=1) / n[None, :, None]
+        rdv = np.cumsum((dof / n[None, :, None])[:, ::-1], axis=1)[:, ::-1]
+    else:
+        ro = np.broadcast_to(vf.mean(axis=1, keepdims=True), vf.shape)
+        rdv = np.broadcast_to((dof / n[None, :, None]).sum(axis=1, keepdims=True), vf.shape)
+    rlse = np.broadcast_to(np.log(n)[None, :], (H, T))
+    go, gl, gdv = gu.to_f64(o[0]), gu.to_f64(lse[0]), gu.to_f64(dv[0])
+    err = {"o": (gu.max_abs(go, ro), gu.rel_rms(go, ro)), "lse": (gu.max_abs(gl, rlse), 0.0),
+           "dv": (gu.max_abs(gdv, rdv), gu.rel_rms(gdv, rdv))}
+    rows = [0, 1, 127, 128, 4095, T // 2 + 3, T - 65, T - 1]
+    gdq = gu.to_f64(dq[0, :, rows])
+    rdq = np.empty_like(gdq)
+    for h in range(H):
+        for r, i in enumerate(rows):
+            vis = slice(0, i + 1) if causal else slice(0, T)
+            dp = vf[h, vis] @ dof[h, i]
+            rdq[h, r] = scale / n[i] * ((dp - dof[h, i] @ ro[h, i]) @ kf[h, vis])
+    err["dq"] = (gu.max_abs(gdq, rdq), gu.rel_rms(gdq, rdq))
+    print({k_: tuple(f"{e:.2e}" for e in v_) for k_, v_ in err.items()})
+    assert err["o"][0] <= gu.TOL_O_MAX_ABS and err["o"][1] <= gu.TOL_O_REL_RMS, err["o"]
+    assert err["lse"][0] <= gu.TOL_LSE_MAX_ABS, err["lse"]
+    assert err["dv"][1] <= gu.TOL_GRAD_REL_RMS and err["dq"][1] <= gu.TOL_GRAD_REL_RMS, (err["dv"], err["dq"])
+
+
 def test_head_dim_80_at_gpt205m_shape():
     """d = 80 at the B4 H16 T2048 shape (the same seeded distributions as that workload),
     compared with the oracle on sampled heads."""
